@@ -1,0 +1,173 @@
+/*
+ * fp64 CPU oracle for multi-head scaled dot-product attention (forward).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is compiled into a host library that
+ * the tests, the package's smoke check and the bench's CPU-baseline leg load to
+ * check the CUDA path.  The product path never links, loads or calls it, and it
+ * shares no code, header or constant with the CUDA sources.
+ *
+ * What it computes, per (batch b, head h, query row i), following
+ * "Attention Is All You Need" as explained on the pages
+ *   - trishampatil.com, "Scaled Dot-Product Attention: Step by Step"
+ *     (Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V, steps 1-4) and
+ *     "Why Masking Is Required" (illegal logits set to -inf, exp(-inf) = 0);
+ *   - aicomputerinstitute.com, "Worked example: attention weights and
+ *     outputs by hand" (the same four steps on numbers);
+ *   - alexdo.xyz, "Decoder block" (causal: position i sees positions <= i;
+ *     cross-attention T x S) and "Two masks, not one" (padded slots get -inf);
+ *   - aicassindra.com, "Pitfalls when reproducing the paper" (padding masks
+ *     keys, not queries; a row with every key masked would be NaN).
+ *
+ *   0. len_b = clamp(key_lengths[b], 0, Lk) when a padding bit is set.
+ *   1. QUERY_PADDING and i >= len_b: the row is padding, output +0.  Stop.
+ *   2. Allowed keys A_i = { j < Lk : (!CAUSAL or j <= i) and
+ *                                    (!KEY_PADDING or j < len_b) }.
+ *   3. A_i empty: output +0 (the pages leave this row undefined -- NaN -- and
+ *      ask that no query attend to nothing; zero is the convention here).
+ *   4. s_j = scale * sum_c q[i,c] k[j,c]                (step 1 and step 2)
+ *   5. w_j = exp(s_j - m) / sum_{j' in A_i} exp(s_j' - m),  m = max s_j
+ *      (step 3; subtracting the row max leaves the quotient unchanged).
+ *      Keys outside A_i have weight exactly 0 (exp(-inf) = 0).
+ *   6. out[i,c] = sum_{j in A_i} w_j v[j,c]             (step 4)
+ *
+ * Every product and sum is in IEEE double, in index order, one row at a time.
+ * Inputs are read in their stored type (double, float or bfloat16 bits) and
+ * widened exactly to double.  Rows are independent; OpenMP spreads them over
+ * host threads without changing any row's arithmetic.
+ *
+ * Layouts: q [B,H,Lq,dk], k [B,H,Lk,dk], v [B,H,Lk,dv], all contiguous.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_IN_F64 = 0, ORACLE_IN_F32 = 1, ORACLE_IN_BF16 = 2 };
+enum { ORACLE_CAUSAL = 1, ORACLE_KEY_PADDING = 2, ORACLE_QUERY_PADDING = 4 };
+
+static double widen(const void *base, int in_dtype, int64_t idx) {
+  if (in_dtype == ORACLE_IN_F64) return ((const double *)base)[idx];
+  if (in_dtype == ORACLE_IN_F32) return (double)((const float *)base)[idx];
+  /* bfloat16: the upper half of a float32 */
+  uint32_t u = (uint32_t)((const uint16_t *)base)[idx] << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/*
+ * Computes the rows listed in `rows` (flat index (b*H + h)*Lq + i), or every
+ * row in order when rows == NULL (then nrows must be B*H*Lq).
+ *   out     [nrows, dv]           attention output rows
+ *   weights [nrows, Lk] or NULL   softmax weights (0 outside A_i)
+ *   scores  [nrows, Lk] or NULL   scaled logits s_j (-inf outside A_i)
+ * Returns 0 on success, 1 on an invalid argument.
+ */
+int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtype,
+                        int B, int H, int Lq, int Lk, int dk, int dv,
+                        int mask_kind, const int32_t *key_lengths, double scale,
+                        const int64_t *rows, int64_t nrows,
+                        double *out, double *weights, double *scores, int nthreads) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk < 0 || dv < 0) return 1;
+  if (in_dtype < ORACLE_IN_F64 || in_dtype > ORACLE_IN_BF16) return 1;
+  if (mask_kind & ~(ORACLE_CAUSAL | ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) return 1;
+  if ((mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)) && Lq != Lk) return 1;
+  if ((mask_kind & (ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) && key_lengths == NULL && B > 0)
+    return 1;
+  const int64_t total = (int64_t)B * H * Lq;
+  if (rows == NULL && nrows != total) return 1;
+  if (nrows < 0) return 1;
+  for (int64_t r = 0; rows != NULL && r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= total) return 1;
+  if (nthreads <= 0) nthreads = oracle_max_threads();
+
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(Lk > 0 ? Lk : 1));
+    char *allowed = (char *)malloc((size_t)(Lk > 0 ? Lk : 1));
+    if (s == NULL || allowed == NULL) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 8)
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (s == NULL || allowed == NULL) continue;
+      const int64_t row = rows ? rows[r] : r;
+      const int64_t bh = row / Lq;
+      const int i = (int)(row % Lq);
+      const int b = (int)(bh / H);
+      double *o = out + r * dv;
+      double *w = weights ? weights + r * Lk : NULL;
+      double *sc = scores ? scores + r * Lk : NULL;
+
+      /* step 0 */
+      int len_b = Lk;
+      if (mask_kind & (ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) {
+        int32_t l = key_lengths[b];
+        len_b = l < 0 ? 0 : (l > Lk ? Lk : (int)l);
+      }
+      for (int c = 0; c < dv; ++c) o[c] = 0.0;
+      for (int j = 0; j < Lk; ++j) {
+        if (w) w[j] = 0.0;
+        if (sc) sc[j] = -INFINITY;
+      }
+      /* step 1 */
+      if ((mask_kind & ORACLE_QUERY_PADDING) && i >= len_b) continue;
+      /* step 2 */
+      int n_allowed = 0;
+      for (int j = 0; j < Lk; ++j) {
+        int ok = 1;
+        if ((mask_kind & ORACLE_CAUSAL) && j > i) ok = 0;
+        if ((mask_kind & ORACLE_KEY_PADDING) && j >= len_b) ok = 0;
+        allowed[j] = (char)ok;
+        n_allowed += ok;
+      }
+      /* step 3 */
+      if (n_allowed == 0) continue;
+      /* step 4 */
+      const int64_t qbase = row * dk;
+      const int64_t kbase = bh * (int64_t)Lk * dk;
+      const int64_t vbase = bh * (int64_t)Lk * dv;
+      for (int j = 0; j < Lk; ++j) {
+        if (!allowed[j]) continue;
+        double dot = 0.0;
+        for (int c = 0; c < dk; ++c)
+          dot += widen(q, in_dtype, qbase + c) * widen(k, in_dtype, kbase + (int64_t)j * dk + c);
+        s[j] = scale * dot;
+        if (sc) sc[j] = s[j];
+      }
+      /* step 5 */
+      double m = -INFINITY;
+      for (int j = 0; j < Lk; ++j)
+        if (allowed[j] && s[j] > m) m = s[j];
+      double denom = 0.0;
+      for (int j = 0; j < Lk; ++j)
+        if (allowed[j]) {
+          s[j] = exp(s[j] - m);
+          denom += s[j];
+        }
+      /* step 6 */
+      for (int j = 0; j < Lk; ++j) {
+        if (!allowed[j]) continue;
+        const double wj = s[j] / denom;
+        if (w) w[j] = wj;
+        for (int c = 0; c < dv; ++c) o[c] += wj * widen(v, in_dtype, vbase + (int64_t)j * dv + c);
+      }
+    }
+    free(s);
+    free(allowed);
+  }
+  return bad ? 1 : 0;
+}
