@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-head scaled dot-product attention forward.
+
+One step = one ``mha_fwd`` call (the whole path: load, Q K^T, scale + mask,
+softmax, P V, normalise + store) over one batch of the workload.  Default
+workload: Transformer-base encoder self-attention, bf16, B=256, H=8, L=64,
+d=64, key + query padding with lengths uniform in [8, 64] (HBM-bound; metric
+GB/s).  ``--workload`` picks another (see gen.WORKLOADS); the long causal one
+reports TFLOP/s.
+
+value  device throughput, inputs resident in HBM; K launches captured in one
+       CUDA graph and replayed between CUDA events; consecutive launches read
+       different input sets whose total exceeds 3x the L2 size, so no launch
+       finds its inputs in L2.
+e2e    the same metric through the public call with host buffers: pinned
+       host -> device copies of Q, K, V (and lengths), mha_fwd, device -> host
+       copy of the output, every step, inside the timed region.
+--impl reference   times the fp64 CPU oracle (the only other implementation
+       of this path) on the host cores, on a bounded sample of the workload.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU (the
+(batch, head) pairs are independent; no collective on the data path), weak
+scaling; value = all ranks' work / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gen  # noqa: E402
+
+DEFAULT_WORKLOAD = "enc_pad_bf16_b256_h8_l64_d64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_NAMES = {1: "attn_f32_simt_kernel", 2: "attn_short_tc_kernel", 3: "attn_long_tc_kernel",
+                4: "zero_fill_kernel"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one launch
+# ---------------------------------------------------------------------------
+def algorithmic(spec, lens):
+    """(bytes, flops) one launch must move / compute, from the realised lengths.
+
+    bytes: Q rows that are not query padding, K and V rows that are not key
+    padding, every output row (zeros included), and the lengths.
+    flops: 2 * (d_k + d_v) per allowed (query, key) pair.
+    """
+    B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
+    esz = 4 if spec["dtype"] == "f32" else 2
+    m = spec["mask"]
+    L = np.full(B, Lk, dtype=np.int64) if lens is None else np.clip(lens.astype(np.int64), 0, Lk)
+    q_rows = (np.minimum(L, Lq) if m & gen.MASK_QUERY_PADDING else np.full(B, Lq)).sum() * H
+    kv_rows = (L if m & gen.MASK_KEY_PADDING else np.full(B, Lk)).sum() * H
+    nbytes = esz * (q_rows * dk + kv_rows * (dk + dv) + B * H * Lq * dv)
+    if lens is not None and m & (gen.MASK_KEY_PADDING | gen.MASK_QUERY_PADDING):
+        nbytes += 4 * B
+    pairs = 0
+    for b in range(B):
+        kmax = int(L[b]) if m & gen.MASK_KEY_PADDING else Lk
+        nq = min(int(L[b]), Lq) if m & gen.MASK_QUERY_PADDING else Lq
+        if m & gen.MASK_CAUSAL:
+            i = np.arange(nq)
+            pairs += int(np.minimum(i + 1, kmax).sum())
+        else:
+            pairs += nq * kmax
+    flops = 2 * (dk + dv) * pairs * H
+    return int(nbytes), int(flops)
+
+
+def bound_of(spec):
+    return "tensor" if spec["Lq"] > 128 or spec["Lk"] > 128 else "hbm"
+
+
+def metric_of(spec):
+    if bound_of(spec) == "tensor":
+        return "attention fwd TFLOP/s (long n)", "TFLOP/s"
+    return "attention fwd GB/s (short n)", "GB/s"
+
+
+def throughput(spec, nbytes, flops, seconds):
+    if bound_of(spec) == "tensor":
+        return flops / seconds / 1e12
+    return nbytes / seconds / 1e9
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    csrc = os.path.join(ROOT, "transformer_head_scaled_mha_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("source_digest") != kernel_source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled with nvidia-smi while the GPU is loaded
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []  # (t, sm_mhz, max_mhz, power, reasons)
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(self.NAMES, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, mx, parts[3], reasons))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        if not self.samples:
+            return None
+        t0, t1 = self.window if self.window else (0, float("inf"))
+        inside = [s for s in self.samples if t0 - 0.05 <= s[0] <= t1 + 0.05] or self.samples[-3:]
+        reasons = sorted({r for s in inside for r in s[4]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (torchrun: one rank per GPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Slowest rank's time (all_reduce MAX); identity for one process."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_rows(spec, lens, target_flops, seed=0):
+    """A random sample of query rows whose oracle work is about target_flops."""
+    B, H, Lq = spec["B"], spec["H"], spec["Lq"]
+    total_rows = B * H * Lq
+    _, total_flops = algorithmic(spec, lens)
+    frac = min(1.0, target_flops / max(total_flops, 1))
+    n = max(1, int(total_rows * frac))
+    if n >= total_rows:
+        return None, 1.0
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False)).astype(np.int64)
+    return rows, n / total_rows
+
+
+def time_oracle(spec, q, k, v, lens, rows, threads=0):
+    import oracle
+    scale = gen.default_scale(spec["dk"])
+    t0 = time.perf_counter()
+    oracle.mha_fwd(q, k, v, mask_kind=spec["mask"], key_lengths=lens, scale=scale, rows=rows,
+                   threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(spec, q, k, v, lens, budget_s=12.0):
+    """Oracle throughput on a bounded random row sample, scaled by the sample's
+    share of the rows (rows are independent units of equal expected cost)."""
+    import oracle
+    cores = oracle.max_threads()
+    _, total_flops = algorithmic(spec, lens)
+    # calibrate on a small sample, then size the real sample for the budget
+    probe_rows, probe_frac = oracle_sample_rows(spec, lens, 2e8)
+    t_probe = time_oracle(spec, q, k, v, lens, probe_rows)
+    rate = (total_flops * probe_frac) / max(t_probe, 1e-6)  # oracle flop/s
+    rows, frac = oracle_sample_rows(spec, lens, rate * budget_s, seed=1)
+    t = time_oracle(spec, q, k, v, lens, rows)
+    nbytes, flops = algorithmic(spec, lens)
+    value = throughput(spec, nbytes * frac, flops * frac, t)
+    n_rows = spec["B"] * spec["H"] * spec["Lq"] if rows is None else len(rows)
+    sample = ("%d of %d query rows (%.4g%%), drawn uniformly at random, %.1f s on %d threads; "
+              "work scaled by the sampled share" % (n_rows, spec["B"] * spec["H"] * spec["Lq"],
+                                                     100 * frac, t, cores))
+    return {"value": value, "unit": metric_of(spec)[1], "cores": cores, "kind": "oracle",
+            "sample": sample}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import transformer_head_scaled_mha_gb300 as mha
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    spec = gen.WORKLOADS[args.workload]
+    dt = spec["dtype"]
+    q, k, v, lens = gen.make_inputs(spec, seed=args.seed)
+    nbytes, flops = algorithmic(spec, lens)
+    metric, unit = metric_of(spec)
+    scale = gen.default_scale(spec["dk"])
+    mask = spec["mask"]
+    B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
+    path = mha.mha_fwd_path(B, H, Lq, Lk, dk, dv, mask, 1 if dt == "bf16" else 0)
+    kernel = KERNEL_NAMES.get(path, "?")
+
+    def host_tensor(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.view(torch.bfloat16) if dt == "bf16" else t
+
+    hq, hk, hv = host_tensor(q), host_tensor(k), host_tensor(v)
+    set_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    set_bytes += B * H * Lq * dv * hq.element_size()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes))
+    sets = []
+    for _ in range(n_sets):
+        sets.append((hq.to(dev), hk.to(dev), hv.to(dev),
+                     torch.empty((B, H, Lq, dv), dtype=hq.dtype, device=dev)))
+    kl = torch.from_numpy(lens).to(dev) if lens is not None else None
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s=None):
+        qq, kk, vv, oo = sets[i % n_sets]
+        mha.mha_fwd(qq, kk, vv, oo, mask_kind=mask, key_lengths=kl, scale=scale, stream=s)
+
+    # warm-up (eager): W steps
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+
+    # capture the K timed launches (one graph, one launch per step)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(i, stream)
+        # soak: replay untimed so clocks settle under load before the timed region
+        t_end = time.time() + args.soak
+        while time.time() < t_end:
+            graph.replay()
+            stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(i, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    if t_wall1 - t_wall0 < 0.3:  # keep sampling a little if the region was short
+        time.sleep(0.3)
+    sampler.mark(t_wall0, t_wall1)
+    clocks = sampler.stop()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    elapsed = max_over_ranks(elapsed, world, dev)
+    per_launch = elapsed / args.steps
+    value_rank = throughput(spec, nbytes, flops, per_launch)
+    value = value_rank * world
+    st = mha.mha_debug_status(stream)
+    if st != mha.MHA_OK:
+        raise RuntimeError("device status after timing: %s" % mha.mha_status_string(st))
+
+    # e2e: pinned host buffers, copies inside the timed region
+    pq, pk, pv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
+    pout = torch.empty((B, H, Lq, dv), dtype=hq.dtype).pin_memory()
+    plen = torch.from_numpy(lens).pin_memory() if lens is not None else None
+    dq, dk_, dv_, do = sets[0]
+    dl = torch.empty_like(kl) if kl is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in (pq, pk, pv))
+    h2d += plen.numel() * 4 if plen is not None else 0
+    d2h = pout.numel() * pout.element_size()
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        dq.copy_(pq, non_blocking=True)
+        dk_.copy_(pk, non_blocking=True)
+        dv_.copy_(pv, non_blocking=True)
+        if plen is not None:
+            dl.copy_(plen, non_blocking=True)
+        mha.mha_fwd(dq, dk_, dv_, do, mask_kind=mask, key_lengths=dl, scale=scale, stream=stream)
+        pout.copy_(do, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / e2e_steps
+    e2e_value = throughput(spec, nbytes, flops, e2e_t) * world
+
+    peaks, peak_src = read_peaks()
+    if bound_of(spec) == "tensor":
+        peak, achieved, runit = peaks["bf16_tflops"], flops / per_launch / 1e12, "TFLOP/s"
+    else:
+        peak, achieved, runit = peaks["hbm_gbs"], nbytes / per_launch / 1e9, "GB/s"
+    roofline = {"bound": bound_of(spec), "achieved": round(achieved, 2), "peak": peak,
+                "unit": runit, "frac": round(achieved / peak, 4), "traffic":
+                recorded_traffic(args.workload), "kernel": kernel,
+                "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback", "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(spec, q, k, v, lens, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_launch * 1e3, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": dt, "data": "synthetic (seeded N(0,1)%s inputs, seed %d)" % (
+                "*%g" % spec["amp"] if spec["amp"] != 1.0 else "", args.seed),
+            "config": {"workload": args.workload, "B": B, "H": H, "Lq": Lq, "Lk": Lk,
+                       "d_k": dk, "d_v": dv, "mask_kind": mask,
+                       "len_range": spec["len_range"], "scale": scale,
+                       "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
+                             % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+                       "timing": "CUDA graph of %d launches, CUDA events" % args.steps
+                       if graph is not None else "eager launches, CUDA events",
+                       "parallelism": "weak: same workload per rank, no collective" if world > 1
+                       else "1 GPU"},
+            "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": args.steps,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    spec = gen.WORKLOADS[args.workload]
+    q, k, v, lens = gen.make_inputs(spec, seed=args.seed)
+    metric, unit = metric_of(spec)
+    import oracle
+    oracle.build()
+    nbytes, flops = algorithmic(spec, lens)
+    # each step: one bounded random sample of the workload's rows
+    budget = args.ref_step_budget
+    probe_rows, probe_frac = oracle_sample_rows(spec, lens, 2e8)
+    t_probe = time_oracle(spec, q, k, v, lens, probe_rows)
+    rate = flops * probe_frac / max(t_probe, 1e-6)
+    rows, frac = oracle_sample_rows(spec, lens, rate * budget, seed=2)
+    for _ in range(args.warmup):
+        time_oracle(spec, q, k, v, lens, rows)
+    times = [time_oracle(spec, q, k, v, lens, rows) for _ in range(args.steps)]
+    t = sum(times)
+    value = throughput(spec, nbytes * frac * args.steps, flops * frac * args.steps, t)
+    cores = oracle.max_threads()
+    n_rows = spec["B"] * spec["H"] * spec["Lq"] if rows is None else len(rows)
+    sample = ("each step: %d of %d query rows (%.4g%%), uniform random, scaled by the sampled "
+              "share" % (n_rows, spec["B"] * spec["H"] * spec["Lq"], 100 * frac))
+    line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, seed %d)" % args.seed,
+            "config": {"workload": args.workload, "B": spec["B"], "H": spec["H"],
+                       "Lq": spec["Lq"], "Lk": spec["Lk"], "d_k": spec["dk"], "d_v": spec["dv"],
+                       "mask_kind": spec["mask"], "len_range": spec["len_range"]},
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a graph")
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing, s")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="oracle baseline budget, s")
+    ap.add_argument("--ref-step-budget", type=float, default=2.0, help="reference arm s/step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    world, _, _ = dist_env()
+    if world != args.gpus:
+        if not (world == 1 and args.gpus == 1):
+            print("warning: --gpus %d but WORLD_SIZE %d; using WORLD_SIZE" % (args.gpus, world),
+                  file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,128 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention forward.
+ *
+ * Operation (per batch b, head h, query row i):
+ *
+ *     out[b,h,i,:] = sum_j softmax_j( scale * q[b,h,i,:] . k[b,h,j,:] ) v[b,h,j,:]
+ *
+ * the scaled dot-product attention of "Attention Is All You Need", as stated
+ * on the pages
+ *   trishampatil.com      "Scaled Dot-Product Attention: Step by Step" (the
+ *                         four steps: QK^T, divide by sqrt(d_k), row softmax,
+ *                         weighted sum of V) and "Multi-Head Attention" (h
+ *                         heads, each its own attention of width d_k = d_v);
+ *   trishampatil.com      "Why Masking Is Required" (illegal logits -> -inf);
+ *   alexdo.xyz            "Decoder block" (causal: i sees j <= i;
+ *                         cross-attention: T queries x S keys, not causal)
+ *                         and "Two masks, not one" (padded slots -> -inf);
+ *   aicassindra.com       "A faithful layer in code" (per-head layout
+ *                         [B, h, T, d_k] after the head split) and "Pitfalls
+ *                         when reproducing the paper" (mask keys, not queries;
+ *                         a fully masked row has no defined output).
+ *
+ * Every call enqueues GPU work on `stream` and returns; nothing is allocated,
+ * nothing is synchronised, no host memory is touched besides the arguments.
+ * The library holds no per-call state and is safe to call from several
+ * threads at once.
+ */
+#ifndef MHA_GB300_H
+#define MHA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and out (all four share it). */
+typedef enum {
+  MHA_DTYPE_F32 = 0,  /* float32 in, float32 out; CUDA-core FFMA, no TF32      */
+  MHA_DTYPE_BF16 = 1  /* bfloat16 in, bfloat16 out (round to nearest even);
+                         tensor-core products, float32 accumulation and softmax */
+} mha_dtype;
+
+/* mask_kind is a bit set. */
+enum {
+  MHA_MASK_NONE = 0,
+  /* key j is allowed for query i only if j <= i (decoder self-attention);
+     requires Lq == Lk */
+  MHA_MASK_CAUSAL = 1,
+  /* key j is allowed only if j < key_lengths[b] (padded source slots) */
+  MHA_MASK_KEY_PADDING = 2,
+  /* query rows i >= key_lengths[b] are padding: written as +0.0; requires
+     Lq == Lk (self-attention over one padded sequence) */
+  MHA_MASK_QUERY_PADDING = 4
+};
+/* encoder self-attention over padded sentences: KEY_PADDING | QUERY_PADDING;
+   cross-attention over a padded source: KEY_PADDING; decoder: CAUSAL. */
+
+typedef enum {
+  MHA_OK = 0,
+  MHA_ERR_INVALID_ARGUMENT = 1, /* rejected before any launch              */
+  MHA_ERR_UNSUPPORTED = 2,      /* valid, but no kernel for this shape/type */
+  MHA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed        */
+  MHA_ERR_TIMEOUT = 4           /* a kernel gave up waiting (device status) */
+} mha_status;
+
+/*
+ * mha_fwd -- attention forward, asynchronous on `stream`.
+ *
+ * q    [B, H, Lq, d_k]  device pointer, contiguous row-major, 16-byte aligned
+ * k    [B, H, Lk, d_k]  device pointer, contiguous row-major, 16-byte aligned
+ * v    [B, H, Lk, d_v]  device pointer, contiguous row-major, 16-byte aligned
+ * out  [B, H, Lq, d_v]  device pointer, contiguous row-major, 16-byte aligned;
+ *                       written in full; must not overlap q, k, v or key_lengths
+ * B, H, Lq, Lk          >= 0; a product B*H*Lq of 0 is a no-op; Lk == 0 (no
+ *                       keys at all) writes +0.0 everywhere
+ * d_k, d_v              > 0.  BF16: d_k == d_v, one of 64 or 128.
+ *                       F32: 1..128 each.  Others: MHA_ERR_UNSUPPORTED
+ * mask_kind             MHA_MASK_* bit set (see above)
+ * key_lengths           device pointer to int32[B], required when a padding bit
+ *                       is set (else ignored, may be NULL).  Read on the
+ *                       device; values are clamped to [0, Lk].
+ * scale                 multiplies every logit; pass 1/sqrt(d_k) for the
+ *                       paper's scaling.  Any finite value (0 gives the mean of
+ *                       the allowed values).
+ * dtype                 mha_dtype
+ * stream                cudaStream_t, or NULL for the legacy default stream
+ *
+ * Rows with no allowed key (key_lengths[b] == 0) and query-padding rows are
+ * written as +0.0.  Keys and values at masked positions never influence the
+ * result, provided they hold finite numbers.
+ *
+ * Ownership: every buffer belongs to the caller and must stay valid until the
+ * enqueued work has run.  Errors: validation failures return before anything
+ * is enqueued; MHA_ERR_CUDA reports a failed launch or driver call (the
+ * runtime's sticky error, if any, is left for the caller to read).  Faults and
+ * device-side timeouts surface at the caller's next synchronisation and in
+ * mha_debug_status().
+ */
+int mha_fwd(const void *q, const void *k, const void *v, void *out,
+            int B, int H, int Lq, int Lk, int d_k, int d_v,
+            int mask_kind, const int32_t *key_lengths,
+            float scale, int dtype, void *stream);
+
+/* Which kernel mha_fwd would launch for these arguments:
+   0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed
+   short-sequence tensor-core kernel (Lq, Lk <= 128), 3 = long-sequence
+   tensor-core kernel, 4 = zero fill (Lk == 0); negative = -(mha_status) for
+   arguments mha_fwd would reject.  Host only, launches nothing. */
+int mha_fwd_path(int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind, int dtype);
+
+/* Static text for a status code. */
+const char *mha_status_string(int status);
+
+/* Reads and clears the device-side status word that kernels set when a
+   bounded wait runs out (MHA_ERR_TIMEOUT).  Synchronises `stream`.  Returns
+   MHA_OK, MHA_ERR_TIMEOUT, or MHA_ERR_CUDA if the read itself failed. */
+int mha_debug_status(void *stream);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int mha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_GB300_H */

@@ -1,0 +1,109 @@
+"""The C ABI: the library loads, exports what include/mha.h declares, and
+rejects bad arguments before touching the GPU (these calls never reach CUDA)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mha():
+    import __graft_entry__
+    __graft_entry__._load_build_module().build()
+    import transformer_head_scaled_mha_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mha.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mha_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(
+        ["mha_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version"])
+
+
+def test_library_exports_every_declared_symbol(mha):
+    lib = ctypes.CDLL(mha.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(mha.mha.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings(mha):
+    assert mha.mha_status_string(0) == "ok"
+    assert "invalid" in mha.mha_status_string(1)
+    assert "unsupported" in mha.mha_status_string(2)
+    assert mha.mha_status_string(99) == "unknown status"
+    assert mha.mha_version() >= 100
+
+
+def test_path_selection(mha):
+    P = mha.mha_fwd_path
+    assert P(2, 8, 32, 32, 64, 64, 0, 0) == 1  # fp32
+    assert P(256, 8, 64, 64, 64, 64, 6, 1) == 2  # packed short
+    assert P(128, 8, 128, 128, 64, 64, 1, 1) == 2
+    assert P(64, 16, 96, 128, 64, 64, 2, 1) == 2
+    assert P(4, 16, 8192, 8192, 128, 128, 1, 1) == 3  # long
+    assert P(2, 2, 129, 129, 64, 64, 1, 1) == 3
+    assert P(2, 2, 64, 64, 128, 128, 0, 1) == 3
+    assert P(0, 2, 64, 64, 64, 64, 0, 1) == 0  # empty
+    assert P(2, 2, 64, 0, 64, 64, 0, 1) == 4  # no keys: zero fill
+    assert P(2, 2, 64, 64, 96, 96, 0, 1) == -2  # bf16 d must be 64 or 128
+    assert P(2, 2, 64, 64, 64, 128, 0, 1) == -2
+    assert P(2, 2, 64, 64, 129, 64, 0, 0) == -2
+    assert P(2, 2, 64, 65, 64, 64, 1, 1) == -1  # causal needs Lq == Lk
+    assert P(2, 2, 64, 65, 64, 64, 4, 1) == -1  # query padding needs Lq == Lk
+    assert P(2, 2, 64, 64, 64, 64, 8, 1) == -1  # unknown mask bit
+    assert P(-1, 2, 64, 64, 64, 64, 0, 1) == -1
+    assert P(2, 2, 64, 64, 0, 64, 0, 1) == -1
+    assert P(2, 2, 64, 64, 64, 64, 0, 7) == -1  # unknown dtype
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every call below fails validation first
+
+
+def call(mha, q=FAKE, k=FAKE + (1 << 24), v=FAKE + (2 << 24), out=FAKE + (3 << 24), B=2, H=2,
+         Lq=64, Lk=64, dk=64, dv=64, mask=0, kl=None, scale=0.125, dtype=1):
+    return mha.lib.mha_fwd(q, k, v, out, B, H, Lq, Lk, dk, dv, mask, kl, scale, dtype, None)
+
+
+def test_rejects_before_launch(mha):
+    E_ARG, E_UNS = mha.MHA_ERR_INVALID_ARGUMENT, mha.MHA_ERR_UNSUPPORTED
+    assert call(mha, B=-1) == E_ARG
+    assert call(mha, dk=0) == E_ARG
+    assert call(mha, mask=1, Lk=65) == E_ARG
+    assert call(mha, mask=2) == E_ARG  # key_lengths missing
+    assert call(mha, mask=4) == E_ARG
+    assert call(mha, q=None) == E_ARG
+    assert call(mha, out=None) == E_ARG
+    assert call(mha, k=None) == E_ARG
+    assert call(mha, q=FAKE + 8) == E_ARG  # not 16-byte aligned
+    assert call(mha, out=FAKE + 4096) == E_ARG  # out overlaps q
+    assert call(mha, out=FAKE + (2 << 24) + 64) == E_ARG  # out overlaps v
+    assert call(mha, mask=2, kl=FAKE + (3 << 24) + 128) == E_ARG  # out overlaps key_lengths
+    assert call(mha, scale=math.inf) == E_ARG
+    assert call(mha, scale=math.nan) == E_ARG
+    assert call(mha, dtype=3) == E_ARG
+    assert call(mha, dk=96, dv=96) == E_UNS
+    assert call(mha, dk=64, dv=128) == E_UNS
+    assert call(mha, dtype=0, dk=200) == E_UNS
+
+
+def test_empty_problem_returns_ok_without_device(mha):
+    # B*H*Lq == 0 enqueues nothing, so it succeeds even without a GPU
+    assert call(mha, B=0) == mha.MHA_OK
+    assert call(mha, Lq=0, q=None, out=None) == mha.MHA_OK
+
+
+def test_binding_refuses_cpu_tensors(mha):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mha.mha_fwd(q, q, q)

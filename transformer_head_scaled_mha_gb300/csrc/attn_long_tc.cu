@@ -1,0 +1,410 @@
+// Long-sequence attention on the tcgen05 tensor cores (bf16, d in {64, 128}).
+//
+// One CTA computes 256 query rows of one (batch, head) as two 128-row tiles,
+// one per softmax warpgroup, streaming the keys/values in 128-row tiles:
+//
+//   S_w = Q_w K_j^T          tcgen05.mma, operands from 128B-swizzled smem,
+//                            fp32 accumulator in TMEM (one 128-column buffer
+//                            per warpgroup)
+//   online softmax           tcgen05.ld of S into registers (thread = row),
+//                            scale folded with log2(e), causal / padding mask
+//                            on the tiles that straddle a boundary, running max
+//                            and running sum; exp2 on the MUFU unit
+//   P_w (bf16) -> smem       K-major operand of the next MMA
+//   O_w += P_w V_j           tcgen05.mma into a TMEM accumulator per warpgroup
+//   epilogue                 O / rowsum -> bf16 -> swizzled smem -> TMA store
+//
+// The score matrix never leaves the SM.  While one warpgroup turns its S into
+// P, the tensor core runs the other warpgroup's products (ping-pong).  The
+// running max is only moved (and O rescaled in TMEM) when it grows by more
+// than 2^8, so the rescale is rare; the final division uses the same max for
+// numerator and denominator, so the result is unchanged.  Under a causal mask
+// the tiles above the diagonal are never loaded nor multiplied, which halves
+// the work; CTAs are issued heaviest query block first.
+//
+// Warp roles (320 threads): warps 0-3 softmax WG0, 4-7 softmax WG1, warp 8 TMA
+// producer (K_j, V_j through a ring of smem slots), warp 9 TMEM owner + MMA.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kBM = 128;  // query rows per warpgroup tile
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kWgThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O may grow to 2^8 before a rescale
+
+template <int D>
+struct Cfg {
+  static constexpr int kBlkBytes = 128 * 128;          // one [128 rows x 64] swizzle block
+  static constexpr int kTileBytes = (D / 64) * kBlkBytes;  // a [128 x D] operand tile
+  static constexpr int kSlots = (D == 128) ? 3 : 6;    // K/V ring
+  static constexpr int kPBytes = 2 * kBlkBytes;        // P: [128 x 128] bf16
+  static constexpr size_t kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 2 * kPBytes + 256;
+};
+
+struct __align__(8) Barriers {
+  uint64_t q_full;
+  uint64_t kv_full[6];
+  uint64_t kv_empty[6];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity))
+    if (global_timer_ns() - t0 > 100000000ull) return false;
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_long_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *q_smem = smem;                               // 2 tiles; reused as output staging
+  uint8_t *kv_smem = q_smem + 2 * C::kTileBytes;        // kSlots tiles
+  uint8_t *p_smem = kv_smem + C::kSlots * C::kTileBytes;  // 2 P tiles
+  Barriers *bars = reinterpret_cast<Barriers *>(p_smem + 2 * C::kPBytes);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int nqb = (p.Lq + 2 * kBM - 1) / (2 * kBM);
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / BH;  // heaviest first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int b = bh / p.H;
+  const int q0 = qb * 2 * kBM;
+
+  int len = p.Lk;
+  if (p.mask & (kMaskKeyPadding | kMaskQueryPadding)) {
+    const int l = p.key_lengths[b];
+    len = l < 0 ? 0 : (l > p.Lk ? p.Lk : l);
+  }
+  // keys [0, kv_end_w) matter for warpgroup w; rows [q0 + 128 w, ...) exist?
+  int n_tiles[2];
+  bool wg_rows[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const int r0 = q0 + w * kBM;
+    wg_rows[w] = r0 < p.Lq;
+    int kv_end = p.Lk;
+    if (p.mask & kMaskKeyPadding) kv_end = min(kv_end, len);
+    if (p.mask & kMaskCausal) kv_end = min(kv_end, min(r0 + kBM, p.Lq));
+    n_tiles[w] = wg_rows[w] ? (kv_end + kBN - 1) / kBN : 0;
+  }
+  const int n_kv = max(n_tiles[0], n_tiles[1]);
+
+  // ---- setup -------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->p_full[w], kWgThreads);
+      mbar_init(&bars->pv_done[w], 1);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  int issued = 0;  // producer: K/V loads issued
+  uint64_t *last_commit = nullptr;
+  uint32_t last_parity = 0;
+
+  if (warp == 8) {
+    // ---- TMA producer ------------------------------------------------------
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      uint32_t qbytes = 0;
+      for (int w = 0; w < 2; ++w)
+        if (n_tiles[w] > 0) qbytes += C::kTileBytes;
+      mbar_arrive_expect_tx(&bars->q_full, qbytes);
+      for (int w = 0; w < 2; ++w)
+        if (n_tiles[w] > 0)
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_load_3d(q_smem + w * C::kTileBytes + blk * C::kBlkBytes, &maps.q, &bars->q_full,
+                        blk * 64, q0 + w * kBM, bh);
+      for (int idx = 0; idx < 2 * n_kv; ++idx) {
+        const int slot = idx % C::kSlots, round = idx / C::kSlots;
+        if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, abort_flag)) break;
+        const int j = idx >> 1;
+        const CUtensorMap *map = (idx & 1) ? &maps.v : &maps.k;
+        mbar_arrive_expect_tx(&bars->kv_full[slot], C::kTileBytes);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_3d(kv_smem + slot * C::kTileBytes + blk * C::kBlkBytes, map,
+                      &bars->kv_full[slot], blk * 64, j * kBN, bh);
+        issued = idx + 1;
+      }
+    }
+  } else if (warp == 9) {
+    // ---- MMA issuer (lane 0 issues; the warp waits together) ---------------
+    const uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0);
+    const uint32_t idesc_o = idesc_bf16_f32(128, 64, 1);
+    bool ok = n_kv == 0 || mbar_wait(&bars->q_full, 0, abort_flag);
+    for (int j = 0; ok && j <= n_kv; ++j) {
+      const int ks = (2 * j) % C::kSlots, kr = (2 * j) / C::kSlots;
+      const int vs = (2 * j - 1) % C::kSlots, vr = (2 * j - 1) / C::kSlots;
+      if (j < n_kv && !(ok = mbar_wait(&bars->kv_full[ks], kr & 1, abort_flag))) break;
+      bool v_ready = false;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const bool do_s = j < n_tiles[w];
+        const bool do_pv = j >= 1 && j - 1 < n_tiles[w];
+        if ((do_s || do_pv) && j >= 1 &&
+            !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag)))
+          break;
+        if (do_pv && !v_ready) {
+          if (!(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag))) break;
+          v_ready = true;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          if (do_s) {
+            const uint32_t sq = smem_addr(q_smem + w * C::kTileBytes);
+            const uint32_t sk = smem_addr(kv_smem + ks * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kBlkBytes + (kk & 3) * 32;
+              tc_mma_ss(tmem + w * 128, smem_desc_sw128(sq + off, 16, 1024),
+                        smem_desc_sw128(sk + off, 16, 1024), idesc_s, kk > 0);
+            }
+            tc_commit(&bars->s_full[w]);
+          }
+          if (do_pv) {
+            const uint32_t sp = smem_addr(p_smem + w * C::kPBytes);
+            const uint32_t sv = smem_addr(kv_smem + vs * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              const uint64_t da =
+                  smem_desc_sw128(sp + (kk >> 2) * C::kBlkBytes + (kk & 3) * 32, 16, 1024);
+#pragma unroll
+              for (int nb = 0; nb < D / 64; ++nb) {
+                const uint64_t db =
+                    smem_desc_sw128(sv + nb * C::kBlkBytes + kk * 16 * 128, 1024, 1024);
+                tc_mma_ss(tmem + 256 + w * 128 + nb * 64, da, db, idesc_o, (j - 1 > 0) || kk > 0);
+              }
+            }
+            tc_commit(&bars->pv_done[w]);
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (j < n_kv) {
+          tc_commit(&bars->kv_empty[ks]);
+          last_commit = &bars->kv_empty[ks];
+          last_parity = kr & 1;
+        }
+        if (j >= 1) {
+          tc_commit(&bars->kv_empty[vs]);
+          last_commit = &bars->kv_empty[vs];
+          last_parity = vr & 1;
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---- softmax warpgroups --------------------------------------------------
+    const int w = warp >> 2;           // warpgroup
+    const int r = threadIdx.x & 127;   // row within the tile (TMEM lane)
+    const int i = q0 + w * kBM + r;    // query row
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_base + w * 128;
+    const uint32_t o_tmem = tmem + lane_base + 256 + w * 128;
+    const int nt = n_tiles[w];
+    int jmax = p.Lk;  // keys j < jmax are allowed for row i
+    if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
+    if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
+    const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
+
+    float m_use = -INFINITY;  // max used for the exponentials (log2 units)
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!(ok = mbar_wait(&bars->s_full[w], j & 1, abort_flag))) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, sr[ch]);
+      tmem_wait_ld();
+
+      const int lim = jmax - j * kBN;  // columns c < lim are allowed
+      const bool need_mask = __any_sync(0xffffffffu, lim < kBN);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(sr[ch][e]) * p.scale_log2;
+          if (need_mask && ch * 32 + e >= lim) x = -INFINITY;
+          sr[ch][e] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      const float m_new = fmaxf(m_use, mt);
+      float alpha = 1.f;
+      if (m_new > m_use + kRescaleThreshold) {
+        if (m_use != -INFINITY) alpha = ex2_approx(m_use - m_new);
+        m_use = m_new;
+      }
+      l_run *= alpha;
+      const bool live = m_use != -INFINITY;
+      float rs = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float pe = live ? ex2_approx(__uint_as_float(sr[ch][e]) - m_use) : 0.f;
+          rs += pe;
+          sr[ch][e] = __float_as_uint(pe);
+        }
+      l_run += rs;
+
+      // P_w(j-1) V_{j-1} must be done: it reads the P buffer and writes O
+      if (j >= 1) {
+        if (!(ok = mbar_wait(&bars->pv_done[w], (j - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+      }
+      const uint32_t sp = smem_addr(p_smem + w * C::kPBytes);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            wv[t] = pack_bf16x2(__uint_as_float(sr[ch][q4 * 8 + 2 * t]),
+                                __uint_as_float(sr[ch][q4 * 8 + 2 * t + 1]));
+          const int c16 = ch * 4 + q4;
+          st_shared_v4(sp + (c16 >> 3) * C::kBlkBytes + sw128_offset(r, c16 & 7), wv[0], wv[1],
+                       wv[2], wv[3]);
+        }
+      // the running max moved: rescale this row of O (rare, warp-wide)
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(o_tmem + ch * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(o_tmem + ch * 32, o);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[w]);
+    }
+
+    // ---- epilogue: O / l -> bf16 -> staging (this warpgroup's Q tile) -> TMA
+    if (ok && wg_rows[w]) {
+      const bool zero_row = qpad || l_run == 0.f || nt == 0;
+      const float inv = zero_row ? 0.f : 1.f / l_run;
+      if (nt > 0) {
+        ok = mbar_wait(&bars->pv_done[w], (nt - 1) & 1, abort_flag);
+        tc_fence_after();
+      }
+      if (ok) {
+        uint8_t *stage = q_smem + w * C::kTileBytes;
+        const uint32_t so = smem_addr(stage);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          if (nt > 0) {
+            tmem_ld32(o_tmem + ch * 32, o);
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float a0 = zero_row ? 0.f : __uint_as_float(o[q4 * 8 + 2 * t]) * inv;
+              const float a1 = zero_row ? 0.f : __uint_as_float(o[q4 * 8 + 2 * t + 1]) * inv;
+              wv[t] = pack_bf16x2(a0, a1);
+            }
+            const int c16 = ch * 4 + q4;  // 16-byte piece within the row
+            st_shared_v4(so + (c16 >> 3) * C::kBlkBytes + sw128_offset(r, c16 & 7), wv[0],
+                         wv[1], wv[2], wv[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1 + w, kWgThreads);
+        if (r == 0) {
+          for (int blk = 0; blk < D / 64; ++blk)
+            tma_store_3d(&maps.o, stage + blk * C::kBlkBytes, blk * 64, q0 + w * kBM, bh);
+          tma_store_commit();
+          tma_store_wait0();
+        }
+      }
+    }
+  }
+
+  // ---- teardown --------------------------------------------------------------
+  if (*abort_flag && warp == 8 && lane == 0) {
+    for (int idx = issued - C::kSlots; idx < issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->kv_full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    if (n_kv > 0) (void)wait_teardown(&bars->q_full, 0);
+  }
+  if (*abort_flag && warp == 9 && lane == 0 && last_commit != nullptr)
+    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+cudaError_t launch_long_impl(const LongMaps &maps, const Problem &p, cudaStream_t stream) {
+  static_assert(Cfg<D>::kSmem <= 232448, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(attn_long_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg<D>::kSmem));
+  if (e != cudaSuccess) return e;
+  const int nqb = (p.Lq + 2 * kBM - 1) / (2 * kBM);
+  const long long grid = static_cast<long long>(p.B) * p.H * nqb;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  attn_long_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmem, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
+                           cudaStream_t stream) {
+  (void)num_sms;
+  if (p.dk == 128) return launch_long_impl<128>(maps, p, stream);
+  return launch_long_impl<64>(maps, p, stream);
+}
+
+}  // namespace mha

@@ -1,0 +1,60 @@
+// Shared definitions between the host dispatcher and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mha {
+
+constexpr int kMaskCausal = 1;
+constexpr int kMaskKeyPadding = 2;
+constexpr int kMaskQueryPadding = 4;
+
+constexpr int kStatusOk = 0;
+constexpr int kStatusTimeout = 4;
+
+// A bounded wait gives up after this much wall time.  Every wait in these
+// kernels normally completes within microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// log2(e): softmax is evaluated as exp2(x * scale * log2(e) - m)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Problem description handed to every kernel by value.
+struct Problem {
+  int B, H, Lq, Lk, dk, dv;
+  int mask;
+  const int32_t *key_lengths;  // device [B] or nullptr
+  float scale_log2;            // scale * log2(e)
+  int *status;                 // device status word (kStatusTimeout on a given-up wait)
+};
+
+// ---- kernel launchers (defined next to each kernel) ----------------------
+cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, float *out,
+                            const Problem &p, cudaStream_t stream);
+
+// tensor maps for the bf16 tensor-core kernels: every map is 3-D
+// (d, L, B*H) over a [B, H, L, d] bf16 tensor with 128-byte swizzle
+struct ShortMaps {
+  CUtensorMap q_full, k_full, v_full;  // box (64, Rq|Rk, P)
+  CUtensorMap q_rows, k_rows, v_rows;  // box (64, 8, 1), for padded tensors
+  CUtensorMap o_store;                 // box (64, Rq, P)
+};
+struct ShortGeom {
+  int Rq, Rk, P;  // rows per packed pair (powers of two) and pairs per unit
+  int units;      // ceil(B*H / P)
+  int rows_q, rows_k;  // load Q/K/V per 8-row box when nonzero (padding)
+};
+cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
+                            int num_sms, cudaStream_t stream);
+
+struct LongMaps {
+  CUtensorMap q, k, v;  // box (64, 128, 1)
+  CUtensorMap o;        // box (64, 128, 1)
+};
+cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
+                           cudaStream_t stream);
+
+cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
+
+}  // namespace mha

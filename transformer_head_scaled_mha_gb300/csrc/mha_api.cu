@@ -1,0 +1,228 @@
+// C ABI of the library: argument validation, path selection, TMA descriptor
+// encoding and kernel launch on the caller's stream.  See include/mha.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mha.h"
+#include "common.cuh"
+
+namespace mha {
+namespace {
+
+// Device status word: a kernel whose bounded wait gave up writes
+// kStatusTimeout here.  One per device, in the module's static memory.
+__device__ int g_status = 0;
+
+enum Path { kPathNone = 0, kPathF32 = 1, kPathShort = 2, kPathLong = 3, kPathZero = 4 };
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+
+int sm_count(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  g_sms[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+std::atomic<int *> g_status_ptr[kMaxDevices];
+
+int *status_ptr(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  int *v = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (v != nullptr) return v;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&v), g_status) != cudaSuccess) return nullptr;
+  g_status_ptr[dev].store(v, std::memory_order_release);
+  return v;
+}
+
+int next_pow2(int x) {
+  int r = 1;
+  while (r < x) r <<= 1;
+  return r;
+}
+
+// 3-D view (d, L, B*H) of a contiguous [B, H, L, d] bf16 tensor, 128B swizzle
+bool make_map(CUtensorMap *map, const void *base, int d, int L, int BH, int box_rows,
+              int box_pairs) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(L) * d * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_pairs)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Validates and picks a path; returns a non-negative Path or -(mha_status).
+int select_path(int B, int H, int Lq, int Lk, int dk, int dv, int mask, int dtype) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk <= 0 || dv <= 0) return -MHA_ERR_INVALID_ARGUMENT;
+  if (mask & ~(kMaskCausal | kMaskKeyPadding | kMaskQueryPadding))
+    return -MHA_ERR_INVALID_ARGUMENT;
+  if ((mask & (kMaskCausal | kMaskQueryPadding)) && Lq != Lk) return -MHA_ERR_INVALID_ARGUMENT;
+  if (dtype != MHA_DTYPE_F32 && dtype != MHA_DTYPE_BF16) return -MHA_ERR_INVALID_ARGUMENT;
+  // TMA coordinates and the kernels' row indices are 32-bit
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return -MHA_ERR_UNSUPPORTED;
+  if (dtype == MHA_DTYPE_F32) {
+    if (dk > 128 || dv > 128) return -MHA_ERR_UNSUPPORTED;
+  } else {
+    if (dk != dv || (dk != 64 && dk != 128)) return -MHA_ERR_UNSUPPORTED;
+  }
+  if (static_cast<long long>(B) * H * Lq == 0) return kPathNone;
+  if (Lk == 0) return kPathZero;
+  if (dtype == MHA_DTYPE_F32) return kPathF32;
+  if (dk == 64 && Lq <= 128 && Lk <= 128) return kPathShort;
+  return kPathLong;
+}
+
+}  // namespace
+}  // namespace mha
+
+using namespace mha;
+
+extern "C" int mha_fwd_path(int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                            int dtype) {
+  return select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
+}
+
+extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
+                       int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                       const int32_t *key_lengths, float scale, int dtype, void *stream_) {
+  const int path = select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
+  if (path < 0) return -path;
+  if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
+  if (path == kPathNone) return MHA_OK;
+  const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
+  if (padded && key_lengths == nullptr) return MHA_ERR_INVALID_ARGUMENT;
+  const size_t esz = dtype == MHA_DTYPE_F32 ? 4 : 2;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nq = BH * Lq * d_k * esz, nk = BH * Lk * d_k * esz, nv = BH * Lk * d_v * esz;
+  const size_t no = BH * Lq * d_v * esz;
+  if (out == nullptr || q == nullptr || (Lk > 0 && (k == nullptr || v == nullptr)))
+    return MHA_ERR_INVALID_ARGUMENT;
+  for (const void *ptr : {static_cast<const void *>(q), static_cast<const void *>(k),
+                          static_cast<const void *>(v), static_cast<const void *>(out)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return MHA_ERR_INVALID_ARGUMENT;
+  if (overlaps(out, no, q, nq) || overlaps(out, no, k, nk) || overlaps(out, no, v, nv) ||
+      (padded && overlaps(out, no, key_lengths, sizeof(int32_t) * B)))
+    return MHA_ERR_INVALID_ARGUMENT;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+  Problem p;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.dk = d_k;
+  p.dv = d_v;
+  p.mask = mask_kind;
+  p.key_lengths = padded ? key_lengths : nullptr;
+  p.scale_log2 = scale * kLog2e;
+  p.status = status_ptr(dev);
+  if (p.status == nullptr) return MHA_ERR_CUDA;
+
+  cudaError_t err = cudaSuccess;
+  if (path == kPathZero) {
+    err = launch_zero_fill(out, no, stream);
+  } else if (path == kPathF32) {
+    err = launch_f32_simt(static_cast<const float *>(q), static_cast<const float *>(k),
+                          static_cast<const float *>(v), static_cast<float *>(out), p, stream);
+  } else {
+    const int sms = sm_count(dev);
+    if (sms <= 0) return MHA_ERR_CUDA;
+    const int bh = static_cast<int>(BH);
+    if (path == kPathShort) {
+      ShortGeom g;
+      g.Rq = next_pow2(Lq < 8 ? 8 : Lq);
+      g.Rk = next_pow2(Lk < 16 ? 16 : Lk);
+      g.P = 128 / (g.Rq > g.Rk ? g.Rq : g.Rk);
+      g.units = (bh + g.P - 1) / g.P;
+      g.rows_q = (mask_kind & kMaskQueryPadding) ? 1 : 0;
+      g.rows_k = (mask_kind & kMaskKeyPadding) ? 1 : 0;
+      ShortMaps m;
+      std::memset(&m, 0, sizeof m);
+      bool ok = make_map(&m.q_full, q, 64, Lq, bh, g.Rq, g.P) &&
+                make_map(&m.k_full, k, 64, Lk, bh, g.Rk, g.P) &&
+                make_map(&m.v_full, v, 64, Lk, bh, g.Rk, g.P) &&
+                make_map(&m.q_rows, q, 64, Lq, bh, 8, 1) &&
+                make_map(&m.k_rows, k, 64, Lk, bh, 8, 1) &&
+                make_map(&m.v_rows, v, 64, Lk, bh, 8, 1) &&
+                make_map(&m.o_store, out, 64, Lq, bh, g.Rq, g.P);
+      if (!ok) return MHA_ERR_CUDA;
+      err = launch_short_tc(m, g, p, sms, stream);
+    } else {
+      LongMaps m;
+      std::memset(&m, 0, sizeof m);
+      bool ok = make_map(&m.q, q, d_k, Lq, bh, 128, 1) && make_map(&m.k, k, d_k, Lk, bh, 128, 1) &&
+                make_map(&m.v, v, d_v, Lk, bh, 128, 1) && make_map(&m.o, out, d_v, Lq, bh, 128, 1);
+      if (!ok) return MHA_ERR_CUDA;
+      err = launch_long_tc(m, p, sms, stream);
+    }
+  }
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+extern "C" const char *mha_status_string(int status) {
+  switch (status) {
+    case MHA_OK: return "ok";
+    case MHA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case MHA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MHA_ERR_CUDA: return "CUDA error";
+    case MHA_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int mha_debug_status(void *stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int host = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&host, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess)
+    return MHA_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess)
+    return MHA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MHA_ERR_CUDA;
+  return host == 0 ? MHA_OK : MHA_ERR_TIMEOUT;
+}
+
+extern "C" int mha_version(void) { return 100; }

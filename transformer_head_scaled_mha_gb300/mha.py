@@ -1,0 +1,122 @@
+"""Python binding of the C ABI in include/mha.h (ctypes; argument marshalling only).
+
+Every function here forwards to the CUDA library libmha.so built from
+``csrc/``.  There is no fallback: if the library is missing or fails to load,
+the import raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+MHA_DTYPE_F32, MHA_DTYPE_BF16 = 0, 1
+MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_QUERY_PADDING = 0, 1, 2, 4
+MHA_OK, MHA_ERR_INVALID_ARGUMENT, MHA_ERR_UNSUPPORTED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = range(5)
+PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fill"}
+
+EXPORTED = ("mha_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
+
+
+class MhaError(RuntimeError):
+    def __init__(self, status: int, what: str = "mha_fwd"):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError("libmha.so is not built (%s); run __graft_entry__.build() or "
+                          "python -m transformer_head_scaled_mha_gb300._build" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.mha_fwd.restype = i32
+    lib.mha_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp,
+                            ctypes.c_float, i32, vp]
+    lib.mha_fwd_path.restype = i32
+    lib.mha_fwd_path.argtypes = [i32] * 8
+    lib.mha_status_string.restype = ctypes.c_char_p
+    lib.mha_status_string.argtypes = [i32]
+    lib.mha_debug_status.restype = i32
+    lib.mha_debug_status.argtypes = [vp]
+    lib.mha_version.restype = i32
+    lib.mha_version.argtypes = []
+    return lib
+
+
+lib = _load()
+LIB_PATH = _build.LIB
+
+
+def status_string(status: int) -> str:
+    return lib.mha_status_string(int(status)).decode()
+
+
+mha_status_string = status_string
+
+
+def mha_version() -> int:
+    return int(lib.mha_version())
+
+
+def mha_fwd_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype) -> int:
+    return int(lib.mha_fwd_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype))
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def mha_debug_status(stream=None) -> int:
+    return int(lib.mha_debug_status(_stream_handle(stream)))
+
+
+def mha_fwd(q, k, v, out=None, *, mask_kind: int = 0, key_lengths=None, scale=None,
+            stream=None):
+    """out = softmax(q k^T * scale) v per (batch, head), on q's CUDA device.
+
+    q [B,H,Lq,d_k], k [B,H,Lk,d_k], v [B,H,Lk,d_v]: contiguous CUDA tensors, all
+    float32 or all bfloat16.  ``key_lengths``: int32 CUDA tensor [B] (needed for
+    the padding masks).  ``scale`` defaults to 1/sqrt(d_k).  Enqueued on
+    ``stream`` (default: torch's current stream); returns ``out``.
+    """
+    import torch
+    B, H, Lq, dk = q.shape
+    Lk, dv = k.shape[2], v.shape[3]
+    if q.dtype == torch.float32:
+        dtype = MHA_DTYPE_F32
+    elif q.dtype == torch.bfloat16:
+        dtype = MHA_DTYPE_BF16
+    else:
+        raise TypeError("q must be float32 or bfloat16")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if tuple(k.shape) != (B, H, Lk, dk) or tuple(v.shape) != (B, H, Lk, dv):
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape),
+                                                             tuple(v.shape)))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if out is None:
+        out = torch.empty((B, H, Lq, dv), dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != (B, H, Lq, dv) or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B,H,Lq,d_v] tensor of q's dtype")
+    kl_ptr = None
+    if key_lengths is not None:
+        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
+            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
+        kl_ptr = key_lengths.data_ptr()
+    if scale is None:
+        scale = float(dk) ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.mha_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Lq, Lk,
+                         dk, dv, int(mask_kind), kl_ptr, float(scale), dtype,
+                         _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st)
+    return out
