@@ -236,12 +236,13 @@ def oracle_sample_rows(spec, lens, target_flops, seed=0):
     return rows, n / total_rows
 
 
-def time_oracle(spec, q, k, v, lens, rows, threads=0):
+def time_oracle(spec, q, k, v, lens, rows, threads=0, reps=1):
     import oracle
     scale = gen.default_scale(spec["dk"])
     t0 = time.perf_counter()
-    oracle.mha_fwd(q, k, v, mask_kind=spec["mask"], key_lengths=lens, scale=scale, rows=rows,
-                   threads=threads)
+    for _ in range(reps):
+        oracle.mha_fwd(q, k, v, mask_kind=spec["mask"], key_lengths=lens, scale=scale,
+                       rows=rows, threads=threads)
     return time.perf_counter() - t0
 
 
@@ -256,13 +257,15 @@ def oracle_baseline(spec, q, k, v, lens, budget_s=12.0):
     t_probe = time_oracle(spec, q, k, v, lens, probe_rows)
     rate = (total_flops * probe_frac) / max(t_probe, 1e-6)  # oracle flop/s
     rows, frac = oracle_sample_rows(spec, lens, rate * budget_s, seed=1)
-    t = time_oracle(spec, q, k, v, lens, rows)
+    # a workload smaller than the budget is run whole, several times over
+    reps = max(1, int(budget_s * rate / max(total_flops, 1))) if rows is None else 1
+    t = time_oracle(spec, q, k, v, lens, rows, reps=reps)
     nbytes, flops = algorithmic(spec, lens)
-    value = throughput(spec, nbytes * frac, flops * frac, t)
+    value = throughput(spec, nbytes * frac * reps, flops * frac * reps, t)
     n_rows = spec["B"] * spec["H"] * spec["Lq"] if rows is None else len(rows)
-    sample = ("%d of %d query rows (%.4g%%), drawn uniformly at random, %.1f s on %d threads; "
-              "work scaled by the sampled share" % (n_rows, spec["B"] * spec["H"] * spec["Lq"],
-                                                     100 * frac, t, cores))
+    sample = ("%d of %d query rows (%.4g%%), drawn uniformly at random, x%d, %.1f s on %d "
+              "threads; work scaled by the sampled share" % (
+                  n_rows, spec["B"] * spec["H"] * spec["Lq"], 100 * frac, reps, t, cores))
     return {"value": value, "unit": metric_of(spec)[1], "cores": cores, "kind": "oracle",
             "sample": sample}
 
@@ -326,33 +329,34 @@ def run_ours(args):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(args.steps):
                 step(i, stream)
-        # soak: replay untimed so clocks settle under load before the timed region
-        t_end = time.time() + args.soak
-        while time.time() < t_end:
-            graph.replay()
-            stream.synchronize()
 
+    def run_steps():
+        # graph.replay() launches on the current stream: make it `stream`
+        with torch.cuda.stream(stream):
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(args.steps):
+                    step(i, stream)
+
+    # Clocks are sampled from the start of an untimed soak (the same launches,
+    # so the GPU is at its loaded clocks) to the end of the timed region.
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.25)
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        run_steps()
+        stream.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
     ev0.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                step(i, stream)
+    run_steps()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier(world)
-    if t_wall1 - t_wall0 < 0.3:  # keep sampling a little if the region was short
-        time.sleep(0.3)
-    sampler.mark(t_wall0, t_wall1)
+    sampler.mark(t_soak + min(0.2, args.soak / 2), t_wall1)
     clocks = sampler.stop()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     elapsed = max_over_ranks(elapsed, world, dev)

@@ -3,27 +3,34 @@
 // One CTA computes 256 query rows of one (batch, head) as two 128-row tiles,
 // one per softmax warpgroup, streaming the keys/values in 128-row tiles:
 //
-//   S_w = Q_w K_j^T          tcgen05.mma, operands from 128B-swizzled smem,
-//                            fp32 accumulator in TMEM (one 128-column buffer
-//                            per warpgroup)
+//   S_w = Q_w K_j^T          tcgen05.mma, both operands from 128B-swizzled
+//                            smem, fp32 accumulator in TMEM (one 128-column
+//                            region per warpgroup)
 //   online softmax           tcgen05.ld of S into registers (thread = row),
 //                            scale folded with log2(e), causal / padding mask
 //                            on the tiles that straddle a boundary, running max
 //                            and running sum; exp2 on the MUFU unit
-//   P_w (bf16) -> smem       K-major operand of the next MMA
-//   O_w += P_w V_j           tcgen05.mma into a TMEM accumulator per warpgroup
+//   P_w (bf16) -> TMEM       tcgen05.st over the first 64 columns of S_w
+//   O_w += P_w V_j           tcgen05.mma with A = P_w read from TMEM, B = V_j
+//                            from smem, fp32 accumulator in TMEM
 //   epilogue                 O / rowsum -> bf16 -> swizzled smem -> TMA store
 //
 // The score matrix never leaves the SM.  While one warpgroup turns its S into
-// P, the tensor core runs the other warpgroup's products (ping-pong).  The
-// running max is only moved (and O rescaled in TMEM) when it grows by more
-// than 2^8, so the rescale is rare; the final division uses the same max for
-// numerator and denominator, so the result is unchanged.  Under a causal mask
-// the tiles above the diagonal are never loaded nor multiplied, which halves
-// the work; CTAs are issued heaviest query block first.
+// P, the tensor core runs the other warpgroup's products (ping-pong).  Per
+// warpgroup the MMA warp issues P_w(j-1) V_{j-1} before S_w(j) (the tensor
+// pipe runs one thread's MMAs in order, so S_w(j) overwrites P_w(j-1) only
+// after it was read), and the commit that announces S_w(j) also covers
+// P_w(j-1) V_{j-1}, so a warpgroup holding S_w(j) may rescale O_w at once.
+// K and V stream through a ring of smem slots two iterations ahead of use.
+// The running max is moved (and O rescaled in TMEM) only when it grows by more
+// than 2^8; numerator and denominator share the stale max, so the quotient is
+// unchanged.  Under a causal mask the tiles above the diagonal are never
+// loaded nor multiplied, which halves the work; CTAs are issued heaviest
+// query block first.
 //
-// Warp roles (320 threads): warps 0-3 softmax WG0, 4-7 softmax WG1, warp 8 TMA
-// producer (K_j, V_j through a ring of smem slots), warp 9 TMEM owner + MMA.
+// Warp roles (384 threads): warps 0-3 softmax WG0, 4-7 softmax WG1, warp 8 TMA
+// producer, warp 9 TMEM owner + MMA issuer, warps 10-11 idle (they complete the
+// third warpgroup so its register budget can be handed to the softmax).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -37,24 +44,30 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per warpgroup tile
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr int kWgThreads = 128;
+// Register split: launched at 168 per thread (384 x 168 = 64512); the
+// producer/MMA warpgroup drops to 56 and the two softmax warpgroups rise to
+// 224: 2 x 128 x 224 + 128 x 56 = 64512.
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsControl = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O may grow to 2^8 before a rescale
+constexpr int kMaxSlots = 8;
 
 template <int D>
 struct Cfg {
-  static constexpr int kBlkBytes = 128 * 128;          // one [128 rows x 64] swizzle block
+  static constexpr int kBlkBytes = 128 * 128;              // one [128 rows x 64] swizzle block
   static constexpr int kTileBytes = (D / 64) * kBlkBytes;  // a [128 x D] operand tile
-  static constexpr int kSlots = (D == 128) ? 3 : 6;    // K/V ring
-  static constexpr int kPBytes = 2 * kBlkBytes;        // P: [128 x 128] bf16
-  static constexpr size_t kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 2 * kPBytes + 256;
+  static constexpr int kSlots = (D == 128) ? 5 : 8;        // K/V ring (K0 V0 K1 V1 ...)
+  static constexpr size_t kSmem = 1024 + 2 * kTileBytes + kSlots * kTileBytes + 256;
 };
 
 struct __align__(8) Barriers {
   uint64_t q_full;
-  uint64_t kv_full[6];
-  uint64_t kv_empty[6];
+  uint64_t kv_full[kMaxSlots];
+  uint64_t kv_empty[kMaxSlots];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -76,10 +89,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *q_smem = smem;                               // 2 tiles; reused as output staging
-  uint8_t *kv_smem = q_smem + 2 * C::kTileBytes;        // kSlots tiles
-  uint8_t *p_smem = kv_smem + C::kSlots * C::kTileBytes;  // 2 P tiles
-  Barriers *bars = reinterpret_cast<Barriers *>(p_smem + 2 * C::kPBytes);
+  uint8_t *q_smem = smem;                         // 2 tiles; reused as output staging
+  uint8_t *kv_smem = q_smem + 2 * C::kTileBytes;  // kSlots tiles
+  Barriers *bars = reinterpret_cast<Barriers *>(kv_smem + C::kSlots * C::kTileBytes);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int l = p.key_lengths[b];
     len = l < 0 ? 0 : (l > p.Lk ? p.Lk : l);
   }
-  // keys [0, kv_end_w) matter for warpgroup w; rows [q0 + 128 w, ...) exist?
+  // warpgroup w owns rows [q0 + 128 w, +128) and needs key tiles [0, n_tiles[w])
   int n_tiles[2];
   bool wg_rows[2];
 #pragma unroll
@@ -132,13 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // TMEM columns: S_w / P_w at [128 w, 128 w + 128), O_w at [256 + 128 w, +D)
 
   int issued = 0;  // producer: K/V loads issued
   uint64_t *last_commit = nullptr;
   uint32_t last_parity = 0;
 
-  if (warp == 8) {
-    // ---- TMA producer ------------------------------------------------------
+  if (warp >= 8) {
+   regs_dec<kRegsControl>();
+   if (warp == 8) {
+    // ---- TMA producer: Q tiles, then K_0 V_0 K_1 V_1 ... through the ring --
     if (lane == 0 && n_kv > 0) {
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.v);
@@ -165,27 +180,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ---- MMA issuer (lane 0 issues; the warp waits together) ---------------
+    // iteration j, per warpgroup w: O_w += P_w(j-1) V_{j-1}, then S_w(j) = Q_w K_j^T
     const uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0);
-    const uint32_t idesc_o = idesc_bf16_f32(128, 64, 1);
+    const uint32_t idesc_o = idesc_bf16_f32(128, D, 1);
+    constexpr uint32_t kVLbo = C::kBlkBytes, kVSbo = 1024;
     bool ok = n_kv == 0 || mbar_wait(&bars->q_full, 0, abort_flag);
     for (int j = 0; ok && j <= n_kv; ++j) {
       const int ks = (2 * j) % C::kSlots, kr = (2 * j) / C::kSlots;
-      const int vs = (2 * j - 1) % C::kSlots, vr = (2 * j - 1) / C::kSlots;
+      const int vi = 2 * j - 1 < 0 ? 0 : 2 * j - 1;
+      const int vs = vi % C::kSlots, vr = vi / C::kSlots;
       if (j < n_kv && !(ok = mbar_wait(&bars->kv_full[ks], kr & 1, abort_flag))) break;
-      bool v_ready = false;
+      if (j >= 1 && !(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag))) break;
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
-        const bool do_s = j < n_tiles[w];
         const bool do_pv = j >= 1 && j - 1 < n_tiles[w];
-        if ((do_s || do_pv) && j >= 1 &&
-            !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag)))
-          break;
-        if (do_pv && !v_ready) {
-          if (!(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag))) break;
-          v_ready = true;
-        }
+        const bool do_s = j < n_tiles[w];
+        if (do_pv && !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag))) break;
         tc_fence_after();
         if (lane == 0) {
+          if (do_pv) {
+            const uint32_t sv = smem_addr(kv_smem + vs * C::kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              // B = V_{j-1}, MN-major: 16 key rows per step (8-row groups 1024 B
+              // apart); its D/64 blocks of 64 value columns lie kBlkBytes apart
+              const uint64_t db = smem_desc_sw128(sv + kk * 16 * 128, kVLbo, kVSbo);
+              // A = P_w(j-1): 16 keys = 8 TMEM columns per step
+              tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, db, idesc_o,
+                        (j - 1 > 0) || kk > 0);
+            }
+            tc_commit(&bars->pv_done[w]);
+          }
           if (do_s) {
             const uint32_t sq = smem_addr(q_smem + w * C::kTileBytes);
             const uint32_t sk = smem_addr(kv_smem + ks * C::kTileBytes);
@@ -196,22 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         smem_desc_sw128(sk + off, 16, 1024), idesc_s, kk > 0);
             }
             tc_commit(&bars->s_full[w]);
-          }
-          if (do_pv) {
-            const uint32_t sp = smem_addr(p_smem + w * C::kPBytes);
-            const uint32_t sv = smem_addr(kv_smem + vs * C::kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t da =
-                  smem_desc_sw128(sp + (kk >> 2) * C::kBlkBytes + (kk & 3) * 32, 16, 1024);
-#pragma unroll
-              for (int nb = 0; nb < D / 64; ++nb) {
-                const uint64_t db =
-                    smem_desc_sw128(sv + nb * C::kBlkBytes + kk * 16 * 128, 1024, 1024);
-                tc_mma_ss(tmem + 256 + w * 128 + nb * 64, da, db, idesc_o, (j - 1 > 0) || kk > 0);
-              }
-            }
-            tc_commit(&bars->pv_done[w]);
           }
         }
         __syncwarp();
@@ -231,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+   }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ---- softmax warpgroups --------------------------------------------------
     const int w = warp >> 2;           // warpgroup
     const int r = threadIdx.x & 127;   // row within the tile (TMEM lane)
@@ -249,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
+      // S_w(j) is ready, and so is P_w(j-1) V_{j-1} (same commit)
       if (!(ok = mbar_wait(&bars->s_full[w], j & 1, abort_flag))) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -258,54 +270,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int lim = jmax - j * kBN;  // columns c < lim are allowed
       const bool need_mask = __any_sync(0xffffffffu, lim < kBN);
-      float mt = -INFINITY;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sr[ch][e]) * p.scale_log2;
-          if (need_mask && ch * 32 + e >= lim) x = -INFINITY;
-          sr[ch][e] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
+      // positive scale: max over the raw scores, then one FMA per score;
+      // otherwise scale first (the max of scale * s is not scale * max s)
+      const bool pos = p.scale_log2 > 0.f;
+      const float mt = pos ? mask_max128(sr, need_mask, 0, lim) * p.scale_log2
+                           : scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
       const float m_new = fmaxf(m_use, mt);
       float alpha = 1.f;
       if (m_new > m_use + kRescaleThreshold) {
         if (m_use != -INFINITY) alpha = ex2_approx(m_use - m_new);
         m_use = m_new;
       }
-      l_run *= alpha;
       const bool live = m_use != -INFINITY;
-      float rs = 0.f;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float pe = live ? ex2_approx(__uint_as_float(sr[ch][e]) - m_use) : 0.f;
-          rs += pe;
-          sr[ch][e] = __float_as_uint(pe);
-        }
-      l_run += rs;
+      l_run = l_run * alpha + (pos ? exp2_fma_sum128(sr, p.scale_log2, m_use, live)
+                                   : exp2_sum128(sr, m_use, live));
 
-      // P_w(j-1) V_{j-1} must be done: it reads the P buffer and writes O
-      if (j >= 1) {
-        if (!(ok = mbar_wait(&bars->pv_done[w], (j - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-      }
-      const uint32_t sp = smem_addr(p_smem + w * C::kPBytes);
+      // P_w(j) as bf16 pairs over the first 64 columns of S_w
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            wv[t] = pack_bf16x2(__uint_as_float(sr[ch][q4 * 8 + 2 * t]),
-                                __uint_as_float(sr[ch][q4 * 8 + 2 * t + 1]));
-          const int c16 = ch * 4 + q4;
-          st_shared_v4(sp + (c16 >> 3) * C::kBlkBytes + sw128_offset(r, c16 & 7), wv[0], wv[1],
-                       wv[2], wv[3]);
+        for (int t = 0; t < 32; ++t) {
+          const int c = h * 64 + 2 * t;
+          pk[t] = pack_bf16x2(__uint_as_float(sr[c >> 5][c & 31]),
+                              __uint_as_float(sr[c >> 5][(c + 1) & 31]));
         }
+        tmem_st32(s_tmem + h * 32, pk);
+      }
       // the running max moved: rescale this row of O (rare, warp-wide)
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -317,9 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(o_tmem + ch * 32, o);
         }
-        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_full[w]);
     }
@@ -386,7 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_long_impl(const LongMaps &maps, const Problem &p, cudaStream_t stream) {
   static_assert(Cfg<D>::kSmem <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_long_tc_kernel<D>,
+  static_assert(Cfg<D>::kSlots <= kMaxSlots, "ring size");
+  // setmaxnreg.inc only succeeds if the launch reserved the registers it hands
+  // out; refuse to launch a build whose register count would not cover them.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, attn_long_tc_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(fa.numRegs) * kThreads <
+      2LL * 128 * kRegsSoftmax + 128LL * kRegsControl)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(attn_long_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Cfg<D>::kSmem));
   if (e != cudaSuccess) return e;

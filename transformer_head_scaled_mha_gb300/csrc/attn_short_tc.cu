@@ -128,10 +128,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t last_commit_parity = 0;
   if (warp == 4) {
     // ---- TMA producer ----------------------------------------------------
+    // lengths of the pairs of unit n, loaded one unit ahead of their use
+    auto load_lens = [&](int n, int (&lens)[16]) {
+      const int bh0 = (blockIdx.x + n * gridDim.x) * g.P;
+#pragma unroll
+      for (int pp = 0; pp < 16; ++pp)
+        lens[pp] = (n < n_local && pp < g.P && bh0 + pp < BH) ? clamp_len(p, (bh0 + pp) / p.H) : 0;
+    };
+    int lens[16], lens_next[16];
+    load_lens(0, lens);
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
       const int u = blockIdx.x + n * gridDim.x;
       const int bh0 = u * g.P;
+      load_lens(n + 1, lens_next);
       if (!mbar_wait(&bars->empty[s], ((n / kStages) & 1) ^ 1, abort_flag)) break;
       uint8_t *sq = stage_base + s * kStageBytes;
       uint8_t *sk = sq + kTileBytes;
@@ -140,15 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bytes = 0;
       if (!g.rows_q) bytes += g.P * g.Rq * 128;
       if (!g.rows_k) bytes += 2 * g.P * g.Rk * 128;
-      int lens[16];
 #pragma unroll
       for (int pp = 0; pp < 16; ++pp) {
-        lens[pp] = 0;
-        if (pp < g.P && bh0 + pp < BH) {
-          lens[pp] = clamp_len(p, (bh0 + pp) / p.H);
-          if (g.rows_q) bytes += ((min(lens[pp], p.Lq) + 7) / 8) * 1024;
-          if (g.rows_k) bytes += 2 * ((lens[pp] + 7) / 8) * 1024;
-        }
+        if (g.rows_q) bytes += ((min(lens[pp], p.Lq) + 7) / 8) * 1024;
+        if (g.rows_k) bytes += 2 * ((lens[pp] + 7) / 8) * 1024;
       }
       if (lane == 0) mbar_arrive_expect_tx(&bars->full[s], bytes);
       __syncwarp();
@@ -183,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = n + 1;
+#pragma unroll
+      for (int pp = 0; pp < 16; ++pp) lens[pp] = lens_next[pp];
     }
   } else if (warp == 5) {
     // ---- MMA issuer (lane 0) ----------------------------------------------
@@ -209,30 +216,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_commit_parity = (n >> 1) & 1;
       return true;
     };
-    bool ok = n_local == 0 || issue_s(0);
-    for (int n = 0; ok && n < n_local; ++n) {
-      const int s = n % kStages, b = n & 1;
-      if (n + 1 < n_local && !issue_s(n + 1)) break;
-      if (!mbar_wait(&bars->p_full[b], (n >> 1) & 1, abort_flag)) break;
-      if (!mbar_wait(&bars->o_free[b], ((n >> 1) & 1) ^ 1, abort_flag)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
-        const uint32_t sp = smem_addr(pbuf_base + b * kPBytes);
-        for (uint32_t kk = 0; kk < n_keys / 16; ++kk) {
-          // A = P (K-major, key block kk/4 of 64 keys, 32-byte step inside it)
-          const uint64_t da = smem_desc_sw128(sp + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32,
-                                              16, 1024);
-          // B = V (MN-major: 16 key rows per step, 64 value columns)
-          const uint64_t db = smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024);
-          tc_mma_ss(tmem + kOCol0 + b * kD, da, db, idesc_o, kk > 0);
-        }
-        tc_commit(&bars->pv_done[b]);
-        tc_commit(&bars->empty[s]);
+    // Issue whichever product is ready first: S for the next unit (its data
+    // landed, its S buffer is free) or P V for the oldest unit whose P is
+    // written.  Neither waits behind the other.
+    int ns = 0, npv = 0;
+    uint64_t t_idle = 0;
+    while (npv < n_local) {
+      bool progressed = false;
+      bool ready_s = false;
+      if (ns < n_local && ns <= npv + 1 && lane == 0)
+        ready_s = mbar_probe(&bars->full[ns % kStages], (ns / kStages) & 1);
+      if (__shfl_sync(0xffffffffu, ready_s, 0)) {
+        if (!issue_s(ns)) break;
+        ++ns;
+        progressed = true;
       }
-      __syncwarp();
-      last_commit = &bars->empty[s];
-      last_commit_parity = (n / kStages) & 1;
+      bool ready_pv = false;
+      if (npv < ns && lane == 0)
+        ready_pv = mbar_probe(&bars->p_full[npv & 1], (npv >> 1) & 1) &&
+                   mbar_probe(&bars->o_free[npv & 1], ((npv >> 1) & 1) ^ 1);
+      if (__shfl_sync(0xffffffffu, ready_pv, 0)) {
+        const int s = npv % kStages, b = npv & 1;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
+          const uint32_t sp = smem_addr(pbuf_base + b * kPBytes);
+          for (uint32_t kk = 0; kk < n_keys / 16; ++kk) {
+            // A = P (K-major, key block kk/4 of 64 keys, 32-byte step inside it)
+            const uint64_t da = smem_desc_sw128(
+                sp + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
+            // B = V (MN-major: 16 key rows per step, 64 value columns)
+            const uint64_t db = smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024);
+            tc_mma_ss(tmem + kOCol0 + b * kD, da, db, idesc_o, kk > 0);
+          }
+          tc_commit(&bars->pv_done[b]);
+          tc_commit(&bars->empty[s]);
+        }
+        __syncwarp();
+        last_commit = &bars->empty[s];
+        last_commit_parity = (npv / kStages) & 1;
+        ++npv;
+        progressed = true;
+      }
+      if (progressed) {
+        t_idle = 0;
+      } else {
+        const uint64_t now = global_timer_ns();
+        if (t_idle == 0) t_idle = now;
+        if (*abort_flag) break;
+        if (now - t_idle > kWaitLimitNs) {
+          *abort_flag = 1;
+          break;
+        }
+      }
     }
   } else {
     // ---- softmax + epilogue (warps 0-3; thread = tile row) -----------------
@@ -241,68 +277,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
 
+    auto len_of = [&](int n) -> int {
+      const int bh = (blockIdx.x + n * gridDim.x) * g.P + pr;
+      const bool valid = pr < g.P && bh < BH && i < p.Lq;
+      return valid ? clamp_len(p, bh / p.H) : 0;
+    };
+    int len_cur = n_local > 0 ? len_of(0) : 0;
     float rowsum_prev = 0.f;  // row sum of the unit whose epilogue is pending
     bool pending_zero = true;
     for (int n = 0; n <= n_local; ++n) {
       float rowsum = 0.f;
       bool zero_row = true;
+      const int len_next = n + 1 < n_local ? len_of(n + 1) : 0;  // load ahead of its use
       if (n < n_local) {
         const int b = n & 1;
         const int u = blockIdx.x + n * gridDim.x;
         const int bh = u * g.P + pr;
         const bool valid = pr < g.P && bh < BH && i < p.Lq;
-        const int len = valid ? clamp_len(p, bh / p.H) : 0;
+        const int len = len_cur;
         int jmax = p.Lk;
         if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
         if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
         const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
         if (!valid || qpad) jmax = 0;
         const int col_lo = pr * g.Rk;
-        // warp-wide column range in 32-column chunks
-        const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
-        const unsigned hi = __reduce_max_sync(0xffffffffu, jmax > 0 ? col_lo + jmax : 0);
-        const int ch_lo = (hi > 0) ? static_cast<int>(lo / 32) : 4;
-        const int ch_hi = (hi > 0) ? static_cast<int>((hi + 31) / 32) : 0;
 
         if (!mbar_wait(&bars->s_full[b], (n >> 1) & 1, abort_flag)) break;
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
-          if (ch >= ch_lo && ch < ch_hi)
-            tmem_ld32(tmem + lane_base + kSCol0 + b * 128 + ch * 32, sr[ch]);
+          tmem_ld32(tmem + lane_base + kSCol0 + b * 128 + ch * 32, sr[ch]);
         tmem_wait_ld();
         tc_fence_before();
-
-        // scale (log2 units), mask, row max
-        float m = -INFINITY;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (ch >= ch_lo && ch < ch_hi) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = ch * 32 + e;
-              const bool allowed = (c >= col_lo) && (c < col_lo + jmax);
-              const float x = allowed ? __uint_as_float(sr[ch][e]) * p.scale_log2 : -INFINITY;
-              sr[ch][e] = __float_as_uint(x);
-              m = fmaxf(m, x);
-            }
-          }
-        }
-        // exp2 against the max, row sum, P in bf16 (masked -> exactly 0)
+        // scale (log2 units), keep only this row's keys [col_lo, col_lo + jmax)
+        const float m = scale_mask_max128(sr, p.scale_log2, true, col_lo, col_lo + jmax);
         const bool any = m != -INFINITY;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (ch >= ch_lo && ch < ch_hi) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float x = __uint_as_float(sr[ch][e]);
-              const float pe = any ? ex2_approx(x - m) : 0.f;
-              rowsum += pe;
-              sr[ch][e] = __float_as_uint(pe);
-            }
-          }
-        }
+        rowsum = exp2_sum128(sr, m, any);
         zero_row = !any;
 
         // the P buffer b was last the staging tile of unit n-2's output store
@@ -311,15 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sp = smem_addr(pbuf_base + b * kPBytes);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const bool loaded = ch >= ch_lo && ch < ch_hi;
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte pieces of 8 columns
             uint32_t w[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              w[t] = loaded ? pack_bf16x2(__uint_as_float(sr[ch][q4 * 8 + 2 * t]),
-                                          __uint_as_float(sr[ch][q4 * 8 + 2 * t + 1]))
-                            : 0u;
+              w[t] = pack_bf16x2(__uint_as_float(sr[ch][q4 * 8 + 2 * t]),
+                                 __uint_as_float(sr[ch][q4 * 8 + 2 * t + 1]));
             const int c16 = ch * 4 + q4;  // 0..15
             const uint32_t addr =
                 sp + (c16 >> 3) * (kTileRows * 128) + sw128_offset(r, c16 & 7);
@@ -366,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       rowsum_prev = rowsum;
       pending_zero = zero_row;
+      len_cur = len_next;
     }
     if (threadIdx.x == 0) tma_store_wait0();
   }

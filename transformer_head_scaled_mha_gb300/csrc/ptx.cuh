@@ -42,6 +42,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// non-blocking probe of a phase (test_wait never suspends the thread)
+__device__ __forceinline__ bool mbar_probe(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -141,6 +154,16 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -156,6 +179,18 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A (M x 16 per step, bf16 pairs
+// packed two per 32-bit column, row m in lane m) read from tensor memory
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -242,6 +277,171 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Pairs of fp32 in one 64-bit register: sm_100-class parts execute add, sub
+// and mul on both halves with one f32x2 instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// three-input maximum (one instruction on sm_100-class parts)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Row softmax numerator over 128 scores held as raw fp32 bits in r[4][32]:
+//   x_c = s_c * scale_log2, and -inf outside lo <= c < hi (when `mask`)
+// returns max_c x_c; r is overwritten with x.  Reductions use a tree (3-input
+// max, 16 independent chains) so the dependency depth is ~8, not 128.
+__device__ __forceinline__ float scale_mask_max128(uint32_t (&r)[4][32], float scale_log2,
+                                                   bool mask, int lo, int hi) {
+  const uint64_t sc = f2_pack(scale_log2, scale_log2);
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    float a, b;
+    f2_unpack(f2_mul(f2_pack(__uint_as_float(r[c >> 5][c & 31]),
+                             __uint_as_float(r[c >> 5][(c + 1) & 31])),
+                     sc),
+              a, b);
+    if (mask) {
+      a = static_cast<unsigned>(c - lo) < static_cast<unsigned>(hi - lo) ? a : -INFINITY;
+      b = static_cast<unsigned>(c + 1 - lo) < static_cast<unsigned>(hi - lo) ? b : -INFINITY;
+    }
+    r[c >> 5][c & 31] = __float_as_uint(a);
+    r[c >> 5][(c + 1) & 31] = __float_as_uint(b);
+  }
+#define MHA_X(c) __uint_as_float(r[(c) >> 5][(c) & 31])
+  float m[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    m[k] = fmax3(MHA_X(k), MHA_X(k + 16), MHA_X(k + 32));
+    m[k] = fmax3(m[k], MHA_X(k + 48), MHA_X(k + 64));
+    m[k] = fmax3(m[k], MHA_X(k + 80), MHA_X(k + 96));
+    m[k] = fmaxf(m[k], MHA_X(k + 112));
+  }
+#undef MHA_X
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmax3(m[9], m[10], m[11]);
+  const float e = fmax3(m[12], m[13], m[14]);
+  return fmax3(fmax3(a, b, c), fmax3(d, e, m[15]), -INFINITY);
+}
+
+// Raw-score variant for a positive scale: s_c -> -inf outside lo <= c < hi
+// (when `mask`), returns max_c s_c (the scaled max is scale_log2 times it).
+__device__ __forceinline__ float mask_max128(uint32_t (&r)[4][32], bool mask, int lo, int hi) {
+  if (mask) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (static_cast<unsigned>(c - lo) >= static_cast<unsigned>(hi - lo))
+        r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+  }
+#define MHA_X(c) __uint_as_float(r[(c) >> 5][(c) & 31])
+  float m[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    m[k] = fmax3(MHA_X(k), MHA_X(k + 16), MHA_X(k + 32));
+    m[k] = fmax3(m[k], MHA_X(k + 48), MHA_X(k + 64));
+    m[k] = fmax3(m[k], MHA_X(k + 80), MHA_X(k + 96));
+    m[k] = fmaxf(m[k], MHA_X(k + 112));
+  }
+#undef MHA_X
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmax3(m[9], m[10], m[11]);
+  const float e = fmax3(m[12], m[13], m[14]);
+  return fmax3(fmax3(a, b, c), fmax3(d, e, m[15]), -INFINITY);
+}
+
+// p_c = exp2(s_c * scale_log2 - m) in place, one packed FMA per pair (0 when
+// !live); returns sum_c p_c
+__device__ __forceinline__ float exp2_fma_sum128(uint32_t (&r)[4][32], float scale_log2, float m,
+                                                 bool live) {
+  const uint64_t sc = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm = f2_pack(-m, -m);
+  uint64_t acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0ull;
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c >> 5][c & 31]),
+                             __uint_as_float(r[c >> 5][(c + 1) & 31])),
+                     sc, nm),
+              a, b);
+    a = live ? ex2_approx(a) : 0.f;
+    b = live ? ex2_approx(b) : 0.f;
+    r[c >> 5][c & 31] = __float_as_uint(a);
+    r[c >> 5][(c + 1) & 31] = __float_as_uint(b);
+    acc[(c >> 1) & 7] = f2_add(acc[(c >> 1) & 7], f2_pack(a, b));
+  }
+  acc[0] = f2_add(acc[0], acc[1]);
+  acc[2] = f2_add(acc[2], acc[3]);
+  acc[4] = f2_add(acc[4], acc[5]);
+  acc[6] = f2_add(acc[6], acc[7]);
+  acc[0] = f2_add(acc[0], acc[2]);
+  acc[4] = f2_add(acc[4], acc[6]);
+  acc[0] = f2_add(acc[0], acc[4]);
+  float lo, hi;
+  f2_unpack(acc[0], lo, hi);
+  return lo + hi;
+}
+
+// p_c = exp2(x_c - m) in place (0 when !live); returns sum_c p_c (16 partial
+// sums, packed adds)
+__device__ __forceinline__ float exp2_sum128(uint32_t (&r)[4][32], float m, bool live) {
+  const uint64_t mm = f2_pack(m, m);
+  uint64_t acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0ull;
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    float a, b;
+    f2_unpack(f2_sub(f2_pack(__uint_as_float(r[c >> 5][c & 31]),
+                             __uint_as_float(r[c >> 5][(c + 1) & 31])),
+                     mm),
+              a, b);
+    a = live ? ex2_approx(a) : 0.f;
+    b = live ? ex2_approx(b) : 0.f;
+    r[c >> 5][c & 31] = __float_as_uint(a);
+    r[c >> 5][(c + 1) & 31] = __float_as_uint(b);
+    acc[(c >> 1) & 7] = f2_add(acc[(c >> 1) & 7], f2_pack(a, b));
+  }
+  acc[0] = f2_add(acc[0], acc[1]);
+  acc[2] = f2_add(acc[2], acc[3]);
+  acc[4] = f2_add(acc[4], acc[5]);
+  acc[6] = f2_add(acc[6], acc[7]);
+  acc[0] = f2_add(acc[0], acc[2]);
+  acc[4] = f2_add(acc[4], acc[6]);
+  acc[0] = f2_add(acc[0], acc[4]);
+  float lo, hi;
+  f2_unpack(acc[0], lo, hi);
+  return lo + hi;
 }
 
 // two floats -> packed bf16x2 (round to nearest even); lo in the low half
