@@ -53,6 +53,9 @@ SMALL = [
     spec(6, 3, 96, 128, 64, mask=KP, len_range=(0, 128)),
     spec(3, 5, 7, 13, 64, mask=KP, len_range=(1, 13)),
     spec(4, 4, 1, 1, 64),
+    spec(4, 3, 16, 16, 64, mask=C),
+    spec(5, 3, 30, 20, 64, mask=KP, len_range=(0, 20)),
+    spec(7, 3, 40, 40, 64, mask=KP | QP, len_range=(0, 40)),
     spec(2, 2, 100, 100, 64, mask=C | KP, len_range=(0, 100)),
     spec(3, 3, 30, 30, 64, mask=0),
     spec(1, 2, 700, 700, 128, mask=C, amp=0.5),

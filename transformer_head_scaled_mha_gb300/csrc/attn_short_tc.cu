@@ -4,23 +4,30 @@
 // arithmetic: each (batch, head) pair is one small Q K^T and one small P V.
 // This kernel packs P = 128 / max(Rq, Rk) pairs into one 128-row tile (Rq,
 // Rk: Lq, Lk rounded up to powers of two) so one tcgen05.mma covers all of
-// them; products between different pairs land in off-diagonal blocks that the
-// mask discards.  Each CTA is persistent (one per SM) and walks the units
+// them; products between different pairs land in off-diagonal blocks that are
+// never read.  Each CTA is persistent (one per SM) and walks the units
 // u = blockIdx.x, + gridDim.x, ...
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue, thread t owns tile row t
-//   warp  4    TMA producer: Q, K, V of a unit into a 3-stage ring
-//   warp  5    TMEM owner and MMA issuer
+// Warp roles (384 threads):
+//   warps 0-3, 4-7  two softmax warpgroups; unit n goes to warpgroup n % 2,
+//                   thread t owns tile row t
+//   warp  8         TMA producer: Q, K, V of a unit into a 4-stage ring
+//   warp  9         TMEM owner and MMA issuer
+//   warps 10-11     idle; they complete the third warpgroup so its register
+//                   budget can be handed to the softmax warpgroups
 // Per unit (the four steps of scaled dot-product attention):
-//   S = Q K^T              tcgen05.mma -> TMEM (fp32), double-buffered
-//   mask, scale, softmax   tcgen05.ld -> registers; exp2 against the row max
-//   P (bf16) -> smem       128-byte swizzled K-major operand
-//   O = P V                tcgen05.mma -> TMEM (fp32), double-buffered
-//   O / rowsum -> bf16     tcgen05.ld, swizzled smem tile, TMA store
-// Padded sequences load only their first ceil(len/8)*8 rows (8-row TMA boxes),
-// so padding costs no HBM reads; masked keys get exactly zero weight; padded
-// query rows and rows without any allowed key are stored as +0.
+//   S = Q K^T              tcgen05.mma -> TMEM (fp32), one region per warpgroup
+//   mask, scale, softmax   tcgen05.ld of the 32-column chunks the warp's rows
+//                          can use -> registers; exp2 against the row max
+//   P (bf16) -> TMEM       over the first 64 columns of the unit's S region
+//   O = P V                tcgen05.mma (A = P from TMEM) -> TMEM, 4 buffers
+//   O / rowsum -> bf16     tcgen05.ld; each warp stages its 32 rows in a
+//                          swizzled 4 KiB buffer and TMA-stores them
+// Padded sequences load only their first ceil(len/8)*8 rows, as at most four
+// TMA boxes of 64/32/16/8 rows per tensor and pair, so padding costs no HBM
+// reads (a CTA's first unit loads whole tiles instead, so it does not wait
+// for the lengths).  Masked keys get exactly zero weight; padded query rows
+// and rows without any allowed key are stored as +0.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,30 +40,36 @@ namespace mha {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * kD * 2;  // 16 KiB per operand tile
 constexpr int kStageBytes = 3 * kTileBytes;     // Q | K | V
-constexpr int kPBytes = kTileRows * 128 * 2;     // P tile: 128 x 128 bf16 (2 swizzle blocks)
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 384;  // 3 warpgroups
+constexpr int kWgThreads = 128;
+// Register split: launched at 168 per thread (384 x 168 = 64512); the control
+// warpgroup drops to 64 and the softmax warpgroups rise to 216.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 64;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0;    // S buffers: cols [0,128), [128,256)
-constexpr uint32_t kOCol0 = 256;  // O buffers: cols [256,320), [320,384)
+constexpr uint32_t kSCol0 = 0;    // S/P region of warpgroup w: [128 w, 128 w + 128)
+constexpr uint32_t kOCol0 = 256;  // O buffer of unit n: [256 + 64 (n % 4), +64)
+constexpr int kOBufs = 4;
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t pv_done[2];
-  uint64_t o_free[2];
+  uint64_t pv_done[kOBufs];
+  uint64_t o_free[kOBufs];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 2 * kPBytes +
-                              sizeof(Barriers);
+constexpr int kStagingBytes = 32 * 128;  // one warp's 32 output rows
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes +
+                              8 * kStagingBytes + sizeof(Barriers);
 
 __device__ __forceinline__ int clamp_len(const Problem &p, int b) {
   if (!(p.mask & (kMaskKeyPadding | kMaskQueryPadding))) return p.Lk;
@@ -71,6 +84,70 @@ __device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
+// Rows [0, rows) of one pair as boxes of 64 rows, then one each of 32, 16 and
+// 8 rows as the remainder needs (rows rounded up to a multiple of 8).
+__device__ __forceinline__ uint32_t box_bytes(int rows) {
+  return static_cast<uint32_t>((rows + 7) / 8) * 1024u;
+}
+__device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *maps, uint64_t *bar,
+                                          int rows, int bh) {
+  int n8 = (rows + 7) / 8, r0 = 0;
+  for (; n8 >= 8; n8 -= 8, r0 += 64) tma_load_3d(dst + r0 * 128, &maps[3], bar, 0, r0, bh);
+#pragma unroll
+  for (int h = 2; h >= 0; --h)
+    if (n8 & (1 << h)) {
+      tma_load_3d(dst + r0 * 128, &maps[h], bar, 0, r0, bh);
+      r0 += 8 << h;
+    }
+}
+
+// One 32-column chunk of a row's scores (raw fp32 bits), sign-flipped by
+// `sgn` (a negative scale is applied as |scale| to -s), with columns outside
+// lo <= c < hi set to -inf when `mask`.
+__device__ __forceinline__ void chunk_prepare(uint32_t (&v)[32], int c0, uint32_t sgn, bool mask,
+                                              int lo, int hi) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    uint32_t x = v[e] ^ sgn;
+    if (mask && static_cast<unsigned>(c0 + e - lo) >= static_cast<unsigned>(hi - lo))
+      x = __float_as_uint(-INFINITY);
+    v[e] = x;
+  }
+}
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k)
+    t[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                 __uint_as_float(v[3 * k + 2]));
+  t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+  return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]),
+               fmax3(fmax3(t[6], t[7], t[8]), t[9], t[10]));
+}
+// p_c = exp2(s_c * sl - m) for one chunk, packed into 16 bf16x2 columns;
+// returns the chunk's sum of p (fp32)
+__device__ __forceinline__ float chunk_exp_pack(const uint32_t (&v)[32], float sl, float m,
+                                                uint32_t (&pk)[16]) {
+  const uint64_t sc = f2_pack(sl, sl);
+  const uint64_t nm = f2_pack(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc, nm), a, b);
+    a = ex2_approx(a);
+    b = ex2_approx(b);
+    acc[(e >> 1) & 3] = f2_add(acc[(e >> 1) & 3], f2_pack(a, b));
+    pk[e >> 1] = pack_bf16x2(a, b);
+  }
+  acc[0] = f2_add(acc[0], acc[1]);
+  acc[2] = f2_add(acc[2], acc[3]);
+  acc[0] = f2_add(acc[0], acc[2]);
+  float lo, hi;
+  f2_unpack(acc[0], lo, hi);
+  return lo + hi;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_short_tc_kernel(const __grid_constant__ ShortMaps maps, const ShortGeom g,
                          const Problem p) {
@@ -78,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *stage_base = smem;
-  uint8_t *pbuf_base = smem + kStages * kStageBytes;
-  Barriers *bars = reinterpret_cast<Barriers *>(pbuf_base + 2 * kPBytes);
+  uint8_t *staging = smem + kStages * kStageBytes;  // 8 softmax warps x 4 KiB
+  Barriers *bars = reinterpret_cast<Barriers *>(staging + 8 * kStagingBytes);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,22 +171,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], kSoftmaxThreads);
-      mbar_init(&bars->pv_done[b], 1);
-      mbar_init(&bars->o_free[b], kSoftmaxThreads);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&bars->s_full[w], 1);
+      mbar_init(&bars->p_full[w], kWgThreads);
+    }
+    for (int o = 0; o < kOBufs; ++o) {
+      mbar_init(&bars->pv_done[o], 1);
+      mbar_init(&bars->o_free[o], kWgThreads);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&maps.q_full);
     tma_prefetch_desc(&maps.k_full);
     tma_prefetch_desc(&maps.v_full);
-    tma_prefetch_desc(&maps.o_store);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -123,102 +201,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  int issued = 0;                        // producer: units whose loads were issued
-  uint64_t *last_commit = nullptr;       // MMA issuer: barrier of the last commit
+  int issued = 0;                   // producer: units whose loads were issued
+  uint64_t *last_commit = nullptr;  // MMA issuer: barrier of the last commit
   uint32_t last_commit_parity = 0;
-  if (warp == 4) {
-    // ---- TMA producer ----------------------------------------------------
-    // lengths of the pairs of unit n, loaded one unit ahead of their use
-    auto load_lens = [&](int n, int (&lens)[16]) {
-      const int bh0 = (blockIdx.x + n * gridDim.x) * g.P;
-#pragma unroll
-      for (int pp = 0; pp < 16; ++pp)
-        lens[pp] = (n < n_local && pp < g.P && bh0 + pp < BH) ? clamp_len(p, (bh0 + pp) / p.H) : 0;
-    };
-    int lens[16], lens_next[16];
-    load_lens(0, lens);
+  if (warp >= 8) {
+   regs_dec<kRegsControl>();
+   if (warp == 8) {
+    // ---- TMA producer (lane pp handles pair pp of the unit) -----------------
+    const int pp = lane;
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
-      const int u = blockIdx.x + n * gridDim.x;
-      const int bh0 = u * g.P;
-      load_lens(n + 1, lens_next);
+      const int bh0 = (blockIdx.x + n * gridDim.x) * g.P;
+      // the first unit loads whole tiles: no wait for the lengths
+      const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
+      const bool has_pair = pp < g.P && bh0 + pp < BH;
+      const int len = (has_pair && (rows_q || rows_k)) ? clamp_len(p, (bh0 + pp) / p.H) : 0;
+      uint32_t bytes = 0;
+      if (has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
+      if (has_pair && rows_k) bytes += 2 * box_bytes(len);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      if (!rows_q) bytes += g.P * g.Rq * 128;
+      if (!rows_k) bytes += 2 * g.P * g.Rk * 128;
       if (!mbar_wait(&bars->empty[s], ((n / kStages) & 1) ^ 1, abort_flag)) break;
       uint8_t *sq = stage_base + s * kStageBytes;
       uint8_t *sk = sq + kTileBytes;
       uint8_t *sv = sk + kTileBytes;
-      // byte count of everything this unit loads
-      uint32_t bytes = 0;
-      if (!g.rows_q) bytes += g.P * g.Rq * 128;
-      if (!g.rows_k) bytes += 2 * g.P * g.Rk * 128;
-#pragma unroll
-      for (int pp = 0; pp < 16; ++pp) {
-        if (g.rows_q) bytes += ((min(lens[pp], p.Lq) + 7) / 8) * 1024;
-        if (g.rows_k) bytes += 2 * ((lens[pp] + 7) / 8) * 1024;
-      }
       if (lane == 0) mbar_arrive_expect_tx(&bars->full[s], bytes);
       __syncwarp();
       if (lane == 0) {
-        if (!g.rows_q) tma_load_3d(sq, &maps.q_full, &bars->full[s], 0, 0, bh0);
-        if (!g.rows_k) {
+        if (!rows_q) tma_load_3d(sq, &maps.q_full, &bars->full[s], 0, 0, bh0);
+        if (!rows_k) {
           tma_load_3d(sk, &maps.k_full, &bars->full[s], 0, 0, bh0);
           tma_load_3d(sv, &maps.v_full, &bars->full[s], 0, 0, bh0);
         }
       }
-      if (g.rows_q || g.rows_k) {
-        // 8-row boxes, spread over the lanes: item = (pair, box)
-        const int boxes_per_pair = (g.Rq > g.Rk ? g.Rq : g.Rk) / 8;
-        for (int it = lane; it < g.P * boxes_per_pair; it += 32) {
-          const int pp = it / boxes_per_pair, bx = it % boxes_per_pair;
-          int len_pp = 0;
-#pragma unroll
-          for (int t = 0; t < 16; ++t)
-            if (t == pp) len_pp = lens[t];
-          if (bh0 + pp >= BH) continue;
-          const int r0 = bx * 8;
-          if (g.rows_q && r0 < min(len_pp, p.Lq))
-            tma_load_3d(sq + (pp * g.Rq + r0) * 128, &maps.q_rows, &bars->full[s], 0, r0,
-                        bh0 + pp);
-          if (g.rows_k && r0 < len_pp) {
-            tma_load_3d(sk + (pp * g.Rk + r0) * 128, &maps.k_rows, &bars->full[s], 0, r0,
-                        bh0 + pp);
-            tma_load_3d(sv + (pp * g.Rk + r0) * 128, &maps.v_rows, &bars->full[s], 0, r0,
-                        bh0 + pp);
-          }
-        }
+      if (has_pair && rows_q) load_rows(sq + pp * g.Rq * 128, maps.q_rows, &bars->full[s],
+                                        min(len, p.Lq), bh0 + pp);
+      if (has_pair && rows_k) {
+        load_rows(sk + pp * g.Rk * 128, maps.k_rows, &bars->full[s], len, bh0 + pp);
+        load_rows(sv + pp * g.Rk * 128, maps.v_rows, &bars->full[s], len, bh0 + pp);
       }
       __syncwarp();
       issued = n + 1;
-#pragma unroll
-      for (int pp = 0; pp < 16; ++pp) lens[pp] = lens_next[pp];
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---- MMA issuer (lane 0) ----------------------------------------------
     const uint32_t n_keys = static_cast<uint32_t>(g.P * g.Rk);  // multiple of 16, <= 128
     const uint32_t idesc_s = idesc_bf16_f32(128, n_keys, 0);
     const uint32_t idesc_o = idesc_bf16_f32(128, kD, 1);
-    auto issue_s = [&](int n) -> bool {
-      const int s = n % kStages, b = n & 1;
-      if (!mbar_wait(&bars->full[s], (n / kStages) & 1, abort_flag)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sq = smem_addr(stage_base + s * kStageBytes);
-        const uint32_t sk = sq + kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t da = smem_desc_sw128(sq + kk * 32, 16, 1024);
-          const uint64_t db = smem_desc_sw128(sk + kk * 32, 16, 1024);
-          tc_mma_ss(tmem + kSCol0 + b * 128, da, db, idesc_s, kk > 0);
-        }
-        tc_commit(&bars->s_full[b]);
-      }
-      __syncwarp();
-      last_commit = &bars->s_full[b];
-      last_commit_parity = (n >> 1) & 1;
-      return true;
-    };
     // Issue whichever product is ready first: S for the next unit (its data
-    // landed, its S buffer is free) or P V for the oldest unit whose P is
-    // written.  Neither waits behind the other.
+    // landed, its warpgroup's S/P region was read by the previous P V) or
+    // P V for the oldest unit whose P is written.  Neither waits behind the
+    // other.
     int ns = 0, npv = 0;
     uint64_t t_idle = 0;
     while (npv < n_local) {
@@ -227,29 +262,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ns < n_local && ns <= npv + 1 && lane == 0)
         ready_s = mbar_probe(&bars->full[ns % kStages], (ns / kStages) & 1);
       if (__shfl_sync(0xffffffffu, ready_s, 0)) {
-        if (!issue_s(ns)) break;
+        const int s = ns % kStages, w = ns & 1;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sq = smem_addr(stage_base + s * kStageBytes);
+          const uint32_t sk = sq + kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            tc_mma_ss(tmem + kSCol0 + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
+                      smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
+          tc_commit(&bars->s_full[w]);
+        }
+        __syncwarp();
+        last_commit = &bars->s_full[w];
+        last_commit_parity = (ns >> 1) & 1;
         ++ns;
         progressed = true;
       }
       bool ready_pv = false;
       if (npv < ns && lane == 0)
         ready_pv = mbar_probe(&bars->p_full[npv & 1], (npv >> 1) & 1) &&
-                   mbar_probe(&bars->o_free[npv & 1], ((npv >> 1) & 1) ^ 1);
+                   mbar_probe(&bars->o_free[npv % kOBufs], ((npv / kOBufs) & 1) ^ 1);
       if (__shfl_sync(0xffffffffu, ready_pv, 0)) {
-        const int s = npv % kStages, b = npv & 1;
+        const int s = npv % kStages, w = npv & 1, ob = npv % kOBufs;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
-          const uint32_t sp = smem_addr(pbuf_base + b * kPBytes);
-          for (uint32_t kk = 0; kk < n_keys / 16; ++kk) {
-            // A = P (K-major, key block kk/4 of 64 keys, 32-byte step inside it)
-            const uint64_t da = smem_desc_sw128(
-                sp + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
-            // B = V (MN-major: 16 key rows per step, 64 value columns)
-            const uint64_t db = smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024);
-            tc_mma_ss(tmem + kOCol0 + b * kD, da, db, idesc_o, kk > 0);
-          }
-          tc_commit(&bars->pv_done[b]);
+          for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
+            // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
+            tc_mma_ts(tmem + kOCol0 + ob * kD, tmem + kSCol0 + w * 128 + kk * 8,
+                      smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
+          tc_commit(&bars->pv_done[ob]);
           tc_commit(&bars->empty[s]);
         }
         __syncwarp();
@@ -261,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (progressed) {
         t_idle = 0;
       } else {
+        // back off: a tight poll would take issue slots from the softmax warps
+        // that share this warp's SM sub-partition
+        __nanosleep(40);
         const uint64_t now = global_timer_ns();
         if (t_idle == 0) t_idle = now;
         if (*abort_flag) break;
@@ -270,29 +316,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+   }
   } else {
-    // ---- softmax + epilogue (warps 0-3; thread = tile row) -----------------
-    const int r = threadIdx.x;
+    regs_inc<kRegsSoftmax>();
+    // ---- softmax + epilogue: warpgroup w takes units n = w, w + 2, ... -----
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;  // tile row = TMEM lane
     const int pr = r / g.Rq, i = r % g.Rq;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_base + kSCol0 + w * 128;
+    // a negative scale is applied as |scale| to sign-flipped scores
+    const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
+    const float sl = fabsf(p.scale_log2);
 
     auto len_of = [&](int n) -> int {
       const int bh = (blockIdx.x + n * gridDim.x) * g.P + pr;
       const bool valid = pr < g.P && bh < BH && i < p.Lq;
       return valid ? clamp_len(p, bh / p.H) : 0;
     };
-    int len_cur = n_local > 0 ? len_of(0) : 0;
+    int len_cur = w < n_local ? len_of(w) : 0;
     float rowsum_prev = 0.f;  // row sum of the unit whose epilogue is pending
     bool pending_zero = true;
-    for (int n = 0; n <= n_local; ++n) {
+    for (int n = w; n < n_local + 2; n += 2) {
       float rowsum = 0.f;
       bool zero_row = true;
-      const int len_next = n + 1 < n_local ? len_of(n + 1) : 0;  // load ahead of its use
+      const int len_next = n + 2 < n_local ? len_of(n + 2) : 0;  // load ahead of its use
       if (n < n_local) {
-        const int b = n & 1;
-        const int u = blockIdx.x + n * gridDim.x;
-        const int bh = u * g.P + pr;
+        const int k = n >> 1;  // this warpgroup's k-th unit
+        const int bh = (blockIdx.x + n * gridDim.x) * g.P + pr;
         const bool valid = pr < g.P && bh < BH && i < p.Lq;
         const int len = len_cur;
         int jmax = p.Lk;
@@ -301,75 +352,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
         if (!valid || qpad) jmax = 0;
         const int col_lo = pr * g.Rk;
+        // 32-column chunks any row of this warp can use
+        const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
+        const unsigned hi = __reduce_max_sync(0xffffffffu, jmax > 0 ? col_lo + jmax : 0);
+        const int ch_lo = hi > 0 ? static_cast<int>(lo / 32) : 4;
+        const int ch_hi = hi > 0 ? static_cast<int>((hi + 31) / 32) : 0;
 
-        if (!mbar_wait(&bars->s_full[b], (n >> 1) & 1, abort_flag)) break;
+        if (!mbar_wait(&bars->s_full[w], k & 1, abort_flag)) break;
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          tmem_ld32(tmem + lane_base + kSCol0 + b * 128 + ch * 32, sr[ch]);
-        tmem_wait_ld();
-        tc_fence_before();
-        // scale (log2 units), keep only this row's keys [col_lo, col_lo + jmax)
-        const float m = scale_mask_max128(sr, p.scale_log2, true, col_lo, col_lo + jmax);
-        const bool any = m != -INFINITY;
-        rowsum = exp2_sum128(sr, m, any);
-        zero_row = !any;
-
-        // the P buffer b was last the staging tile of unit n-2's output store
-        if (threadIdx.x == 0) tma_store_wait_read0();
-        named_barrier_sync(1, kSoftmaxThreads);
-        const uint32_t sp = smem_addr(pbuf_base + b * kPBytes);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte pieces of 8 columns
-            uint32_t w[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              w[t] = pack_bf16x2(__uint_as_float(sr[ch][q4 * 8 + 2 * t]),
-                                 __uint_as_float(sr[ch][q4 * 8 + 2 * t + 1]));
-            const int c16 = ch * 4 + q4;  // 0..15
-            const uint32_t addr =
-                sp + (c16 >> 3) * (kTileRows * 128) + sw128_offset(r, c16 & 7);
-            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-          }
+        // keep only this row's keys [col_lo, col_lo + jmax); pass 1: row max
+        const int lo_c = col_lo, hi_c = col_lo + jmax;
+        float m = -INFINITY;
+#pragma unroll 1
+        for (int ch = ch_lo; ch < ch_hi; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(s_tmem + ch * 32, v);
+          tmem_wait_ld();
+          const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
+          chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
+          m = fmaxf(m, chunk_max(v));
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->p_full[b]);
+        const bool any = m != -INFINITY;
+        const float ms = any ? m * sl : 0.f;
+        zero_row = !any;
+        // pass 2: P = exp2(s * sl - ms) as bf16 pairs over the first 64
+        // columns of the S region (chunk ch -> columns [16 ch, 16 ch + 16),
+        // which pass 2 has already read); exactly 0 outside the row's keys
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pk[16];
+          if (ch >= ch_lo && ch < ch_hi) {
+            uint32_t v[32];
+            tmem_ld32(s_tmem + ch * 32, v);
+            tmem_wait_ld();
+            const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
+            chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
+            const float cs = chunk_exp_pack(v, sl, ms, pk);
+            rowsum += any ? cs : 0.f;
+            if (!any) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) pk[t] = 0u;
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) pk[t] = 0u;
+          }
+          tmem_st16(s_tmem + ch * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[w]);
       }
-      // epilogue of unit n-1 (its P V product ran while we did unit n)
-      if (n >= 1) {
-        const int pn = n - 1, b = pn & 1;
-        const int u = blockIdx.x + pn * gridDim.x;
-        if (!mbar_wait(&bars->pv_done[b], (pn >> 1) & 1, abort_flag)) break;
+      // epilogue of this warpgroup's previous unit (its P V ran meanwhile)
+      if (n - 2 >= 0 && n - 2 < n_local) {
+        const int pn = n - 2, ob = pn % kOBufs;
+        if (!mbar_wait(&bars->pv_done[ob], (pn / kOBufs) & 1, abort_flag)) break;
         tc_fence_after();
         uint32_t o[2][32];
-        tmem_ld32(tmem + lane_base + kOCol0 + b * kD, o[0]);
-        tmem_ld32(tmem + lane_base + kOCol0 + b * kD + 32, o[1]);
+        tmem_ld32(tmem + lane_base + kOCol0 + ob * kD, o[0]);
+        tmem_ld32(tmem + lane_base + kOCol0 + ob * kD + 32, o[1]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&bars->o_free[b]);
+        mbar_arrive(&bars->o_free[ob]);
+        // bf16 row into this warp's staging rows (128-byte swizzle), then
+        // lane 0 stores the warp's rows pair by pair (TMA clips rows >= Lq)
         const float inv = pending_zero ? 0.f : 1.f / rowsum_prev;
-        // stage the bf16 row in the (now free) P buffer b, 128-byte swizzled
-        const uint32_t so = smem_addr(pbuf_base + b * kPBytes);
+        uint8_t *stg = staging + warp * kStagingBytes;
+        const uint32_t so = smem_addr(stg);
+        if (lane == 0) tma_store_wait_read0();  // the previous store left this buffer
+        __syncwarp();
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          uint32_t w[4];
+          uint32_t wv[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const int c = c8 * 8 + 2 * t;
-            const float a0 = pending_zero ? 0.f : __uint_as_float(o[c >> 5][c & 31]) * inv;
-            const float a1 =
-                pending_zero ? 0.f : __uint_as_float(o[(c + 1) >> 5][(c + 1) & 31]) * inv;
-            w[t] = pack_bf16x2(a0, a1);
+            wv[t] = pending_zero ? 0u
+                                 : pack_bf16x2(__uint_as_float(o[c >> 5][c & 31]) * inv,
+                                               __uint_as_float(o[c >> 5][(c + 1) & 31]) * inv);
           }
-          st_shared_v4(so + sw128_offset(r, c8), w[0], w[1], w[2], w[3]);
+          st_shared_v4(so + sw128_offset(lane, c8), wv[0], wv[1], wv[2], wv[3]);
         }
         fence_proxy_async_smem();
-        named_barrier_sync(1, kSoftmaxThreads);
-        if (threadIdx.x == 0) {
-          tma_store_3d(&maps.o_store, pbuf_base + b * kPBytes, 0, 0, u * g.P);
+        __syncwarp();
+        if (lane == 0) {
+          const int bh0 = (blockIdx.x + pn * gridDim.x) * g.P;
+          const int rows = g.Rq < 32 ? g.Rq : 32;       // rows of one pair in this warp
+          const int h = rows >= 32 ? 2 : (rows == 16 ? 1 : 0);
+          for (int r0 = (warp & 3) * 32; r0 < (warp & 3) * 32 + 32; r0 += rows) {
+            const int ppair = r0 / g.Rq, i0 = r0 % g.Rq;
+            if (ppair < g.P && bh0 + ppair < BH && i0 < p.Lq)
+              tma_store_3d(&maps.o_rows[h], stg + (r0 - (warp & 3) * 32) * 128, 0, i0,
+                           bh0 + ppair);
+          }
           tma_store_commit();
         }
       }
@@ -377,16 +452,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       pending_zero = zero_row;
       len_cur = len_next;
     }
-    if (threadIdx.x == 0) tma_store_wait0();
+    if (lane == 0) tma_store_wait0();
   }
 
   // ---- teardown ------------------------------------------------------------
-  if (*abort_flag && warp == 4 && lane == 0) {
+  if (*abort_flag && warp == 8 && lane == 0) {
     // let copies already in flight land before the CTA's shared memory goes away
     for (int n = issued - kStages; n < issued; ++n)
       if (n >= 0) (void)wait_teardown(&bars->full[n % kStages], (n / kStages) & 1);
   }
-  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr) {
+  if (*abort_flag && warp == 9 && lane == 0 && last_commit != nullptr) {
     // tcgen05 ops complete in order: the last commit covers all of them
     (void)wait_teardown(last_commit, last_commit_parity);
   }
@@ -394,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -402,7 +477,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             int num_sms, cudaStream_t stream) {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_short_tc_kernel,
+  // setmaxnreg.inc only succeeds if the launch reserved the registers it hands
+  // out; refuse to launch a build whose register count would not cover them.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, attn_short_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(fa.numRegs) * kThreads <
+      2LL * 128 * kRegsSoftmax + 128LL * kRegsControl)
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(attn_short_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;

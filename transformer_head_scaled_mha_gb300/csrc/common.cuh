@@ -35,15 +35,18 @@ cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, floa
 
 // tensor maps for the bf16 tensor-core kernels: every map is 3-D
 // (d, L, B*H) over a [B, H, L, d] bf16 tensor with 128-byte swizzle
+constexpr int kRowBoxes = 4;  // row-box heights 8, 16, 32, 64
 struct ShortMaps {
   CUtensorMap q_full, k_full, v_full;  // box (64, Rq|Rk, P)
-  CUtensorMap q_rows, k_rows, v_rows;  // box (64, 8, 1), for padded tensors
-  CUtensorMap o_store;                 // box (64, Rq, P)
+  CUtensorMap q_rows[kRowBoxes];       // box (64, 8 << h, 1), for padded tensors
+  CUtensorMap k_rows[kRowBoxes];
+  CUtensorMap v_rows[kRowBoxes];
+  CUtensorMap o_rows[3];               // box (64, 8 << h, 1): output stores
 };
 struct ShortGeom {
-  int Rq, Rk, P;  // rows per packed pair (powers of two) and pairs per unit
-  int units;      // ceil(B*H / P)
-  int rows_q, rows_k;  // load Q/K/V per 8-row box when nonzero (padding)
+  int Rq, Rk, P;       // rows per packed pair (powers of two) and pairs per unit
+  int units;           // ceil(B*H / P)
+  int rows_q, rows_k;  // load Q / K,V only up to each pair's length (padding)
 };
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             int num_sms, cudaStream_t stream);
