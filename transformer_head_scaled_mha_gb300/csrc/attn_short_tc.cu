@@ -191,10 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // Rows that a padded unit does not load keep earlier contents; start from
-  // zeros so they are always finite (their weights are exactly zero).
-  for (int i = threadIdx.x; i < kStages * kStageBytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(stage_base)[i] = make_uint4(0, 0, 0, 0);
+  // V rows that a padded unit does not load keep earlier contents; start
+  // from zeros so they are always finite (their weights are exactly zero, and
+  // 0 * NaN would not be).  Unloaded K and Q rows are masked by selection.
+  for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads) {
+    const int st = i / (kTileBytes / 16), off = i % (kTileBytes / 16);
+    reinterpret_cast<uint4 *>(stage_base + st * kStageBytes + 2 * kTileBytes)[off] =
+        make_uint4(0, 0, 0, 0);
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();

@@ -42,6 +42,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// Probe that may suspend the thread for up to `hint_ns` (it wakes as soon as
+// the phase completes); returns whether the phase completed.
+__device__ __forceinline__ bool mbar_try_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // non-blocking probe of a phase (test_wait never suspends the thread)
 __device__ __forceinline__ bool mbar_probe(uint64_t *bar, uint32_t parity) {
   uint32_t done;
