@@ -213,6 +213,12 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def weak_scaling_value(spec, nbytes, flops, slowest_seconds, world: int) -> float:
+    """Whole-job throughput: every rank ran the same launch; all ranks' work
+    divided by the slowest rank's time."""
+    return throughput(spec, nbytes, flops, slowest_seconds) * world
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -284,6 +290,7 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    # every rank runs the same workload on its own GPU (weak scaling)
 
     spec = gen.WORKLOADS[args.workload]
     dt = spec["dtype"]
@@ -361,8 +368,7 @@ def run_ours(args):
     elapsed = ev0.elapsed_time(ev1) / 1e3
     elapsed = max_over_ranks(elapsed, world, dev)
     per_launch = elapsed / args.steps
-    value_rank = throughput(spec, nbytes, flops, per_launch)
-    value = value_rank * world
+    value = weak_scaling_value(spec, nbytes, flops, per_launch, world)
     st = mha.mha_debug_status(stream)
     if st != mha.MHA_OK:
         raise RuntimeError("device status after timing: %s" % mha.mha_status_string(st))
@@ -399,7 +405,7 @@ def run_ours(args):
         e1.record(stream)
     stream.synchronize()
     e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / e2e_steps
-    e2e_value = throughput(spec, nbytes, flops, e2e_t) * world
+    e2e_value = weak_scaling_value(spec, nbytes, flops, e2e_t, world)
 
     peaks, peak_src = read_peaks()
     if bound_of(spec) == "tensor":
