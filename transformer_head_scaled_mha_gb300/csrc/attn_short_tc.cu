@@ -23,10 +23,9 @@
 //   O = P V                tcgen05.mma (A = P from TMEM) -> TMEM, 4 buffers
 //   O / rowsum -> bf16     tcgen05.ld; each warp stages its 32 rows in a
 //                          swizzled 4 KiB buffer and TMA-stores them
-// Padded sequences load only their first ceil(len/8)*8 rows, as at most four
-// TMA boxes of 64/32/16/8 rows per tensor and pair, so padding costs no HBM
-// reads (a CTA's first unit loads whole tiles instead, so it does not wait
-// for the lengths).  Masked keys get exactly zero weight; padded query rows
+// Padded sequences load only their first ceil(len/8)*8 rows, as one TMA box
+// of that height per tensor and pair, so padding costs no HBM reads (a CTA's
+// first unit loads whole tiles instead, so it does not wait for the lengths).  Masked keys get exactly zero weight; padded query rows
 // and rows without any allowed key are stored as +0.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -84,21 +83,16 @@ __device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
   return true;
 }
 
-// Rows [0, rows) of one pair as boxes of 64 rows, then one each of 32, 16 and
-// 8 rows as the remainder needs (rows rounded up to a multiple of 8).
+// Rows [0, rows) of one pair (rounded up to a multiple of 8) as one TMA box
+// of exactly that height: each box costs the TMA unit a fixed overhead, so
+// one box per pair and tensor beats a split into power-of-two pieces.
 __device__ __forceinline__ uint32_t box_bytes(int rows) {
   return static_cast<uint32_t>((rows + 7) / 8) * 1024u;
 }
 __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *maps, uint64_t *bar,
                                           int rows, int bh) {
-  int n8 = (rows + 7) / 8, r0 = 0;
-  for (; n8 >= 8; n8 -= 8, r0 += 64) tma_load_3d(dst + r0 * 128, &maps[3], bar, 0, r0, bh);
-#pragma unroll
-  for (int h = 2; h >= 0; --h)
-    if (n8 & (1 << h)) {
-      tma_load_3d(dst + r0 * 128, &maps[h], bar, 0, r0, bh);
-      r0 += 8 << h;
-    }
+  const int n8 = (rows + 7) / 8;
+  if (n8 > 0) tma_load_3d(dst, &maps[n8 - 1], bar, 0, 0, bh);
 }
 
 // One 32-column chunk of a row's scores (raw fp32 bits), sign-flipped by
@@ -194,16 +188,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // V rows that a padded unit does not load keep earlier contents; start
   // from zeros so they are always finite (their weights are exactly zero, and
   // 0 * NaN would not be).  Unloaded K and Q rows are masked by selection.
-  for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads) {
-    const int st = i / (kTileBytes / 16), off = i % (kTileBytes / 16);
-    reinterpret_cast<uint4 *>(stage_base + st * kStageBytes + 2 * kTileBytes)[off] =
-        make_uint4(0, 0, 0, 0);
+  if (g.rows_k) {
+    for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads) {
+      const int st = i / (kTileBytes / 16), off = i % (kTileBytes / 16);
+      reinterpret_cast<uint4 *>(stage_base + st * kStageBytes + 2 * kTileBytes)[off] =
+          make_uint4(0, 0, 0, 0);
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // Everything above overlaps the previous launch's tail when launched as a
+  // programmatic dependent; global memory is touched only after this wait.
+  griddep_wait();
+  griddep_launch_dependents();
 
   int issued = 0;                   // producer: units whose loads were issued
   uint64_t *last_commit = nullptr;  // MMA issuer: barrier of the last commit
@@ -213,13 +213,24 @@ __global__ void __launch_bounds__(kThreads, 1)
    if (warp == 8) {
     // ---- TMA producer (lane pp handles pair pp of the unit) -----------------
     const int pp = lane;
+    const bool need_len = g.rows_q || g.rows_k;
+    // lane pp's pair length for unit n, read two units ahead of its use
+    auto len_at = [&](int n) -> int {
+      const int bh = (blockIdx.x + n * gridDim.x) * g.P + pp;
+      return (need_len && n < n_local && pp < g.P && bh < BH) ? clamp_len(p, bh / p.H) : 0;
+    };
+    int len_n1 = len_at(1), len_n2 = len_at(2);
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
       const int bh0 = (blockIdx.x + n * gridDim.x) * g.P;
       // the first unit loads whole tiles: no wait for the lengths
       const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
       const bool has_pair = pp < g.P && bh0 + pp < BH;
-      const int len = (has_pair && (rows_q || rows_k)) ? clamp_len(p, (bh0 + pp) / p.H) : 0;
+      const int len = n > 0 ? len_n1 : 0;
+      if (n > 0) {
+        len_n1 = len_n2;
+        len_n2 = len_at(n + 2);
+      }
       uint32_t bytes = 0;
       if (has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
       if (has_pair && rows_k) bytes += 2 * box_bytes(len);
@@ -495,8 +506,20 @@ cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Pro
   if (e != cudaSuccess) return e;
   const int grid = g.units < num_sms ? g.units : num_sms;
   if (grid <= 0) return cudaSuccess;
-  attn_short_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, g, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: this grid's set-up may overlap the end of
+  // the previous kernel in the stream (the kernel waits before any global
+  // memory access), and the next launch may do the same with this one
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_short_tc_kernel, maps, g, p);
 }
 
 }  // namespace mha

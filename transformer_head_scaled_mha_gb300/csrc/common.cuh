@@ -35,10 +35,10 @@ cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, floa
 
 // tensor maps for the bf16 tensor-core kernels: every map is 3-D
 // (d, L, B*H) over a [B, H, L, d] bf16 tensor with 128-byte swizzle
-constexpr int kRowBoxes = 4;  // row-box heights 8, 16, 32, 64
+constexpr int kRowBoxes = 16;  // row-box heights 8, 16, ..., 128
 struct ShortMaps {
   CUtensorMap q_full, k_full, v_full;  // box (64, Rq|Rk, P)
-  CUtensorMap q_rows[kRowBoxes];       // box (64, 8 << h, 1), for padded tensors
+  CUtensorMap q_rows[kRowBoxes];       // box (64, 8 (h + 1), 1), for padded tensors
   CUtensorMap k_rows[kRowBoxes];
   CUtensorMap v_rows[kRowBoxes];
   CUtensorMap o_rows[3];               // box (64, 8 << h, 1): output stores

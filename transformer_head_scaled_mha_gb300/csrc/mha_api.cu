@@ -182,10 +182,12 @@ extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, i
       bool ok = make_map(&m.q_full, q, 64, Lq, bh, g.Rq, g.P) &&
                 make_map(&m.k_full, k, 64, Lk, bh, g.Rk, g.P) &&
                 make_map(&m.v_full, v, 64, Lk, bh, g.Rk, g.P);
-      for (int h = 0; ok && h < kRowBoxes; ++h)
-        ok = make_map(&m.q_rows[h], q, 64, Lq, bh, 8 << h, 1) &&
-             make_map(&m.k_rows[h], k, 64, Lk, bh, 8 << h, 1) &&
-             make_map(&m.v_rows[h], v, 64, Lk, bh, 8 << h, 1);
+      // one row-box map per height 8, 16, ..., Rq (Rk) for the padded tensors
+      for (int h = 0; ok && g.rows_q && h < g.Rq / 8; ++h)
+        ok = make_map(&m.q_rows[h], q, 64, Lq, bh, 8 * (h + 1), 1);
+      for (int h = 0; ok && g.rows_k && h < g.Rk / 8; ++h)
+        ok = make_map(&m.k_rows[h], k, 64, Lk, bh, 8 * (h + 1), 1) &&
+             make_map(&m.v_rows[h], v, 64, Lk, bh, 8 * (h + 1), 1);
       for (int h = 0; ok && h < 3; ++h) ok = make_map(&m.o_rows[h], out, 64, Lq, bh, 8 << h, 1);
       if (!ok) return MHA_ERR_CUDA;
       err = launch_short_tc(m, g, p, sms, stream);

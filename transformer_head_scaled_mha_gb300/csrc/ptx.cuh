@@ -101,6 +101,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Blocks until the grid this launch depends on has completed and its memory
+// operations are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next dependent launch in the stream start its CTAs early (they
+// still run their own griddep_wait before touching global memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // fences
 // ---------------------------------------------------------------------------
 // generic-proxy shared-memory writes -> visible to the async proxy (TMA store,
