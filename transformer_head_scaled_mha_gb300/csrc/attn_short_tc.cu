@@ -265,71 +265,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t n_keys = static_cast<uint32_t>(g.P * g.Rk);  // multiple of 16, <= 128
     const uint32_t idesc_s = idesc_bf16_f32(128, n_keys, 0);
     const uint32_t idesc_o = idesc_bf16_f32(128, kD, 1);
-    // Issue whichever product is ready first: S for the next unit (its data
-    // landed, its warpgroup's S/P region was read by the previous P V) or
-    // P V for the oldest unit whose P is written.  Neither waits behind the
-    // other.
-    int ns = 0, npv = 0;
-    uint64_t t_idle = 0;
-    while (npv < n_local) {
-      bool progressed = false;
-      bool ready_s = false;
-      if (ns < n_local && ns <= npv + 1 && lane == 0)
-        ready_s = mbar_probe(&bars->full[ns % kStages], (ns / kStages) & 1);
-      if (__shfl_sync(0xffffffffu, ready_s, 0)) {
-        const int s = ns % kStages, w = ns & 1;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sq = smem_addr(stage_base + s * kStageBytes);
-          const uint32_t sk = sq + kTileBytes;
+    // Fixed order S_0, S_1, then for each unit n: P V for n, S for n + 2.
+    // S_{n+2} reuses warpgroup (n % 2)'s S region, free once its softmax of
+    // unit n finished (p_full) -- which P V for n also needs.  Every wait
+    // suspends in hardware until its phase completes.
+    auto issue_s = [&](int ns) -> bool {
+      const int s = ns % kStages, w = ns & 1;
+      if (!mbar_wait(&bars->full[s], (ns / kStages) & 1, abort_flag)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sq = smem_addr(stage_base + s * kStageBytes);
+        const uint32_t sk = sq + kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            tc_mma_ss(tmem + kSCol0 + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
-                      smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
-          tc_commit(&bars->s_full[w]);
-        }
-        __syncwarp();
-        last_commit = &bars->s_full[w];
-        last_commit_parity = (ns >> 1) & 1;
-        ++ns;
-        progressed = true;
+        for (int kk = 0; kk < kD / 16; ++kk)
+          tc_mma_ss(tmem + kSCol0 + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
+                    smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
+        tc_commit(&bars->s_full[w]);
       }
-      bool ready_pv = false;
-      if (npv < ns && lane == 0)
-        ready_pv = mbar_probe(&bars->p_full[npv & 1], (npv >> 1) & 1) &&
-                   mbar_probe(&bars->o_free[npv % kOBufs], ((npv / kOBufs) & 1) ^ 1);
-      if (__shfl_sync(0xffffffffu, ready_pv, 0)) {
-        const int s = npv % kStages, w = npv & 1, ob = npv % kOBufs;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
-          for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
-            // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
-            tc_mma_ts(tmem + kOCol0 + ob * kD, tmem + kSCol0 + w * 128 + kk * 8,
-                      smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
-          tc_commit(&bars->pv_done[ob]);
-          tc_commit(&bars->empty[s]);
-        }
-        __syncwarp();
-        last_commit = &bars->empty[s];
-        last_commit_parity = (npv / kStages) & 1;
-        ++npv;
-        progressed = true;
+      __syncwarp();
+      last_commit = &bars->s_full[w];
+      last_commit_parity = (ns >> 1) & 1;
+      return true;
+    };
+    bool ok = true;
+    for (int ns = 0; ok && ns < 2 && ns < n_local; ++ns) ok = issue_s(ns);
+    for (int n = 0; ok && n < n_local; ++n) {
+      const int s = n % kStages, w = n & 1, ob = n % kOBufs;
+      if (!mbar_wait(&bars->p_full[w], (n >> 1) & 1, abort_flag)) break;
+      if (!mbar_wait(&bars->o_free[ob], ((n / kOBufs) & 1) ^ 1, abort_flag)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
+        for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
+          // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
+          tc_mma_ts(tmem + kOCol0 + ob * kD, tmem + kSCol0 + w * 128 + kk * 8,
+                    smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
+        tc_commit(&bars->pv_done[ob]);
+        tc_commit(&bars->empty[s]);
       }
-      if (progressed) {
-        t_idle = 0;
-      } else {
-        // back off: a tight poll would take issue slots from the softmax warps
-        // that share this warp's SM sub-partition
-        __nanosleep(40);
-        const uint64_t now = global_timer_ns();
-        if (t_idle == 0) t_idle = now;
-        if (*abort_flag) break;
-        if (now - t_idle > kWaitLimitNs) {
-          *abort_flag = 1;
-          break;
-        }
-      }
+      __syncwarp();
+      last_commit = &bars->empty[s];
+      last_commit_parity = (n / kStages) & 1;
+      if (n + 2 < n_local) ok = issue_s(n + 2);
     }
    }
   } else {
