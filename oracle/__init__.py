@@ -52,10 +52,11 @@ def _load():
         if _lib is None:
             build()
             lib = ctypes.CDLL(_LIB)
-            lib.oracle_mha_rows_f64.restype = ctypes.c_int
-            lib.oracle_mha_rows_f64.argtypes = [
+            lib.oracle_mha_rows_ex_f64.restype = ctypes.c_int
+            lib.oracle_mha_rows_ex_f64.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
@@ -74,25 +75,38 @@ def _ptr(a):
 
 def mha_fwd(q, k, v, *, mask_kind: int = 0, key_lengths=None, scale: float,
             rows=None, threads: int = 0, return_weights: bool = False,
-            return_scores: bool = False):
+            return_scores: bool = False, layout: str = "bhsd"):
     """Attention output in float64.
 
-    q [B,H,Lq,dk], k [B,H,Lk,dk], v [B,H,Lk,dv]: float64, float32 or uint16
-    (bfloat16 bit patterns), all the same type.  ``key_lengths`` int [B].
-    ``rows``: optional flat row indices (b*H + h)*Lq + i; then the result is
-    [len(rows), dv] (and [len(rows), Lk] for weights/scores), else
-    [B,H,Lq,dv] ([B,H,Lq,Lk]).
+    layout "bhsd": q [B,H,Lq,dk], k [B,Hkv,Lk,dk], v [B,Hkv,Lk,dv];
+    layout "bshd": q [B,Lq,H,dk], k [B,Lk,Hkv,dk], v [B,Lk,Hkv,dv].
+    Hkv (taken from k) divides H; query head h reads key/value head
+    h // (H // Hkv).  Arrays: float64, float32 or uint16 (bfloat16 bit
+    patterns), all the same type.  ``key_lengths`` int [B].
+    ``rows``: optional logical row indices (b*H + h)*Lq + i; then the result is
+    [len(rows), dv] (and [len(rows), Lk] for weights/scores), else the output
+    in the inputs' layout and weights/scores as [B,H,Lq,Lk].
     """
     q = np.ascontiguousarray(q)
     k = np.ascontiguousarray(k)
     v = np.ascontiguousarray(v)
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _IN_CODES:
         raise TypeError("q, k, v must share one of float64, float32, uint16(bf16)")
-    B, H, Lq, dk = q.shape
-    Bk, Hk, Lk, dk2 = k.shape
-    Bv, Hv, Lk2, dv = v.shape
-    if (Bk, Hk, dk2) != (B, H, dk) or (Bv, Hv, Lk2) != (B, H, Lk):
+    if layout not in ("bhsd", "bshd"):
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    bshd = layout == "bshd"
+    if bshd:
+        B, Lq, H, dk = q.shape
+        Bk, Lk, Hkv, dk2 = k.shape
+        Bv, Lk2, Hv, dv = v.shape
+    else:
+        B, H, Lq, dk = q.shape
+        Bk, Hkv, Lk, dk2 = k.shape
+        Bv, Hv, Lk2, dv = v.shape
+    if (Bk, dk2) != (B, dk) or (Bv, Hv, Lk2) != (B, Hkv, Lk):
         raise ValueError("shape mismatch")
+    if Hkv <= 0 and H > 0 or (Hkv > 0 and H % Hkv):
+        raise ValueError("key/value heads must divide query heads")
     kl = None
     if key_lengths is not None:
         kl = np.ascontiguousarray(key_lengths, dtype=np.int32)
@@ -109,12 +123,15 @@ def mha_fwd(q, k, v, *, mask_kind: int = 0, key_lengths=None, scale: float,
     out = np.zeros(oshape, dtype=np.float64)
     w = np.zeros(wshape, dtype=np.float64) if return_weights else None
     s = np.zeros(wshape, dtype=np.float64) if return_scores else None
-    rc = _load().oracle_mha_rows_f64(
-        _ptr(q), _ptr(k), _ptr(v), _IN_CODES[q.dtype], B, H, Lq, Lk, dk, dv,
+    rc = _load().oracle_mha_rows_ex_f64(
+        _ptr(q), _ptr(k), _ptr(v), _IN_CODES[q.dtype], B, H, max(Hkv, 1) if H == 0 else Hkv,
+        Lq, Lk, dk, dv, 1 if bshd else 0,
         int(mask_kind), _ptr(kl), float(scale), _ptr(rows_a), nrows,
         _ptr(out), _ptr(w), _ptr(s), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    if rows is None and bshd:
+        out = np.ascontiguousarray(out.transpose(0, 2, 1, 3))
     res = [out]
     if return_weights:
         res.append(w)

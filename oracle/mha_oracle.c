@@ -35,7 +35,13 @@
  * widened exactly to double.  Rows are independent; OpenMP spreads them over
  * host threads without changing any row's arithmetic.
  *
- * Layouts: q [B,H,Lq,dk], k [B,H,Lk,dk], v [B,H,Lk,dv], all contiguous.
+ * Layouts (contiguous): layout 0 ("BHSD", the per-head layout after the head
+ * split): q [B,H,Lq,dk], k [B,Hkv,Lk,dk], v [B,Hkv,Lk,dv]; layout 1 ("BSHD",
+ * the layout before the split): q [B,Lq,H,dk], k [B,Lk,Hkv,dk],
+ * v [B,Lk,Hkv,dv].  Hkv key/value heads serve H query heads, Hkv dividing H:
+ * query head h reads key/value head h / (H / Hkv) (zeroshotmind.com, "Many
+ * heads, many subspaces": grouped- and multi-query attention share or
+ * collapse the key/value heads).  Hkv == H is plain multi-head attention.
  */
 #include <math.h>
 #include <stdint.h>
@@ -66,20 +72,31 @@ int oracle_max_threads(void) {
 #endif
 }
 
+/* element offset of (b, head, position, c) in a tensor of `heads` heads,
+   `len` positions and `d` columns */
+static int64_t offset(int layout, int64_t b, int64_t head, int64_t pos, int64_t c, int64_t heads,
+                      int64_t len, int64_t d) {
+  if (layout == 0) return ((b * heads + head) * len + pos) * d + c;
+  return ((b * len + pos) * heads + head) * d + c;
+}
+
 /*
- * Computes the rows listed in `rows` (flat index (b*H + h)*Lq + i), or every
- * row in order when rows == NULL (then nrows must be B*H*Lq).
+ * Computes the rows listed in `rows` (logical index (b*H + h)*Lq + i,
+ * whatever the layout), or every row in that order when rows == NULL (then
+ * nrows must be B*H*Lq).
  *   out     [nrows, dv]           attention output rows
  *   weights [nrows, Lk] or NULL   softmax weights (0 outside A_i)
  *   scores  [nrows, Lk] or NULL   scaled logits s_j (-inf outside A_i)
  * Returns 0 on success, 1 on an invalid argument.
  */
-int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtype,
-                        int B, int H, int Lq, int Lk, int dk, int dv,
-                        int mask_kind, const int32_t *key_lengths, double scale,
-                        const int64_t *rows, int64_t nrows,
-                        double *out, double *weights, double *scores, int nthreads) {
+int oracle_mha_rows_ex_f64(const void *q, const void *k, const void *v, int in_dtype,
+                           int B, int H, int Hkv, int Lq, int Lk, int dk, int dv, int layout,
+                           int mask_kind, const int32_t *key_lengths, double scale,
+                           const int64_t *rows, int64_t nrows,
+                           double *out, double *weights, double *scores, int nthreads) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk < 0 || dv < 0) return 1;
+  if (Hkv <= 0 ? H > 0 : (H % Hkv) != 0) return 1;
+  if (layout != 0 && layout != 1) return 1;
   if (in_dtype < ORACLE_IN_F64 || in_dtype > ORACLE_IN_BF16) return 1;
   if (mask_kind & ~(ORACLE_CAUSAL | ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) return 1;
   if ((mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)) && Lq != Lk) return 1;
@@ -137,14 +154,14 @@ int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtyp
       /* step 3 */
       if (n_allowed == 0) continue;
       /* step 4 */
-      const int64_t qbase = row * dk;
-      const int64_t kbase = bh * (int64_t)Lk * dk;
-      const int64_t vbase = bh * (int64_t)Lk * dv;
+      const int h = (int)(bh % H);
+      const int hk = h / (H / Hkv);
       for (int j = 0; j < Lk; ++j) {
         if (!allowed[j]) continue;
         double dot = 0.0;
         for (int c = 0; c < dk; ++c)
-          dot += widen(q, in_dtype, qbase + c) * widen(k, in_dtype, kbase + (int64_t)j * dk + c);
+          dot += widen(q, in_dtype, offset(layout, b, h, i, c, H, Lq, dk)) *
+                 widen(k, in_dtype, offset(layout, b, hk, j, c, Hkv, Lk, dk));
         s[j] = scale * dot;
         if (sc) sc[j] = s[j];
       }
@@ -163,11 +180,22 @@ int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtyp
         if (!allowed[j]) continue;
         const double wj = s[j] / denom;
         if (w) w[j] = wj;
-        for (int c = 0; c < dv; ++c) o[c] += wj * widen(v, in_dtype, vbase + (int64_t)j * dv + c);
+        for (int c = 0; c < dv; ++c)
+          o[c] += wj * widen(v, in_dtype, offset(layout, b, hk, j, c, Hkv, Lk, dv));
       }
     }
     free(s);
     free(allowed);
   }
   return bad ? 1 : 0;
+}
+
+/* multi-head attention in the per-head layout (Hkv == H, layout 0) */
+int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtype,
+                        int B, int H, int Lq, int Lk, int dk, int dv,
+                        int mask_kind, const int32_t *key_lengths, double scale,
+                        const int64_t *rows, int64_t nrows,
+                        double *out, double *weights, double *scores, int nthreads) {
+  return oracle_mha_rows_ex_f64(q, k, v, in_dtype, B, H, H, Lq, Lk, dk, dv, 0, mask_kind,
+                                key_lengths, scale, rows, nrows, out, weights, scores, nthreads);
 }

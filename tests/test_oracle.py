@@ -319,3 +319,49 @@ def test_brute_force_high_precision(oracle_lib, mask, lens):
                     else:
                         ref = mp.fsum(e[j] * mp.mpf(v[b, h, j, c]) for j in range(L)) / z
                     assert abs(float(ref) - out[b, h, i, c]) < 1e-14
+
+
+# --------------------------------------------------------------------------
+# grouped key/value heads and the [B, L, H, d] layout, pinned to the
+# multi-head oracle above
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("mask,lens", MASKS)
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (6, 1), (6, 3)])
+def test_grouped_heads_equal_repeated_heads(oracle_lib, mask, lens, H, Hkv):
+    # Sharing key/value head g among H/Hkv query heads is multi-head attention
+    # with that head repeated (zeroshotmind.com, "Many heads, many subspaces").
+    B, L, d = 4, 9, 5
+    q = gen.tensor(3, 0, (B, H, L, d), "f64")
+    k = gen.tensor(3, 1, (B, Hkv, L, d), "f64")
+    v = gen.tensor(3, 2, (B, Hkv, L, d), "f64")
+    got = oracle.mha_fwd(q, k, v, mask_kind=mask, key_lengths=lens, scale=0.45)
+    rep = H // Hkv
+    ref = oracle.mha_fwd(q, np.repeat(k, rep, axis=1), np.repeat(v, rep, axis=1),
+                         mask_kind=mask, key_lengths=lens, scale=0.45)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("mask,lens", MASKS)
+def test_bshd_layout_equals_bhsd(oracle_lib, mask, lens):
+    # the layout before the head split, [B, L, h, d_k] (aicassindra.com, "A
+    # faithful layer in code"), holds the same numbers as [B, h, L, d_k]
+    B, H, Hkv, L, d = 4, 4, 2, 9, 5
+    q = gen.tensor(4, 0, (B, H, L, d), "f64")
+    k = gen.tensor(4, 1, (B, Hkv, L, d), "f64")
+    v = gen.tensor(4, 2, (B, Hkv, L, d), "f64")
+    ref = oracle.mha_fwd(q, k, v, mask_kind=mask, key_lengths=lens, scale=0.3)
+    t = lambda a: np.ascontiguousarray(a.transpose(0, 2, 1, 3))
+    got = oracle.mha_fwd(t(q), t(k), t(v), mask_kind=mask, key_lengths=lens, scale=0.3,
+                         layout="bshd")
+    np.testing.assert_array_equal(got, t(ref))
+    rows = np.array([0, 7, 20, 35, 143])
+    np.testing.assert_array_equal(
+        oracle.mha_fwd(t(q), t(k), t(v), mask_kind=mask, key_lengths=lens, scale=0.3,
+                       layout="bshd", rows=rows), ref.reshape(-1, d)[rows])
+
+
+def test_grouped_heads_reject_non_divisor(oracle_lib):
+    q = np.zeros((1, 4, 3, 2))
+    k = np.zeros((1, 3, 3, 2))
+    with pytest.raises(ValueError):
+        oracle.mha_fwd(q, k, k, scale=1.0)
