@@ -177,12 +177,21 @@ def default_scale(dk: int) -> float:
 
 
 def make_inputs(spec: dict, seed: int = 0):
-    """Q, K, V (layout [B, H, L, d]) and key lengths for a workload spec."""
+    """Q, K, V and key lengths for a workload spec.
+
+    Layout spec["layout"] ("bhsd" [B, heads, L, d], the default, or "bshd"
+    [B, L, heads, d]); K and V have spec["Hkv"] heads (default H).
+    """
     B, H, Lq, Lk = spec["B"], spec["H"], spec["Lq"], spec["Lk"]
     dk, dv, dt, amp = spec["dk"], spec["dv"], spec["dtype"], spec.get("amp", 1.0)
-    q = tensor(seed, STREAM_Q, (B, H, Lq, dk), dt, amp)
-    k = tensor(seed, STREAM_K, (B, H, Lk, dk), dt, amp)
-    v = tensor(seed, STREAM_V, (B, H, Lk, dv), dt, amp)
+    Hkv = spec.get("Hkv", H)
+    if spec.get("layout", "bhsd") == "bshd":
+        qs, ks, vs = (B, Lq, H, dk), (B, Lk, Hkv, dk), (B, Lk, Hkv, dv)
+    else:
+        qs, ks, vs = (B, H, Lq, dk), (B, Hkv, Lk, dk), (B, Hkv, Lk, dv)
+    q = tensor(seed, STREAM_Q, qs, dt, amp)
+    k = tensor(seed, STREAM_K, ks, dt, amp)
+    v = tensor(seed, STREAM_V, vs, dt, amp)
     lr = spec.get("len_range")
     lens = lengths(seed, B, lr[0], lr[1]) if lr is not None else None
     return q, k, v, lens

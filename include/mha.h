@@ -57,6 +57,16 @@ enum {
 /* encoder self-attention over padded sentences: KEY_PADDING | QUERY_PADDING;
    cross-attention over a padded source: KEY_PADDING; decoder: CAUSAL. */
 
+/* Memory layout of q, k, v and out (mha_fwd_ex; all four share it). */
+enum {
+  /* [B, heads, L, d]: the per-head layout after the head split and transpose
+     (aicassindra.com, "A faithful layer in code") */
+  MHA_LAYOUT_BHSD = 0,
+  /* [B, L, heads, d]: the projection output viewed as heads, before the
+     transpose, so no transpose copy is needed on either side of the call */
+  MHA_LAYOUT_BSHD = 1
+};
+
 typedef enum {
   MHA_OK = 0,
   MHA_ERR_INVALID_ARGUMENT = 1, /* rejected before any launch              */
@@ -102,6 +112,36 @@ int mha_fwd(const void *q, const void *k, const void *v, void *out,
             int B, int H, int Lq, int Lk, int d_k, int d_v,
             int mask_kind, const int32_t *key_lengths,
             float scale, int dtype, void *stream);
+
+/*
+ * mha_fwd_ex -- mha_fwd with shared key/value heads and a choice of layout.
+ *
+ * Grouped-query and multi-query attention are multi-head attention whose key
+ * and value heads are shared by groups of query heads, or collapsed into one
+ * (zeroshotmind.com, "Many heads, many subspaces"; trishampatil.com,
+ * "Limitations of the Original Design").  Query head h reads key/value head
+ * h / (H / H_kv):
+ *
+ *     out[b,h,i,:] = sum_j softmax_j( scale * q[b,h,i,:] . k[b,g,j,:] ) v[b,g,j,:],
+ *     g = h / (H / H_kv)
+ *
+ * H_kv                  key/value heads, > 0 and dividing H (H_kv == H is
+ *                       plain multi-head attention, H_kv == 1 multi-query)
+ * layout                MHA_LAYOUT_BHSD: q [B, H, Lq, d_k], k [B, H_kv, Lk, d_k],
+ *                       v [B, H_kv, Lk, d_v], out [B, H, Lq, d_v];
+ *                       MHA_LAYOUT_BSHD: q [B, Lq, H, d_k], k [B, Lk, H_kv, d_k],
+ *                       v [B, Lk, H_kv, d_v], out [B, Lq, H, d_v]
+ *
+ * Every other argument, the ownership rules and the error behaviour are those
+ * of mha_fwd; an H_kv that does not divide H, or another layout value, is
+ * MHA_ERR_INVALID_ARGUMENT.  mha_fwd(...) equals mha_fwd_ex with H_kv = H and
+ * MHA_LAYOUT_BHSD.  The kernel choice does not depend on H_kv or the layout
+ * (mha_fwd_path applies).
+ */
+int mha_fwd_ex(const void *q, const void *k, const void *v, void *out,
+               int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
+               int mask_kind, const int32_t *key_lengths,
+               float scale, int dtype, void *stream);
 
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed

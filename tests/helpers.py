@@ -30,14 +30,20 @@ def as_f64(a, dtype):
 
 
 def run_gpu(q, k, v, lens, spec, scale=None, mask=None):
+    """The CUDA path on one case: mha_fwd for plain multi-head attention in
+    [B, H, L, d], mha_fwd_ex for shared key/value heads or [B, L, H, d]."""
     import torch
     import transformer_head_scaled_mha_gb300 as mha
     dt = spec["dtype"]
     scale = gen.default_scale(spec["dk"]) if scale is None else scale
     mask = spec["mask"] if mask is None else mask
     kl = torch.from_numpy(np.asarray(lens, dtype=np.int32)).cuda() if lens is not None else None
-    out = mha.mha_fwd(to_device(q, dt), to_device(k, dt), to_device(v, dt), mask_kind=mask,
-                      key_lengths=kl, scale=scale)
+    layout = spec.get("layout", "bhsd")
+    args = (to_device(q, dt), to_device(k, dt), to_device(v, dt))
+    if layout == "bhsd" and spec.get("Hkv", spec["H"]) == spec["H"]:
+        out = mha.mha_fwd(*args, mask_kind=mask, key_lengths=kl, scale=scale)
+    else:
+        out = mha.mha_fwd_ex(*args, layout=layout, mask_kind=mask, key_lengths=kl, scale=scale)
     torch.cuda.synchronize()
     return from_device(out)
 
@@ -72,11 +78,18 @@ def check_case(spec, seed=0, rows=None, scale=None, mask=None, label=""):
     q, k, v, lens = gen.make_inputs(spec, seed=seed)
     mask = spec["mask"] if mask is None else mask
     scale = gen.default_scale(spec["dk"]) if scale is None else scale
+    layout = spec.get("layout", "bhsd")
     out = run_gpu(q, k, v, lens, spec, scale=scale, mask=mask)
-    ref = oracle.mha_fwd(q, k, v, mask_kind=mask, key_lengths=lens, scale=scale, rows=rows)
+    ref = oracle.mha_fwd(q, k, v, mask_kind=mask, key_lengths=lens, scale=scale, rows=rows,
+                         layout=layout)
+    if layout == "bshd":  # compare in [B, H, L, d], where logical row indices apply
+        out = np.ascontiguousarray(out.transpose(0, 2, 1, 3))
+        if rows is None:
+            ref = np.ascontiguousarray(ref.transpose(0, 2, 1, 3))
     return compare(out, ref, spec["dtype"], rows=rows, label=label or str(spec))
 
 
-def spec(B, H, Lq, Lk, d, dtype="bf16", mask=0, len_range=None, amp=1.0):
+def spec(B, H, Lq, Lk, d, dtype="bf16", mask=0, len_range=None, amp=1.0, Hkv=None,
+         layout="bhsd"):
     return dict(B=B, H=H, Lq=Lq, Lk=Lk, dk=d, dv=d, dtype=dtype, amp=amp, mask=mask,
-                len_range=len_range)
+                len_range=len_range, Hkv=H if Hkv is None else Hkv, layout=layout)

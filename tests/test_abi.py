@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["mha_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version"])
+        ["mha_fwd", "mha_fwd_ex", "mha_fwd_path", "mha_status_string", "mha_debug_status",
+         "mha_version"])
 
 
 def test_library_exports_every_declared_symbol(mha):
@@ -94,6 +95,32 @@ def test_rejects_before_launch(mha):
     assert call(mha, dk=96, dv=96) == E_UNS
     assert call(mha, dk=64, dv=128) == E_UNS
     assert call(mha, dtype=0, dk=200) == E_UNS
+
+
+def call_ex(mha, q=FAKE, k=FAKE + (1 << 24), v=FAKE + (2 << 24), out=FAKE + (3 << 24), B=2,
+            H=4, Hkv=2, Lq=64, Lk=64, dk=64, dv=64, layout=0, mask=0, kl=None, scale=0.125,
+            dtype=1):
+    return mha.lib.mha_fwd_ex(q, k, v, out, B, H, Hkv, Lq, Lk, dk, dv, layout, mask, kl, scale,
+                              dtype, None)
+
+
+def test_ex_rejects_before_launch(mha):
+    E_ARG, E_UNS = mha.MHA_ERR_INVALID_ARGUMENT, mha.MHA_ERR_UNSUPPORTED
+    assert call_ex(mha, Hkv=3) == E_ARG  # does not divide H
+    assert call_ex(mha, Hkv=0) == E_ARG
+    assert call_ex(mha, Hkv=-2) == E_ARG
+    assert call_ex(mha, Hkv=8) == E_ARG  # more key/value heads than query heads
+    assert call_ex(mha, layout=2) == E_ARG
+    assert call_ex(mha, layout=-1) == E_ARG
+    assert call_ex(mha, layout=1, mask=2) == E_ARG  # key_lengths missing
+    assert call_ex(mha, layout=1, q=FAKE + 8) == E_ARG
+    assert call_ex(mha, layout=1, dk=96, dv=96) == E_UNS
+    # k holds H_kv heads: an out over its last 16 bytes is caught
+    k_bytes = 2 * 2 * 64 * 64 * 2
+    assert call_ex(mha, out=FAKE + (1 << 24) + k_bytes - 16) == E_ARG
+    assert call_ex(mha, B=0) == mha.MHA_OK
+    assert call_ex(mha, B=0, Hkv=3) == E_ARG  # arguments are checked even when empty
+    assert call_ex(mha, H=0, Hkv=0, B=2) == mha.MHA_OK
 
 
 def test_empty_problem_returns_ok_without_device(mha):

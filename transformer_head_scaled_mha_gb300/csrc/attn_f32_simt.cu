@@ -1,6 +1,7 @@
 // fp32 scaled dot-product attention on the CUDA cores (FFMA only, no TF32).
 //
-// One CTA = one (batch, head) and 16 query rows; each of its 4 warps owns 4
+// One CTA = one (batch, head) and 16 query rows (with shared key/value heads,
+// query head h reads head h / (H / H_kv); either tensor layout); each of its 4 warps owns 4
 // rows.  Keys/values stream through shared memory 32 at a time (one key per
 // lane); each row keeps a running max and running sum (online softmax) so the
 // n x n score matrix is never stored.  Steps follow the four of "Scaled
@@ -40,6 +41,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Element offset of row 0 of one head, and the stride between its rows, in a
+// contiguous tensor of `heads` heads, `len` rows and `d` columns.
+struct HeadView {
+  int64_t base, row;
+};
+__device__ __forceinline__ HeadView head_view(int layout, int b, int head, int heads, int len,
+                                              int d) {
+  if (layout == kLayoutBHSD)
+    return {(static_cast<int64_t>(b) * heads + head) * len * d, static_cast<int64_t>(d)};
+  return {(static_cast<int64_t>(b) * len * heads + head) * d, static_cast<int64_t>(heads) * d};
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
     attn_f32_simt_kernel(const float *__restrict__ q, const float *__restrict__ k,
                          const float *__restrict__ v, float *__restrict__ out, Problem p) {
@@ -53,7 +66,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int n_qblk = (p.Lq + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t bh = blockIdx.x / n_qblk;
   const int q0 = (blockIdx.x % n_qblk) * kRowsPerCta;
-  const int b = static_cast<int>(bh / p.H);
+  const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H);
+  const int hkv = h / (p.H / p.Hkv);  // key/value head this query head reads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   int len = p.Lk;
@@ -65,14 +79,18 @@ __global__ void __launch_bounds__(kWarps * 32)
   if (p.mask & kMaskKeyPadding) kv_end = len;
   if (p.mask & kMaskCausal) kv_end = min(kv_end, min(q0 + kRowsPerCta, p.Lq));
 
-  const float *qb = q + (bh * p.Lq) * dk;
-  const float *kb = k + (bh * p.Lk) * dk;
-  const float *vb = v + (bh * p.Lk) * dv;
-  float *ob = out + (bh * p.Lq) * dv;
+  const HeadView vq = head_view(p.layout, b, h, p.H, p.Lq, dk);
+  const HeadView vk = head_view(p.layout, b, hkv, p.Hkv, p.Lk, dk);
+  const HeadView vv = head_view(p.layout, b, hkv, p.Hkv, p.Lk, dv);
+  const HeadView vo = head_view(p.layout, b, h, p.H, p.Lq, dv);
+  const float *qb = q + vq.base;
+  const float *kb = k + vk.base;
+  const float *vb = v + vv.base;
+  float *ob = out + vo.base;
 
   for (int e = threadIdx.x; e < kRowsPerCta * dk; e += blockDim.x) {
     const int r = e / dk, c = e % dk;
-    sq[e] = (q0 + r < p.Lq) ? qb[static_cast<int64_t>(q0 + r) * dk + c] : 0.f;
+    sq[e] = (q0 + r < p.Lq) ? qb[(q0 + r) * vq.row + c] : 0.f;
   }
 
   float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxD / 32];
@@ -88,11 +106,11 @@ __global__ void __launch_bounds__(kWarps * 32)
     __syncthreads();  // previous tile fully consumed (and sq written, first time)
     for (int e = threadIdx.x; e < kKeysPerTile * dk; e += blockDim.x) {
       const int j = e / dk, c = e % dk;
-      sk[j * ks + c] = (kv0 + j < p.Lk) ? kb[static_cast<int64_t>(kv0 + j) * dk + c] : 0.f;
+      sk[j * ks + c] = (kv0 + j < p.Lk) ? kb[(kv0 + j) * vk.row + c] : 0.f;
     }
     for (int e = threadIdx.x; e < kKeysPerTile * dv; e += blockDim.x) {
       const int j = e / dv, c = e % dv;
-      sv[e] = (kv0 + j < p.Lk) ? vb[static_cast<int64_t>(kv0 + j) * dv + c] : 0.f;
+      sv[e] = (kv0 + j < p.Lk) ? vb[(kv0 + j) * vv.row + c] : 0.f;
     }
     __syncthreads();
 
@@ -139,7 +157,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int t = 0; t < kMaxD / 32; ++t) {
       const int c = lane + 32 * t;
-      if (c < dv) ob[static_cast<int64_t>(i) * dv + c] = zero_row ? 0.f : acc[r][t] * inv;
+      if (c < dv) ob[i * vo.row + c] = zero_row ? 0.f : acc[r][t] * inv;
     }
   }
 }

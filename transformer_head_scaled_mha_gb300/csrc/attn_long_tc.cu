@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nqb = (p.Lq + 2 * kBM - 1) / (2 * kBM);
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / BH;  // heaviest first
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int b = bh / p.H;
+  const int b = bh / p.H, h = bh % p.H;
+  const int hkv = h / (p.H / p.Hkv);  // key/value head this query head reads
   const int q0 = qb * 2 * kBM;
 
   int len = p.Lk;
@@ -164,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < 2; ++w)
         if (n_tiles[w] > 0)
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_3d(q_smem + w * C::kTileBytes + blk * C::kBlkBytes, &maps.q, &bars->q_full,
-                        blk * 64, q0 + w * kBM, bh);
+            tma_load_4d(q_smem + w * C::kTileBytes + blk * C::kBlkBytes, &maps.q, &bars->q_full,
+                        blk * 64, q0 + w * kBM, h, b);
       for (int idx = 0; idx < 2 * n_kv; ++idx) {
         const int slot = idx % C::kSlots, round = idx / C::kSlots;
         if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, abort_flag)) break;
@@ -173,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap *map = (idx & 1) ? &maps.v : &maps.k;
         mbar_arrive_expect_tx(&bars->kv_full[slot], C::kTileBytes);
         for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_3d(kv_smem + slot * C::kTileBytes + blk * C::kBlkBytes, map,
-                      &bars->kv_full[slot], blk * 64, j * kBN, bh);
+          tma_load_4d(kv_smem + slot * C::kTileBytes + blk * C::kBlkBytes, map,
+                      &bars->kv_full[slot], blk * 64, j * kBN, hkv, b);
         issued = idx + 1;
       }
     }
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_barrier_sync(1 + w, kWgThreads);
         if (r == 0) {
           for (int blk = 0; blk < D / 64; ++blk)
-            tma_store_3d(&maps.o, stage + blk * C::kBlkBytes, blk * 64, q0 + w * kBM, bh);
+            tma_store_4d(&maps.o, stage + blk * C::kBlkBytes, blk * 64, q0 + w * kBM, h, b);
           tma_store_commit();
           tma_store_wait0();
         }

@@ -5,8 +5,10 @@
 // This kernel packs P = 128 / max(Rq, Rk) pairs into one 128-row tile (Rq,
 // Rk: Lq, Lk rounded up to powers of two) so one tcgen05.mma covers all of
 // them; products between different pairs land in off-diagonal blocks that are
-// never read.  Each CTA is persistent (one per SM) and walks the units
-// u = blockIdx.x, + gridDim.x, ...
+// never read.  A unit holds P consecutive heads of one batch element; with
+// shared key/value heads (grouped- or multi-query attention) pair h reads the
+// K and V of head h / (H / H_kv).  Each CTA is persistent (one per SM) and
+// walks the units u = blockIdx.x, + gridDim.x, ...
 //
 // Warp roles (384 threads):
 //   warps 0-3, 4-7  two softmax warpgroups; unit n goes to warpgroup n % 2,
@@ -25,8 +27,10 @@
 //                          swizzled 4 KiB buffer and TMA-stores them
 // Padded sequences load only their first ceil(len/8)*8 rows, as one TMA box
 // of that height per tensor and pair, so padding costs no HBM reads (a CTA's
-// first unit loads whole tiles instead, so it does not wait for the lengths).  Masked keys get exactly zero weight; padded query rows
-// and rows without any allowed key are stored as +0.
+// first unit loads whole tiles instead, so it does not wait for the lengths).
+// Masked keys get exactly zero weight; padded query rows and rows without any
+// allowed key are stored as +0.  All tensor maps are 4-D (d, L, heads, B), so
+// the [B, H, L, d] and [B, L, H, d] layouts run the same code.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -90,9 +94,9 @@ __device__ __forceinline__ uint32_t box_bytes(int rows) {
   return static_cast<uint32_t>((rows + 7) / 8) * 1024u;
 }
 __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *maps, uint64_t *bar,
-                                          int rows, int bh) {
+                                          int rows, int head, int b) {
   const int n8 = (rows + 7) / 8;
-  if (n8 > 0) tma_load_3d(dst, &maps[n8 - 1], bar, 0, 0, bh);
+  if (n8 > 0) tma_load_4d(dst, &maps[n8 - 1], bar, 0, 0, head, b);
 }
 
 // One 32-column chunk of a row's scores (raw fp32 bits), sign-flipped by
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
+  const int group = p.H / p.Hkv;  // query heads per key/value head
   const int n_local = (static_cast<int>(blockIdx.x) < g.units)
                           ? (g.units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                           : 0;
@@ -178,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&maps.q_full);
-    tma_prefetch_desc(&maps.k_full);
-    tma_prefetch_desc(&maps.v_full);
+    tma_prefetch_desc(group == 1 ? &maps.k_full : &maps.k_one);
+    tma_prefetch_desc(group == 1 ? &maps.v_full : &maps.v_one);
   }
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -216,16 +220,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool need_len = g.rows_q || g.rows_k;
     // lane pp's pair length for unit n, read two units ahead of its use
     auto len_at = [&](int n) -> int {
-      const int bh = (blockIdx.x + n * gridDim.x) * g.P + pp;
-      return (need_len && n < n_local && pp < g.P && bh < BH) ? clamp_len(p, bh / p.H) : 0;
+      const int u = blockIdx.x + n * gridDim.x;
+      const int h = (u % g.units_per_b) * g.P + pp;
+      return (need_len && n < n_local && pp < g.P && h < p.H) ? clamp_len(p, u / g.units_per_b)
+                                                               : 0;
     };
     int len_n1 = len_at(1), len_n2 = len_at(2);
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
-      const int bh0 = (blockIdx.x + n * gridDim.x) * g.P;
+      const int u = blockIdx.x + n * gridDim.x;
+      const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
+      // key/value head of pair pp (a pair past the last head, whose rows are
+      // never stored, reads the last head so every box is in bounds)
+      const int hkv = min(h0 + pp, p.H - 1) / group;
       // the first unit loads whole tiles: no wait for the lengths
       const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
-      const bool has_pair = pp < g.P && bh0 + pp < BH;
+      const bool has_pair = pp < g.P && h0 + pp < p.H;
       const int len = n > 0 ? len_n1 : 0;
       if (n > 0) {
         len_n1 = len_n2;
@@ -244,18 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *sv = sk + kTileBytes;
       if (lane == 0) mbar_arrive_expect_tx(&bars->full[s], bytes);
       __syncwarp();
+      // whole tiles: one box of P heads, or with shared key/value heads one
+      // box per pair (heads past H read as zeros and are never stored)
       if (lane == 0) {
-        if (!rows_q) tma_load_3d(sq, &maps.q_full, &bars->full[s], 0, 0, bh0);
-        if (!rows_k) {
-          tma_load_3d(sk, &maps.k_full, &bars->full[s], 0, 0, bh0);
-          tma_load_3d(sv, &maps.v_full, &bars->full[s], 0, 0, bh0);
+        if (!rows_q) tma_load_4d(sq, &maps.q_full, &bars->full[s], 0, 0, h0, b);
+        if (!rows_k && group == 1) {
+          tma_load_4d(sk, &maps.k_full, &bars->full[s], 0, 0, h0, b);
+          tma_load_4d(sv, &maps.v_full, &bars->full[s], 0, 0, h0, b);
         }
       }
+      if (!rows_k && group != 1 && pp < g.P) {
+        tma_load_4d(sk + pp * g.Rk * 128, &maps.k_one, &bars->full[s], 0, 0, hkv, b);
+        tma_load_4d(sv + pp * g.Rk * 128, &maps.v_one, &bars->full[s], 0, 0, hkv, b);
+      }
       if (has_pair && rows_q) load_rows(sq + pp * g.Rq * 128, maps.q_rows, &bars->full[s],
-                                        min(len, p.Lq), bh0 + pp);
+                                        min(len, p.Lq), h0 + pp, b);
       if (has_pair && rows_k) {
-        load_rows(sk + pp * g.Rk * 128, maps.k_rows, &bars->full[s], len, bh0 + pp);
-        load_rows(sv + pp * g.Rk * 128, maps.v_rows, &bars->full[s], len, bh0 + pp);
+        load_rows(sk + pp * g.Rk * 128, maps.k_rows, &bars->full[s], len, hkv, b);
+        load_rows(sv + pp * g.Rk * 128, maps.v_rows, &bars->full[s], len, hkv, b);
       }
       __syncwarp();
       issued = n + 1;
@@ -322,9 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = fabsf(p.scale_log2);
 
     auto len_of = [&](int n) -> int {
-      const int bh = (blockIdx.x + n * gridDim.x) * g.P + pr;
-      const bool valid = pr < g.P && bh < BH && i < p.Lq;
-      return valid ? clamp_len(p, bh / p.H) : 0;
+      const int u = blockIdx.x + n * gridDim.x;
+      const bool valid = pr < g.P && (u % g.units_per_b) * g.P + pr < p.H && i < p.Lq;
+      return valid ? clamp_len(p, u / g.units_per_b) : 0;
     };
     int len_cur = w < n_local ? len_of(w) : 0;
     float rowsum_prev = 0.f;  // row sum of the unit whose epilogue is pending
@@ -335,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int len_next = n + 2 < n_local ? len_of(n + 2) : 0;  // load ahead of its use
       if (n < n_local) {
         const int k = n >> 1;  // this warpgroup's k-th unit
-        const int bh = (blockIdx.x + n * gridDim.x) * g.P + pr;
-        const bool valid = pr < g.P && bh < BH && i < p.Lq;
+        const int u = blockIdx.x + n * gridDim.x;
+        const bool valid = pr < g.P && (u % g.units_per_b) * g.P + pr < p.H && i < p.Lq;
         const int len = len_cur;
         int jmax = p.Lk;
         if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
@@ -428,14 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int bh0 = (blockIdx.x + pn * gridDim.x) * g.P;
+          const int u = blockIdx.x + pn * gridDim.x;
+          const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
           const int rows = g.Rq < 32 ? g.Rq : 32;       // rows of one pair in this warp
           const int h = rows >= 32 ? 2 : (rows == 16 ? 1 : 0);
           for (int r0 = (warp & 3) * 32; r0 < (warp & 3) * 32 + 32; r0 += rows) {
             const int ppair = r0 / g.Rq, i0 = r0 % g.Rq;
-            if (ppair < g.P && bh0 + ppair < BH && i0 < p.Lq)
-              tma_store_3d(&maps.o_rows[h], stg + (r0 - (warp & 3) * 32) * 128, 0, i0,
-                           bh0 + ppair);
+            if (ppair < g.P && h0 + ppair < p.H && i0 < p.Lq)
+              tma_store_4d(&maps.o_rows[h], stg + (r0 - (warp & 3) * 32) * 128, 0, i0,
+                           h0 + ppair, b);
           }
           tma_store_commit();
         }

@@ -20,9 +20,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // log2(e): softmax is evaluated as exp2(x * scale * log2(e) - m)
 constexpr float kLog2e = 1.4426950408889634f;
 
+constexpr int kLayoutBHSD = 0;  // [B, heads, L, d]
+constexpr int kLayoutBSHD = 1;  // [B, L, heads, d]
+
 // Problem description handed to every kernel by value.
 struct Problem {
-  int B, H, Lq, Lk, dk, dv;
+  int B, H, Hkv, Lq, Lk, dk, dv;  // query head h reads key/value head h / (H / Hkv)
+  int layout;                      // kLayoutBHSD or kLayoutBSHD (all four tensors)
   int mask;
   const int32_t *key_lengths;  // device [B] or nullptr
   float scale_log2;            // scale * log2(e)
@@ -33,27 +37,30 @@ struct Problem {
 cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, float *out,
                             const Problem &p, cudaStream_t stream);
 
-// tensor maps for the bf16 tensor-core kernels: every map is 3-D
-// (d, L, B*H) over a [B, H, L, d] bf16 tensor with 128-byte swizzle
+// tensor maps for the bf16 tensor-core kernels: every map is 4-D
+// (d, L, heads, B) over a bf16 tensor in either layout, 128-byte swizzle
 constexpr int kRowBoxes = 16;  // row-box heights 8, 16, ..., 128
 struct ShortMaps {
-  CUtensorMap q_full, k_full, v_full;  // box (64, Rq|Rk, P)
-  CUtensorMap q_rows[kRowBoxes];       // box (64, 8 (h + 1), 1), for padded tensors
+  CUtensorMap q_full;                  // box (64, Rq, P, 1): P consecutive query heads
+  CUtensorMap k_full, v_full;          // box (64, Rk, P, 1) (key/value heads not shared)
+  CUtensorMap k_one, v_one;            // box (64, Rk, 1, 1) (shared key/value heads)
+  CUtensorMap q_rows[kRowBoxes];       // box (64, 8 (h + 1), 1, 1), for padded tensors
   CUtensorMap k_rows[kRowBoxes];
   CUtensorMap v_rows[kRowBoxes];
-  CUtensorMap o_rows[3];               // box (64, 8 << h, 1): output stores
+  CUtensorMap o_rows[3];               // box (64, 8 << h, 1, 1): output stores
 };
 struct ShortGeom {
   int Rq, Rk, P;       // rows per packed pair (powers of two) and pairs per unit
-  int units;           // ceil(B*H / P)
+  int units_per_b;     // ceil(H / P): a unit never spans two batch elements
+  int units;           // B * units_per_b
   int rows_q, rows_k;  // load Q / K,V only up to each pair's length (padding)
 };
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             int num_sms, cudaStream_t stream);
 
 struct LongMaps {
-  CUtensorMap q, k, v;  // box (64, 128, 1)
-  CUtensorMap o;        // box (64, 128, 1)
+  CUtensorMap q, k, v;  // box (64, 128, 1, 1)
+  CUtensorMap o;        // box (64, 128, 1, 1)
 };
 cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
                            cudaStream_t stream);

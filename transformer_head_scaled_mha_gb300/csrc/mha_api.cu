@@ -66,19 +66,23 @@ int next_pow2(int x) {
   return r;
 }
 
-// 3-D view (d, L, B*H) of a contiguous [B, H, L, d] bf16 tensor, 128B swizzle
-bool make_map(CUtensorMap *map, const void *base, int d, int L, int BH, int box_rows,
-              int box_pairs) {
+// 4-D view (d, L, heads, B) of a contiguous bf16 tensor in either layout,
+// 128-byte swizzle; box (64, box_rows, box_heads, 1)
+bool make_map(CUtensorMap *map, const void *base, int d, int L, int heads, int B, int layout,
+              int box_rows, int box_heads) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(L) * d * 2};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows),
-                             static_cast<cuuint32_t>(box_pairs)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+  const cuuint64_t e = 2;  // bytes per element
+  const cuuint64_t row = layout == kLayoutBHSD ? d * e : static_cast<cuuint64_t>(heads) * d * e;
+  const cuuint64_t head = layout == kLayoutBHSD ? static_cast<cuuint64_t>(L) * d * e : d * e;
+  const cuuint64_t batch = static_cast<cuuint64_t>(heads) * L * d * e;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {row, head, batch};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_heads), 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -121,19 +125,22 @@ extern "C" int mha_fwd_path(int B, int H, int Lq, int Lk, int d_k, int d_v, int 
   return select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
 }
 
-extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
-                       int Lq, int Lk, int d_k, int d_v, int mask_kind,
-                       const int32_t *key_lengths, float scale, int dtype, void *stream_) {
+extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H,
+                          int H_kv, int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
+                          const int32_t *key_lengths, float scale, int dtype, void *stream_) {
   const int path = select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
+  if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
+  if (H_kv <= 0 ? H > 0 : (H % H_kv) != 0) return MHA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   if (path == kPathNone) return MHA_OK;
   const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
   if (padded && key_lengths == nullptr) return MHA_ERR_INVALID_ARGUMENT;
   const size_t esz = dtype == MHA_DTYPE_F32 ? 4 : 2;
-  const size_t BH = static_cast<size_t>(B) * H;
-  const size_t nq = BH * Lq * d_k * esz, nk = BH * Lk * d_k * esz, nv = BH * Lk * d_v * esz;
-  const size_t no = BH * Lq * d_v * esz;
+  const size_t nq = static_cast<size_t>(B) * H * Lq * d_k * esz;
+  const size_t nk = static_cast<size_t>(B) * H_kv * Lk * d_k * esz;
+  const size_t nv = static_cast<size_t>(B) * H_kv * Lk * d_v * esz;
+  const size_t no = static_cast<size_t>(B) * H * Lq * d_v * esz;
   if (out == nullptr || q == nullptr || (Lk > 0 && (k == nullptr || v == nullptr)))
     return MHA_ERR_INVALID_ARGUMENT;
   for (const void *ptr : {static_cast<const void *>(q), static_cast<const void *>(k),
@@ -149,10 +156,12 @@ extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, i
   Problem p;
   p.B = B;
   p.H = H;
+  p.Hkv = H_kv;
   p.Lq = Lq;
   p.Lk = Lk;
   p.dk = d_k;
   p.dv = d_v;
+  p.layout = layout;
   p.mask = mask_kind;
   p.key_lengths = padded ? key_lengths : nullptr;
   p.scale_log2 = scale * kLog2e;
@@ -168,39 +177,56 @@ extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, i
   } else {
     const int sms = sm_count(dev);
     if (sms <= 0) return MHA_ERR_CUDA;
-    const int bh = static_cast<int>(BH);
     if (path == kPathShort) {
       ShortGeom g;
       g.Rq = next_pow2(Lq < 8 ? 8 : Lq);
       g.Rk = next_pow2(Lk < 16 ? 16 : Lk);
       g.P = 128 / (g.Rq > g.Rk ? g.Rq : g.Rk);
-      g.units = (bh + g.P - 1) / g.P;
+      if (g.P > H) g.P = H;  // a unit holds heads of one batch element
+      g.units_per_b = (H + g.P - 1) / g.P;
+      if (static_cast<long long>(B) * g.units_per_b > 0x7fffffffLL) return MHA_ERR_UNSUPPORTED;
+      g.units = B * g.units_per_b;
       g.rows_q = (mask_kind & kMaskQueryPadding) ? 1 : 0;
       g.rows_k = (mask_kind & kMaskKeyPadding) ? 1 : 0;
       ShortMaps m;
       std::memset(&m, 0, sizeof m);
-      bool ok = make_map(&m.q_full, q, 64, Lq, bh, g.Rq, g.P) &&
-                make_map(&m.k_full, k, 64, Lk, bh, g.Rk, g.P) &&
-                make_map(&m.v_full, v, 64, Lk, bh, g.Rk, g.P);
+      const bool shared_kv = H_kv != H;
+      bool ok = make_map(&m.q_full, q, 64, Lq, H, B, layout, g.Rq, g.P);
+      if (ok && !shared_kv)
+        ok = make_map(&m.k_full, k, 64, Lk, H_kv, B, layout, g.Rk, g.P) &&
+             make_map(&m.v_full, v, 64, Lk, H_kv, B, layout, g.Rk, g.P);
+      if (ok && shared_kv)
+        ok = make_map(&m.k_one, k, 64, Lk, H_kv, B, layout, g.Rk, 1) &&
+             make_map(&m.v_one, v, 64, Lk, H_kv, B, layout, g.Rk, 1);
       // one row-box map per height 8, 16, ..., Rq (Rk) for the padded tensors
       for (int h = 0; ok && g.rows_q && h < g.Rq / 8; ++h)
-        ok = make_map(&m.q_rows[h], q, 64, Lq, bh, 8 * (h + 1), 1);
+        ok = make_map(&m.q_rows[h], q, 64, Lq, H, B, layout, 8 * (h + 1), 1);
       for (int h = 0; ok && g.rows_k && h < g.Rk / 8; ++h)
-        ok = make_map(&m.k_rows[h], k, 64, Lk, bh, 8 * (h + 1), 1) &&
-             make_map(&m.v_rows[h], v, 64, Lk, bh, 8 * (h + 1), 1);
-      for (int h = 0; ok && h < 3; ++h) ok = make_map(&m.o_rows[h], out, 64, Lq, bh, 8 << h, 1);
+        ok = make_map(&m.k_rows[h], k, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1) &&
+             make_map(&m.v_rows[h], v, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1);
+      for (int h = 0; ok && h < 3; ++h)
+        ok = make_map(&m.o_rows[h], out, 64, Lq, H, B, layout, 8 << h, 1);
       if (!ok) return MHA_ERR_CUDA;
       err = launch_short_tc(m, g, p, sms, stream);
     } else {
       LongMaps m;
       std::memset(&m, 0, sizeof m);
-      bool ok = make_map(&m.q, q, d_k, Lq, bh, 128, 1) && make_map(&m.k, k, d_k, Lk, bh, 128, 1) &&
-                make_map(&m.v, v, d_v, Lk, bh, 128, 1) && make_map(&m.o, out, d_v, Lq, bh, 128, 1);
+      bool ok = make_map(&m.q, q, d_k, Lq, H, B, layout, 128, 1) &&
+                make_map(&m.k, k, d_k, Lk, H_kv, B, layout, 128, 1) &&
+                make_map(&m.v, v, d_v, Lk, H_kv, B, layout, 128, 1) &&
+                make_map(&m.o, out, d_v, Lq, H, B, layout, 128, 1);
       if (!ok) return MHA_ERR_CUDA;
       err = launch_long_tc(m, p, sms, stream);
     }
   }
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
+                       int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                       const int32_t *key_lengths, float scale, int dtype, void *stream) {
+  return mha_fwd_ex(q, k, v, out, B, H, H, Lq, Lk, d_k, d_v, kLayoutBHSD, mask_kind, key_lengths,
+                    scale, dtype, stream);
 }
 
 extern "C" const char *mha_status_string(int status) {

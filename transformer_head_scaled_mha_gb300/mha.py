@@ -16,7 +16,9 @@ MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_QUERY_PADDING = 0
 MHA_OK, MHA_ERR_INVALID_ARGUMENT, MHA_ERR_UNSUPPORTED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = range(5)
 PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fill"}
 
-EXPORTED = ("mha_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
+MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
+
+EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
 
 
 class MhaError(RuntimeError):
@@ -35,6 +37,9 @@ def _load() -> ctypes.CDLL:
     lib.mha_fwd.restype = i32
     lib.mha_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp,
                             ctypes.c_float, i32, vp]
+    lib.mha_fwd_ex.restype = i32
+    lib.mha_fwd_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp,
+                               ctypes.c_float, i32, vp]
     lib.mha_fwd_path.restype = i32
     lib.mha_fwd_path.argtypes = [i32] * 8
     lib.mha_status_string.restype = ctypes.c_char_p
@@ -76,6 +81,47 @@ def mha_debug_status(stream=None) -> int:
     return int(lib.mha_debug_status(_stream_handle(stream)))
 
 
+def _marshal(q, k, v, out, key_lengths, scale, layout):
+    """Check shapes/dtypes, allocate ``out`` if needed; returns the C arguments."""
+    import torch
+    if layout not in ("bhsd", "bshd"):
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    if layout == "bshd":
+        B, Lq, H, dk = q.shape
+        Lk, Hkv, dv = k.shape[1], k.shape[2], v.shape[3]
+        kshape, vshape, oshape = (B, Lk, Hkv, dk), (B, Lk, Hkv, dv), (B, Lq, H, dv)
+    else:
+        B, H, Lq, dk = q.shape
+        Hkv, Lk, dv = k.shape[1], k.shape[2], v.shape[3]
+        kshape, vshape, oshape = (B, Hkv, Lk, dk), (B, Hkv, Lk, dv), (B, H, Lq, dv)
+    if q.dtype == torch.float32:
+        dtype = MHA_DTYPE_F32
+    elif q.dtype == torch.bfloat16:
+        dtype = MHA_DTYPE_BF16
+    else:
+        raise TypeError("q must be float32 or bfloat16")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if tuple(k.shape) != kshape or tuple(v.shape) != vshape:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape),
+                                                             tuple(v.shape)))
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if out is None:
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != oshape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous %s tensor of q's dtype" % (oshape,))
+    kl_ptr = None
+    if key_lengths is not None:
+        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
+            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
+        kl_ptr = key_lengths.data_ptr()
+    if scale is None:
+        scale = float(dk) ** -0.5
+    return out, (B, H, Hkv, Lq, Lk, dk, dv), kl_ptr, float(scale), dtype
+
+
 def mha_fwd(q, k, v, out=None, *, mask_kind: int = 0, key_lengths=None, scale=None,
             stream=None):
     """out = softmax(q k^T * scale) v per (batch, head), on q's CUDA device.
@@ -86,37 +132,36 @@ def mha_fwd(q, k, v, out=None, *, mask_kind: int = 0, key_lengths=None, scale=No
     ``stream`` (default: torch's current stream); returns ``out``.
     """
     import torch
-    B, H, Lq, dk = q.shape
-    Lk, dv = k.shape[2], v.shape[3]
-    if q.dtype == torch.float32:
-        dtype = MHA_DTYPE_F32
-    elif q.dtype == torch.bfloat16:
-        dtype = MHA_DTYPE_BF16
-    else:
-        raise TypeError("q must be float32 or bfloat16")
-    if k.dtype != q.dtype or v.dtype != q.dtype:
-        raise TypeError("q, k, v must share one dtype")
-    if tuple(k.shape) != (B, H, Lk, dk) or tuple(v.shape) != (B, H, Lk, dv):
-        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape),
-                                                             tuple(v.shape)))
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous CUDA tensor" % name)
-    if out is None:
-        out = torch.empty((B, H, Lq, dv), dtype=q.dtype, device=q.device)
-    elif tuple(out.shape) != (B, H, Lq, dv) or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [B,H,Lq,d_v] tensor of q's dtype")
-    kl_ptr = None
-    if key_lengths is not None:
-        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
-            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
-        kl_ptr = key_lengths.data_ptr()
-    if scale is None:
-        scale = float(dk) ** -0.5
+    out, (B, H, Hkv, Lq, Lk, dk, dv), kl_ptr, scale, dtype = _marshal(q, k, v, out, key_lengths,
+                                                                      scale, "bhsd")
+    if Hkv != H:
+        raise ValueError("mha_fwd needs as many key/value heads as query heads; "
+                         "use mha_fwd_ex for shared key/value heads")
     with torch.cuda.device(q.device):
         st = lib.mha_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Lq, Lk,
-                         dk, dv, int(mask_kind), kl_ptr, float(scale), dtype,
-                         _stream_handle(stream))
+                         dk, dv, int(mask_kind), kl_ptr, scale, dtype, _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st)
+    return out
+
+
+def mha_fwd_ex(q, k, v, out=None, *, layout: str = "bhsd", mask_kind: int = 0,
+               key_lengths=None, scale=None, stream=None):
+    """mha_fwd with shared key/value heads and a choice of layout.
+
+    layout "bhsd": q [B,H,Lq,d_k], k [B,H_kv,Lk,d_k], v [B,H_kv,Lk,d_v];
+    layout "bshd": q [B,Lq,H,d_k], k [B,Lk,H_kv,d_k], v [B,Lk,H_kv,d_v]; ``out``
+    has q's layout.  H_kv (from k) divides H; query head h reads key/value head
+    h // (H // H_kv).
+    """
+    import torch
+    out, (B, H, Hkv, Lq, Lk, dk, dv), kl_ptr, scale, dtype = _marshal(q, k, v, out, key_lengths,
+                                                                      scale, layout)
+    with torch.cuda.device(q.device):
+        st = lib.mha_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Hkv,
+                            Lq, Lk, dk, dv, MHA_LAYOUT_BSHD if layout == "bshd" else
+                            MHA_LAYOUT_BHSD, int(mask_kind), kl_ptr, scale, dtype,
+                            _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_fwd_ex")
     return out
