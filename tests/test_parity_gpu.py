@@ -152,6 +152,32 @@ def test_empty_problem_is_noop():
     assert out.shape == (0, 2, 5, 64)
 
 
+@pytest.mark.parametrize("Lq,Lk,d,mask", [(128, 128, 64, C), (64, 64, 64, 0), (96, 128, 64, KP),
+                                          (16, 16, 64, C), (300, 300, 128, C),
+                                          (200, 333, 64, KP)])
+def test_scores_climbing_along_keys(Lq, Lk, d, mask):
+    # scores that rise by about 10 (log2 units) every 32 keys: each later key
+    # block's max far exceeds the earlier ones, which is where a kernel that
+    # takes exponents against a provisional max must correct what it wrote
+    rng = np.random.default_rng(7)
+    B, H = 2, 2
+    q = np.abs(rng.normal(size=(B, H, Lq, d))) * 0.5 + 0.5
+    ramp = (np.arange(Lk) / 16.0)[None, None, :, None] * (64.0 / d)
+    k = ramp * (0.5 + 0.1 * rng.normal(size=(B, H, Lk, d)))
+    v = rng.normal(size=(B, H, Lk, d))
+    q, k, v = (gen.f64_to_bf16_bits(x) for x in (q, k, v))
+    lens = np.array([Lk - 5, min(Lk, 70)], dtype=np.int32) if mask & KP else None
+    s = spec(B, H, Lq, Lk, d, mask=mask)
+    out = run_gpu(q, k, v, lens, s)
+    ref = oracle.mha_fwd(q, k, v, mask_kind=mask, key_lengths=lens, scale=gen.default_scale(d))
+    compare(out, ref, "bf16", label="climbing scores")
+    # and the reverse: the first key block holds the largest scores
+    k2 = np.ascontiguousarray(k[:, :, ::-1])
+    out = run_gpu(q, k2, v, lens, s)
+    ref = oracle.mha_fwd(q, k2, v, mask_kind=mask, key_lengths=lens, scale=gen.default_scale(d))
+    compare(out, ref, "bf16", label="falling scores")
+
+
 @pytest.mark.parametrize("scale", [0.0, 1.0, -0.3])
 def test_other_scales(scale):
     check_case(spec(2, 2, 96, 128, 64), scale=scale, seed=8)

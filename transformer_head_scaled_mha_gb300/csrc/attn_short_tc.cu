@@ -21,10 +21,14 @@
 //   S = Q K^T              tcgen05.mma -> TMEM (fp32), one region per warpgroup
 //   mask, scale, softmax   tcgen05.ld of the 32-column chunks the warp's rows
 //                          can use -> registers; exp2 against the row max
-//   P (bf16) -> TMEM       over the first 64 columns of the unit's S region
-//   O = P V                tcgen05.mma (A = P from TMEM) -> TMEM, 4 buffers
+//   P (bf16) -> TMEM       the warpgroup's own P columns, so S of its next
+//                          unit is computed while P V still reads P
+//   O = P V                tcgen05.mma (A = P from TMEM) -> TMEM
 //   O / rowsum -> bf16     tcgen05.ld; each warp stages its 32 rows in a
-//                          swizzled 4 KiB buffer and TMA-stores them
+//                          swizzled 4 KiB buffer and writes them back with
+//                          stores that each cover four whole rows
+// The MMA warp issues S for unit n + 2 as soon as the warpgroup posted P for
+// unit n, and P V for unit n once the warpgroup has read O of unit n - 2.
 // Padded sequences load only their first ceil(len/8)*8 rows, as one TMA box
 // of that height per tensor and pair, so padding costs no HBM reads (a CTA's
 // first unit loads whole tiles instead, so it does not wait for the lengths).
@@ -55,17 +59,20 @@ constexpr uint32_t kRegsSoftmax = 216;
 constexpr uint32_t kRegsControl = 64;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0;    // S/P region of warpgroup w: [128 w, 128 w + 128)
-constexpr uint32_t kOCol0 = 256;  // O buffer of unit n: [256 + 64 (n % 4), +64)
-constexpr int kOBufs = 4;
+// TMEM columns of warpgroup w: S (fp32) [128 w, +128), P (bf16 pairs)
+// [256 + 64 w, +64), O (fp32) [384 + 64 w, +64).  P has its own columns so
+// the next S of a warpgroup can be computed while P V still reads P.
+constexpr uint32_t kSCol0 = 0;
+constexpr uint32_t kPCol0 = 256;
+constexpr uint32_t kOCol0 = 384;
 
 struct __align__(8) Barriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[kOBufs];
-  uint64_t o_free[kOBufs];
+  uint64_t s_full[2];   // S of the warpgroup's unit is in TMEM
+  uint64_t p_full[2];   // the warpgroup read its S and wrote P
+  uint64_t pv_done[2];  // P V done: O ready, P columns free
+  uint64_t o_free[2];   // the warpgroup read O
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -101,15 +108,23 @@ __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *maps,
 
 // One 32-column chunk of a row's scores (raw fp32 bits), sign-flipped by
 // `sgn` (a negative scale is applied as |scale| to -s), with columns outside
-// lo <= c < hi set to -inf when `mask`.
+// lo <= c < hi set to -inf when `mask`.  Both steps are skipped when they do
+// nothing (the usual case), which keeps the executed code small.
 __device__ __forceinline__ void chunk_prepare(uint32_t (&v)[32], int c0, uint32_t sgn, bool mask,
                                               int lo, int hi) {
+  if (sgn) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    uint32_t x = v[e] ^ sgn;
-    if (mask && static_cast<unsigned>(c0 + e - lo) >= static_cast<unsigned>(hi - lo))
-      x = __float_as_uint(-INFINITY);
-    v[e] = x;
+    for (int e = 0; e < 32; ++e) v[e] ^= sgn;
+  }
+  if (mask) {
+    // bit e set: column c0 + e is kept
+    const int a = min(max(lo - c0, 0), 32), z = min(max(hi - c0, 0), 32);
+    const uint32_t upto_z = z >= 32 ? 0xffffffffu : (1u << z) - 1u;
+    const uint32_t upto_a = a >= 32 ? 0xffffffffu : (1u << a) - 1u;
+    const uint32_t keep = upto_z & ~upto_a;
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (!((keep >> e) & 1u)) v[e] = __float_as_uint(-INFINITY);
   }
 }
 __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32]) {
@@ -122,6 +137,18 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&v)[32]) {
   return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]),
                fmax3(fmax3(t[6], t[7], t[8]), t[9], t[10]));
 }
+// Multiplies the 32 bf16 P values of one chunk (16 TMEM columns) by f.
+__device__ __noinline__ void rescale_p(uint32_t taddr, float f) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+    r[t] = pack_bf16x2(__uint_as_float(r[t] << 16) * f, __uint_as_float(r[t] & 0xffff0000u) * f);
+  tmem_st16(taddr, r);
+  tmem_wait_st();
+}
+
 // p_c = exp2(s_c * sl - m) for one chunk, packed into 16 bf16x2 columns;
 // returns the chunk's sum of p (fp32)
 __device__ __forceinline__ float chunk_exp_pack(const uint32_t (&v)[32], float sl, float m,
@@ -148,7 +175,7 @@ __device__ __forceinline__ float chunk_exp_pack(const uint32_t (&v)[32], float s
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_short_tc_kernel(const __grid_constant__ ShortMaps maps, const ShortGeom g,
-                         const Problem p) {
+                         const Problem p, void *out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -159,6 +186,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = p.H / p.Hkv;  // query heads per key/value head
+  // Causal 128-row tiles: row 96 + t needs four 32-key chunks of softmax,
+  // row t one, and TMEM lanes 32 q .. 32 q + 31 belong to the warps on SM
+  // sub-partition q.  Warpgroup 1 therefore holds its query rows with the
+  // 32-row blocks in reverse order, so each sub-partition gets one heavy and
+  // one light warp.
+  const bool rev = (p.mask & kMaskCausal) && g.Rq == 128 && !g.rows_q;
   const int n_local = (static_cast<int>(blockIdx.x) < g.units)
                           ? (g.units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                           : 0;
@@ -172,10 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bars->s_full[w], 1);
       mbar_init(&bars->p_full[w], kWgThreads);
-    }
-    for (int o = 0; o < kOBufs; ++o) {
-      mbar_init(&bars->pv_done[o], 1);
-      mbar_init(&bars->o_free[o], kWgThreads);
+      mbar_init(&bars->pv_done[w], 1);
+      mbar_init(&bars->o_free[w], kWgThreads);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -225,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (need_len && n < n_local && pp < g.P && h < p.H) ? clamp_len(p, u / g.units_per_b)
                                                                : 0;
     };
-    int len_n1 = len_at(1), len_n2 = len_at(2);
+    int len_n1 = 0, len_n2 = 0;  // read once unit 0's loads are on their way
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
       const int u = blockIdx.x + n * gridDim.x;
@@ -256,8 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       // whole tiles: one box of P heads, or with shared key/value heads one
       // box per pair (heads past H read as zeros and are never stored)
+      if (rev && (n & 1)) {
+        // warpgroup 1 of a causal tile: reversed 32-row blocks (see above)
+        if (lane < 4)
+          tma_load_4d(sq + lane * 32 * 128, &maps.q_blk32, &bars->full[s], 0, (3 - lane) * 32, h0,
+                      b);
+      } else if (lane == 0 && !rows_q) {
+        tma_load_4d(sq, &maps.q_full, &bars->full[s], 0, 0, h0, b);
+      }
       if (lane == 0) {
-        if (!rows_q) tma_load_4d(sq, &maps.q_full, &bars->full[s], 0, 0, h0, b);
         if (!rows_k && group == 1) {
           tma_load_4d(sk, &maps.k_full, &bars->full[s], 0, 0, h0, b);
           tma_load_4d(sv, &maps.v_full, &bars->full[s], 0, 0, h0, b);
@@ -275,15 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = n + 1;
+      if (n == 0) {
+        len_n1 = len_at(1);
+        len_n2 = len_at(2);
+      }
     }
   } else if (warp == 9) {
     // ---- MMA issuer (lane 0) ----------------------------------------------
     const uint32_t n_keys = static_cast<uint32_t>(g.P * g.Rk);  // multiple of 16, <= 128
     const uint32_t idesc_s = idesc_bf16_f32(128, n_keys, 0);
     const uint32_t idesc_o = idesc_bf16_f32(128, kD, 1);
-    // Fixed order S_0, S_1, then for each unit n: P V for n, S for n + 2.
-    // S_{n+2} reuses warpgroup (n % 2)'s S region, free once its softmax of
-    // unit n finished (p_full) -- which P V for n also needs.  Every wait
+    // Fixed order S_0, S_1, then for each unit n: S for n + 2 (warpgroup
+    // n % 2 is done reading S_n once it posted P_n), then P V for n (its O
+    // columns are free once the warpgroup read O of unit n - 2).  Every wait
     // suspends in hardware until its phase completes.
     auto issue_s = [&](int ns) -> bool {
       const int s = ns % kStages, w = ns & 1;
@@ -306,23 +348,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int ns = 0; ok && ns < 2 && ns < n_local; ++ns) ok = issue_s(ns);
     for (int n = 0; ok && n < n_local; ++n) {
-      const int s = n % kStages, w = n & 1, ob = n % kOBufs;
+      const int s = n % kStages, w = n & 1;
       if (!mbar_wait(&bars->p_full[w], (n >> 1) & 1, abort_flag)) break;
-      if (!mbar_wait(&bars->o_free[ob], ((n / kOBufs) & 1) ^ 1, abort_flag)) break;
+      if (n + 2 < n_local && !(ok = issue_s(n + 2))) break;
+      if (n >= 2 && !mbar_wait(&bars->o_free[w], ((n - 2) >> 1) & 1, abort_flag)) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
         for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
           // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
-          tc_mma_ts(tmem + kOCol0 + ob * kD, tmem + kSCol0 + w * 128 + kk * 8,
+          tc_mma_ts(tmem + kOCol0 + w * kD, tmem + kPCol0 + w * 64 + kk * 8,
                     smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
-        tc_commit(&bars->pv_done[ob]);
+        tc_commit(&bars->pv_done[w]);
         tc_commit(&bars->empty[s]);
       }
       __syncwarp();
       last_commit = &bars->empty[s];
       last_commit_parity = (n / kStages) & 1;
-      if (n + 2 < n_local) ok = issue_s(n + 2);
     }
    }
   } else {
@@ -330,9 +372,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- softmax + epilogue: warpgroup w takes units n = w, w + 2, ... -----
     const int w = warp >> 2;
     const int r = threadIdx.x & 127;  // tile row = TMEM lane
-    const int pr = r / g.Rq, i = r % g.Rq;
+    const bool my_rev = rev && w == 1;  // query row of tile row r
+    const int pr = r / g.Rq, i = my_rev ? ((3 - (r >> 5)) << 5) | (r & 31) : r % g.Rq;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tmem = tmem + lane_base + kSCol0 + w * 128;
+    const uint32_t p_tmem = tmem + lane_base + kPCol0 + w * 64;
+    const uint32_t o_tmem = tmem + lane_base + kOCol0 + w * kD;
+    // output rows: this lane stores 16-byte piece (lane & 7) of warp rows
+    // 4 t + (lane >> 3), t = 0..7, so each store instruction writes four
+    // whole 128-byte rows
+    const int rq_shift = __ffs(g.Rq) - 1;
+    const long long row_stride = p.layout == kLayoutBHSD ? 128 : 128LL * p.H;
+    const long long head_stride = p.layout == kLayoutBHSD ? 128LL * p.Lq : 128;
+    const long long batch_stride = 128LL * p.Lq * p.H;
     // a negative scale is applied as |scale| to sign-flipped scores
     const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
     const float sl = fabsf(p.scale_log2);
@@ -368,24 +420,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!mbar_wait(&bars->s_full[w], k & 1, abort_flag)) break;
         tc_fence_after();
-        // keep only this row's keys [col_lo, col_lo + jmax); pass 1: row max
+        // keep only this row's keys [col_lo, col_lo + jmax).  One pass over
+        // the chunks: exponents are taken against the first chunk's max m;
+        // a later chunk may exceed m by up to 2^8 (P stays far from bf16
+        // overflow, and numerator and denominator share m, so the quotient
+        // is unchanged).  A row whose max grows further rescales the P it
+        // already wrote (rare: the scores would have to climb steeply along
+        // the keys).
         const int lo_c = col_lo, hi_c = col_lo + jmax;
-        float m = -INFINITY;
-#pragma unroll 1
-        for (int ch = ch_lo; ch < ch_hi; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(s_tmem + ch * 32, v);
-          tmem_wait_ld();
-          const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
-          chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
-          m = fmaxf(m, chunk_max(v));
-        }
-        const bool any = m != -INFINITY;
-        const float ms = any ? m * sl : 0.f;
-        zero_row = !any;
-        // pass 2: P = exp2(s * sl - ms) as bf16 pairs over the first 64
-        // columns of the S region (chunk ch -> columns [16 ch, 16 ch + 16),
-        // which pass 2 has already read); exactly 0 outside the row's keys
+        float ms = -INFINITY;  // reference max, scaled (log2 units)
+        bool gave_up = false;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
@@ -395,40 +439,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
             chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
-            const float cs = chunk_exp_pack(v, sl, ms, pk);
-            rowsum += any ? cs : 0.f;
-            if (!any) {
-#pragma unroll
-              for (int t = 0; t < 16; ++t) pk[t] = 0u;
+            const float cm = chunk_max(v) * sl;  // -inf when no key of the chunk is kept
+            if (ms == -INFINITY) ms = cm;
+            const bool climb = cm > ms + 8.f;
+            if (__any_sync(0xffffffffu, climb)) {
+              const float f = climb ? ex2_approx(ms - cm) : 1.f;
+              rowsum *= f;
+              for (int c = ch_lo; c < ch; ++c) rescale_p(p_tmem + c * 16, f);
+              if (climb) ms = cm;
             }
+            const float cs = chunk_exp_pack(v, sl, ms == -INFINITY ? 0.f : ms, pk);
+            rowsum += cs;
           } else {
 #pragma unroll
             for (int t = 0; t < 16; ++t) pk[t] = 0u;
           }
-          tmem_st16(s_tmem + ch * 16, pk);
+          // the P columns are free once P V of this warpgroup's previous unit ran
+          if (ch == 0 && k > 0 && !mbar_wait(&bars->pv_done[w], (k - 1) & 1, abort_flag)) {
+            gave_up = true;
+            break;
+          }
+          if (ch == 0) tc_fence_after();
+          tmem_st16(p_tmem + ch * 16, pk);
         }
+        if (gave_up) break;
+        zero_row = ms == -INFINITY;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[w]);
       }
       // epilogue of this warpgroup's previous unit (its P V ran meanwhile)
       if (n - 2 >= 0 && n - 2 < n_local) {
-        const int pn = n - 2, ob = pn % kOBufs;
-        if (!mbar_wait(&bars->pv_done[ob], (pn / kOBufs) & 1, abort_flag)) break;
+        const int pn = n - 2;
+        if (!mbar_wait(&bars->pv_done[w], (pn >> 1) & 1, abort_flag)) break;
         tc_fence_after();
         uint32_t o[2][32];
-        tmem_ld32(tmem + lane_base + kOCol0 + ob * kD, o[0]);
-        tmem_ld32(tmem + lane_base + kOCol0 + ob * kD + 32, o[1]);
+        tmem_ld32(o_tmem, o[0]);
+        tmem_ld32(o_tmem + 32, o[1]);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(&bars->o_free[ob]);
+        mbar_arrive(&bars->o_free[w]);
         // bf16 row into this warp's staging rows (128-byte swizzle), then
-        // lane 0 stores the warp's rows pair by pair (TMA clips rows >= Lq)
+        // read back row-major so every store covers four whole rows
         const float inv = pending_zero ? 0.f : 1.f / rowsum_prev;
         uint8_t *stg = staging + warp * kStagingBytes;
         const uint32_t so = smem_addr(stg);
-        if (lane == 0) tma_store_wait_read0();  // the previous store left this buffer
-        __syncwarp();
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           uint32_t wv[4];
@@ -441,27 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           st_shared_v4(so + sw128_offset(lane, c8), wv[0], wv[1], wv[2], wv[3]);
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          const int u = blockIdx.x + pn * gridDim.x;
-          const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
-          const int rows = g.Rq < 32 ? g.Rq : 32;       // rows of one pair in this warp
-          const int h = rows >= 32 ? 2 : (rows == 16 ? 1 : 0);
-          for (int r0 = (warp & 3) * 32; r0 < (warp & 3) * 32 + 32; r0 += rows) {
-            const int ppair = r0 / g.Rq, i0 = r0 % g.Rq;
-            if (ppair < g.P && h0 + ppair < p.H && i0 < p.Lq)
-              tma_store_4d(&maps.o_rows[h], stg + (r0 - (warp & 3) * 32) * 128, 0, i0,
-                           h0 + ppair, b);
-          }
-          tma_store_commit();
+        const int u = blockIdx.x + pn * gridDim.x;
+        const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
+        uint8_t *obase = static_cast<uint8_t *>(out) + b * batch_stride;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int rr = 4 * t + (lane >> 3);           // warp row
+          const int row = (warp & 3) * 32 + rr;          // tile row
+          const int pr_o = row >> rq_shift;
+          const int i_o = my_rev ? ((3 - (row >> 5)) << 5) | (row & 31) : row & (g.Rq - 1);
+          const uint4 val = ld_shared_v4(so + sw128_offset(rr, lane & 7));
+          if (pr_o < g.P && h0 + pr_o < p.H && i_o < p.Lq)
+            st_global_v4(obase + (h0 + pr_o) * head_stride + i_o * row_stride + (lane & 7) * 16,
+                         val);
         }
+        __syncwarp();
       }
       rowsum_prev = rowsum;
       pending_zero = zero_row;
       len_cur = len_next;
     }
-    if (lane == 0) tma_store_wait0();
   }
 
   // ---- teardown ------------------------------------------------------------
@@ -484,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
-                            int num_sms, cudaStream_t stream) {
+                            void *out, int num_sms, cudaStream_t stream) {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   // setmaxnreg.inc only succeeds if the launch reserved the registers it hands
   // out; refuse to launch a build whose register count would not cover them.
@@ -513,7 +568,7 @@ cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Pro
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_short_tc_kernel, maps, g, p);
+  return cudaLaunchKernelEx(&cfg, attn_short_tc_kernel, maps, g, p, out);
 }
 
 }  // namespace mha

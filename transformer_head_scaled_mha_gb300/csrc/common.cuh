@@ -47,7 +47,7 @@ struct ShortMaps {
   CUtensorMap q_rows[kRowBoxes];       // box (64, 8 (h + 1), 1, 1), for padded tensors
   CUtensorMap k_rows[kRowBoxes];
   CUtensorMap v_rows[kRowBoxes];
-  CUtensorMap o_rows[3];               // box (64, 8 << h, 1, 1): output stores
+  CUtensorMap q_blk32;                 // box (64, 32, 1, 1): causal row-block order
 };
 struct ShortGeom {
   int Rq, Rk, P;       // rows per packed pair (powers of two) and pairs per unit
@@ -56,7 +56,7 @@ struct ShortGeom {
   int rows_q, rows_k;  // load Q / K,V only up to each pair's length (padding)
 };
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
-                            int num_sms, cudaStream_t stream);
+                            void *out, int num_sms, cudaStream_t stream);
 
 struct LongMaps {
   CUtensorMap q, k, v;  // box (64, 128, 1, 1)

@@ -199,15 +199,15 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
         ok = make_map(&m.k_one, k, 64, Lk, H_kv, B, layout, g.Rk, 1) &&
              make_map(&m.v_one, v, 64, Lk, H_kv, B, layout, g.Rk, 1);
       // one row-box map per height 8, 16, ..., Rq (Rk) for the padded tensors
+      if (ok && (mask_kind & kMaskCausal) && g.Rq == 128)
+        ok = make_map(&m.q_blk32, q, 64, Lq, H, B, layout, 32, 1);
       for (int h = 0; ok && g.rows_q && h < g.Rq / 8; ++h)
         ok = make_map(&m.q_rows[h], q, 64, Lq, H, B, layout, 8 * (h + 1), 1);
       for (int h = 0; ok && g.rows_k && h < g.Rk / 8; ++h)
         ok = make_map(&m.k_rows[h], k, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1) &&
              make_map(&m.v_rows[h], v, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1);
-      for (int h = 0; ok && h < 3; ++h)
-        ok = make_map(&m.o_rows[h], out, 64, Lq, H, B, layout, 8 << h, 1);
       if (!ok) return MHA_ERR_CUDA;
-      err = launch_short_tc(m, g, p, sms, stream);
+      err = launch_short_tc(m, g, p, out, sms, stream);
     } else {
       LongMaps m;
       std::memset(&m, 0, sizeof m);
