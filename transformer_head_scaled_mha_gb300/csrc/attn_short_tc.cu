@@ -54,9 +54,9 @@ constexpr int kStageBytes = 3 * kTileBytes;     // Q | K | V
 constexpr int kThreads = 384;  // 3 warpgroups
 constexpr int kWgThreads = 128;
 // Register split: launched at 168 per thread (384 x 168 = 64512); the control
-// warpgroup drops to 64 and the softmax warpgroups rise to 216.
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsControl = 64;
+// warpgroup drops to 80 and the softmax warpgroups rise to 208 (no spills).
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsControl = 80;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of warpgroup w: S (fp32) [128 w, +128), P (bf16 pairs)
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (need_len && n < n_local && pp < g.P && h < p.H) ? clamp_len(p, u / g.units_per_b)
                                                                : 0;
     };
-    int len_n1 = 0, len_n2 = 0;  // read once unit 0's loads are on their way
+    int len_n1 = len_at(1), len_n2 = len_at(2);
     for (int n = 0; n < n_local; ++n) {
       const int s = n % kStages;
       const int u = blockIdx.x + n * gridDim.x;
@@ -313,10 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = n + 1;
-      if (n == 0) {
-        len_n1 = len_at(1);
-        len_n2 = len_at(2);
-      }
     }
   } else if (warp == 9) {
     // ---- MMA issuer (lane 0) ----------------------------------------------
