@@ -87,6 +87,22 @@ __device__ __forceinline__ int clamp_len(const Problem &p, int b) {
   return l < 0 ? 0 : (l > p.Lk ? p.Lk : l);
 }
 
+// (batch element, head group) of the units u0, u0 + step, u0 + 2 step, ...,
+// stepped without a division per unit
+struct UnitWalk {
+  int b, hu, db, dh, per_b;
+  __device__ __forceinline__ UnitWalk(int u0, int step, int per_b_)
+      : b(u0 / per_b_), hu(u0 % per_b_), db(step / per_b_), dh(step % per_b_), per_b(per_b_) {}
+  __device__ __forceinline__ void next() {
+    b += db;
+    hu += dh;
+    if (hu >= per_b) {
+      hu -= per_b;
+      ++b;
+    }
+  }
+};
+
 __device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity))
@@ -249,34 +265,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- TMA producer (lane pp handles pair pp of the unit) -----------------
     const int pp = lane;
     const bool need_len = g.rows_q || g.rows_k;
-    // lane pp's pair length for unit n, read two units ahead of its use
-    auto len_at = [&](int n) -> int {
-      const int u = blockIdx.x + n * gridDim.x;
-      const int h = (u % g.units_per_b) * g.P + pp;
-      return (need_len && n < n_local && pp < g.P && h < p.H) ? clamp_len(p, u / g.units_per_b)
-                                                               : 0;
+    // lane pp's pair length for the unit at `at` (unit n), read two units
+    // ahead of its use
+    auto len_at = [&](const UnitWalk &at, int n) -> int {
+      return (need_len && n < n_local && pp < g.P && at.hu * g.P + pp < p.H) ? clamp_len(p, at.b)
+                                                                           : 0;
     };
-    int len_n1 = len_at(1), len_n2 = len_at(2);
-    for (int n = 0; n < n_local; ++n) {
+    UnitWalk cur(blockIdx.x, gridDim.x, g.units_per_b);
+    UnitWalk ahead(blockIdx.x + gridDim.x, gridDim.x, g.units_per_b);
+    int len_n1 = len_at(ahead, 1);
+    ahead.next();
+    int len_n2 = len_at(ahead, 2);
+    for (int n = 0; n < n_local; ++n, cur.next()) {
       const int s = n % kStages;
-      const int u = blockIdx.x + n * gridDim.x;
-      const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
+      const int b = cur.b, h0 = cur.hu * g.P;
       // key/value head of pair pp (a pair past the last head, whose rows are
       // never stored, reads the last head so every box is in bounds)
-      const int hkv = min(h0 + pp, p.H - 1) / group;
+      const int hq = min(h0 + pp, p.H - 1);
+      const int hkv = group == 1 ? hq : hq / group;
       // the first unit loads whole tiles: no wait for the lengths
       const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
       const bool has_pair = pp < g.P && h0 + pp < p.H;
       const int len = n > 0 ? len_n1 : 0;
       if (n > 0) {
+        ahead.next();
         len_n1 = len_n2;
-        len_n2 = len_at(n + 2);
+        len_n2 = len_at(ahead, n + 2);
       }
       uint32_t bytes = 0;
       if (has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
       if (has_pair && rows_k) bytes += 2 * box_bytes(len);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      bytes = __reduce_add_sync(0xffffffffu, bytes);
       if (!rows_q) bytes += g.P * g.Rq * 128;
       if (!rows_k) bytes += 2 * g.P * g.Rk * 128;
       if (!mbar_wait(&bars->empty[s], ((n / kStages) & 1) ^ 1, abort_flag)) break;
@@ -385,22 +404,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
     const float sl = fabsf(p.scale_log2);
 
-    auto len_of = [&](int n) -> int {
-      const int u = blockIdx.x + n * gridDim.x;
-      const bool valid = pr < g.P && (u % g.units_per_b) * g.P + pr < p.H && i < p.Lq;
-      return valid ? clamp_len(p, u / g.units_per_b) : 0;
+    // this thread's row is real in the unit at `at`
+    auto row_valid = [&](const UnitWalk &at) -> bool {
+      return pr < g.P && at.hu * g.P + pr < p.H && i < p.Lq;
     };
-    int len_cur = w < n_local ? len_of(w) : 0;
+    UnitWalk cur(blockIdx.x + w * gridDim.x, 2 * gridDim.x, g.units_per_b);
+    UnitWalk nxt = cur;
+    nxt.next();
+    int len_cur = (w < n_local && row_valid(cur)) ? clamp_len(p, cur.b) : 0;
     float rowsum_prev = 0.f;  // row sum of the unit whose epilogue is pending
     bool pending_zero = true;
-    for (int n = w; n < n_local + 2; n += 2) {
+    int prev_b = 0, prev_h0 = 0;  // the pending unit's batch element and first head
+    for (int n = w; n < n_local + 2; n += 2, cur.next(), nxt.next()) {
       float rowsum = 0.f;
       bool zero_row = true;
-      const int len_next = n + 2 < n_local ? len_of(n + 2) : 0;  // load ahead of its use
+      // load ahead of its use
+      const int len_next = (n + 2 < n_local && row_valid(nxt)) ? clamp_len(p, nxt.b) : 0;
       if (n < n_local) {
         const int k = n >> 1;  // this warpgroup's k-th unit
-        const int u = blockIdx.x + n * gridDim.x;
-        const bool valid = pr < g.P && (u % g.units_per_b) * g.P + pr < p.H && i < p.Lq;
+        const bool valid = row_valid(cur);
         const int len = len_cur;
         int jmax = p.Lk;
         if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
@@ -493,8 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_v4(so + sw128_offset(lane, c8), wv[0], wv[1], wv[2], wv[3]);
         }
         __syncwarp();
-        const int u = blockIdx.x + pn * gridDim.x;
-        const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
+        const int b = prev_b, h0 = prev_h0;
         uint8_t *obase = static_cast<uint8_t *>(out) + b * batch_stride;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
@@ -512,6 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       rowsum_prev = rowsum;
       pending_zero = zero_row;
       len_cur = len_next;
+      prev_b = cur.b;
+      prev_h0 = cur.hu * g.P;
     }
   }
 
