@@ -231,6 +231,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&maps.q_full);
     tma_prefetch_desc(group == 1 ? &maps.k_full : &maps.k_one);
     tma_prefetch_desc(group == 1 ? &maps.v_full : &maps.v_one);
+    // While the previous grid drains, warm L2 with this CTA's first two
+    // units (whole tiles) and first three lengths.  All global writes land
+    // in L2, so an L2 prefetch can never make a later read stale; the reads
+    // that count still come after the dependency wait below.
+    for (int n = 0; n < 3 && n < n_local; ++n) {
+      const int u = blockIdx.x + n * gridDim.x;
+      const int b = u / g.units_per_b, h0 = (u % g.units_per_b) * g.P;
+      if (p.key_lengths != nullptr) prefetch_l2(p.key_lengths + b);
+      if (n < 2) {
+        tma_prefetch_l2_4d(&maps.q_full, 0, 0, h0, b);
+        if (group == 1) {
+          tma_prefetch_l2_4d(&maps.k_full, 0, 0, h0, b);
+          tma_prefetch_l2_4d(&maps.v_full, 0, 0, h0, b);
+        }
+      }
+    }
   }
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
