@@ -10,25 +10,27 @@
 // K and V of head h / (H / H_kv).  Each CTA is persistent (one per SM) and
 // walks the units u = blockIdx.x, + gridDim.x, ...
 //
-// Warp roles (384 threads):
-//   warps 0-3, 4-7  two softmax warpgroups; unit n goes to warpgroup n % 2,
-//                   thread t owns tile row t
-//   warp  8         TMA producer: Q, K, V of a unit into a 4-stage ring
-//   warp  9         TMEM owner and MMA issuer
-//   warps 10-11     idle; they complete the third warpgroup so its register
-//                   budget can be handed to the softmax warpgroups
+// Warp roles (640 threads):
+//   warps 0-15      four softmax warpgroups; unit n goes to warpgroup n % 4,
+//                   thread t of a warpgroup owns tile row t
+//   warp  16        TMA producer of Q and K (a 4-stage Q|K ring)
+//   warp  17        TMA producer of V (a 4-stage V ring)
+//   warp  18        TMEM owner and MMA issuer
+//   warp  19        idle
 // Per unit (the four steps of scaled dot-product attention):
-//   S = Q K^T              tcgen05.mma -> TMEM (fp32), one region per warpgroup
+//   S = Q K^T              tcgen05.mma -> the warpgroup's 128 TMEM columns
 //   mask, scale, softmax   tcgen05.ld of the 32-column chunks the warp's rows
 //                          can use -> registers; exp2 against the row max
-//   P (bf16) -> TMEM       the warpgroup's own P columns, so S of its next
-//                          unit is computed while P V still reads P
-//   O = P V                tcgen05.mma (A = P from TMEM) -> TMEM
-//   O / rowsum -> bf16     tcgen05.ld; each warp stages its 32 rows in a
-//                          swizzled 4 KiB buffer and writes them back with
-//                          stores that each cover four whole rows
-// The MMA warp issues S for unit n + 2 as soon as the warpgroup posted P for
-// unit n, and P V for unit n once the warpgroup has read O of unit n - 2.
+//   P (bf16) -> TMEM       over the S columns already read
+//   O = P V                tcgen05.mma (A = P from TMEM) -> the upper 64 of the
+//                          warpgroup's columns
+//   O / rowsum -> bf16     tcgen05.ld, 32 columns at a time; each warp stages
+//                          its 32 half-rows in a swizzled 2 KiB buffer and
+//                          writes them back, eight 64-byte pieces per store
+// A Q|K stage is free once S is computed, a V stage once P V is: Q and K run
+// ahead of the softmax independently of V.  The MMA warp issues whichever of
+// the next S (its warpgroup free, Q and K landed) and the next P V (P
+// posted, V landed) is ready.
 // Padded sequences load only their first ceil(len/8)*8 rows, as one TMA box
 // of that height per tensor and pair, so padding costs no HBM reads (a CTA's
 // first unit loads whole tiles instead, so it does not wait for the lengths).
@@ -47,39 +49,31 @@ namespace mha {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kStages = 4;
+constexpr int kWGs = 4;                         // softmax warpgroups
+constexpr int kStages = 4;                      // Q|K stages and V stages
 constexpr int kTileRows = 128;
 constexpr int kTileBytes = kTileRows * kD * 2;  // 16 KiB per operand tile
-constexpr int kStageBytes = 3 * kTileBytes;     // Q | K | V
-constexpr int kThreads = 384;  // 3 warpgroups
+constexpr int kThreads = (kWGs + 1) * 128;      // 640
 constexpr int kWgThreads = 128;
-// Register split: launched at 168 per thread (384 x 168 = 64512); the control
-// warpgroup drops to 80 and the softmax warpgroups rise to 208 (no spills).
-constexpr uint32_t kRegsSoftmax = 208;
-constexpr uint32_t kRegsControl = 80;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
-constexpr uint32_t kTmemCols = 512;
-// TMEM columns of warpgroup w: S (fp32) [128 w, +128), P (bf16 pairs)
-// [256 + 64 w, +64), O (fp32) [384 + 64 w, +64).  P has its own columns so
-// the next S of a warpgroup can be computed while P V still reads P.
-constexpr uint32_t kSCol0 = 0;
-constexpr uint32_t kPCol0 = 256;
-constexpr uint32_t kOCol0 = 384;
+constexpr int kWarpProdQK = 4 * kWGs, kWarpProdV = kWarpProdQK + 1, kWarpMma = kWarpProdQK + 2;
+// 640 threads at 96 registers each fill the register file; every role fits in
+// 96 without spills, so no register split is needed.
+constexpr uint32_t kTmemCols = 512;  // warpgroup w: [128 w, 128 w + 128)
 
 struct __align__(8) Barriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t s_full[2];   // S of the warpgroup's unit is in TMEM
-  uint64_t p_full[2];   // the warpgroup read its S and wrote P
-  uint64_t pv_done[2];  // P V done: O ready, P columns free
-  uint64_t o_free[2];   // the warpgroup read O
+  uint64_t qk_full[kStages], qk_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[kWGs];   // S of the warpgroup's unit is in TMEM
+  uint64_t p_full[kWGs];   // the warpgroup read its S and wrote P
+  uint64_t pv_done[kWGs];  // P V done: O ready
+  uint64_t o_free[kWGs];   // the warpgroup read O: its columns are free
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr int kStagingBytes = 32 * 128;  // one warp's 32 output rows
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes +
-                              8 * kStagingBytes + sizeof(Barriers);
+constexpr int kStagingBytes = 32 * 64;  // 32 output half-rows of one warp
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * 2 * kTileBytes +
+                              kStages * kTileBytes + 4 * kWGs * kStagingBytes + sizeof(Barriers);
 
 __device__ __forceinline__ int clamp_len(const Problem &p, int b) {
   if (!(p.mask & (kMaskKeyPadding | kMaskQueryPadding))) return p.Lk;
@@ -102,6 +96,13 @@ struct UnitWalk {
     }
   }
 };
+
+// byte offset of 16-byte piece c (0..3) of 64-byte row `row` in a warp's
+// staging buffer, swizzled so that eight consecutive lanes (one shared
+// memory wavefront) never share a bank group, writing or reading
+__device__ __forceinline__ uint32_t stage64_offset(uint32_t row, uint32_t c) {
+  return row * 64u + ((c ^ ((row >> 1) & 3u)) << 4);
+}
 
 __device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -195,19 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *stage_base = smem;
-  uint8_t *staging = smem + kStages * kStageBytes;  // 8 softmax warps x 4 KiB
-  Barriers *bars = reinterpret_cast<Barriers *>(staging + 8 * kStagingBytes);
+  uint8_t *qk_base = smem;                              // stage s: Q | K, 32 KiB
+  uint8_t *v_base = qk_base + kStages * 2 * kTileBytes;  // stage s: V, 16 KiB
+  uint8_t *staging = v_base + kStages * kTileBytes;     // 16 softmax warps x 2 KiB
+  Barriers *bars = reinterpret_cast<Barriers *>(staging + 4 * kWGs * kStagingBytes);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = p.H / p.Hkv;  // query heads per key/value head
   // Causal 128-row tiles: row 96 + t needs four 32-key chunks of softmax,
   // row t one, and TMEM lanes 32 q .. 32 q + 31 belong to the warps on SM
-  // sub-partition q.  Warpgroup 1 therefore holds its query rows with the
-  // 32-row blocks in reverse order, so each sub-partition gets one heavy and
-  // one light warp.
-  const bool rev = (p.mask & kMaskCausal) && g.Rq == 128 && !g.rows_q;
+  // sub-partition q.  Warpgroup w holds query-row block (j + w) % 4 in tile
+  // rows 32 j .. 32 j + 31, so each sub-partition gets every kind of block.
+  const bool rot = (p.mask & kMaskCausal) && g.Rq == 128 && !g.rows_q;
   const int n_local = (static_cast<int>(blockIdx.x) < g.units)
                           ? (g.units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
                           : 0;
@@ -215,10 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup -------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->qk_full[s], 1);
+      mbar_init(&bars->qk_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
-    for (int w = 0; w < 2; ++w) {
+    for (int w = 0; w < kWGs; ++w) {
       mbar_init(&bars->s_full[w], 1);
       mbar_init(&bars->p_full[w], kWgThreads);
       mbar_init(&bars->pv_done[w], 1);
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kWarpProdQK && lane == 0) {
     tma_prefetch_desc(&maps.q_full);
     tma_prefetch_desc(group == 1 ? &maps.k_full : &maps.k_one);
     tma_prefetch_desc(group == 1 ? &maps.v_full : &maps.v_one);
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -256,11 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // from zeros so they are always finite (their weights are exactly zero, and
   // 0 * NaN would not be).  Unloaded K and Q rows are masked by selection.
   if (g.rows_k) {
-    for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads) {
-      const int st = i / (kTileBytes / 16), off = i % (kTileBytes / 16);
-      reinterpret_cast<uint4 *>(stage_base + st * kStageBytes + 2 * kTileBytes)[off] =
-          make_uint4(0, 0, 0, 0);
-    }
+    for (int i = threadIdx.x; i < kStages * kTileBytes / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(v_base)[i] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -272,15 +272,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
 
-  int issued = 0;                   // producer: units whose loads were issued
+  int issued = 0;                   // producers: units whose loads were issued
   uint64_t *last_commit = nullptr;  // MMA issuer: barrier of the last commit
   uint32_t last_commit_parity = 0;
-  if (warp >= 8) {
-   regs_dec<kRegsControl>();
-   if (warp == 8) {
-    // ---- TMA producer (lane pp handles pair pp of the unit) -----------------
+  if (warp >= 4 * kWGs) {
+   if (warp == kWarpProdQK || warp == kWarpProdV) {
+    // ---- TMA producers (lane pp handles pair pp of the unit) ---------------
+    const bool is_qk = warp == kWarpProdQK;
     const int pp = lane;
-    const bool need_len = g.rows_q || g.rows_k;
+    const bool need_len = is_qk ? (g.rows_q || g.rows_k) : g.rows_k != 0;
     // lane pp's pair length for the unit at `at` (unit n), read two units
     // ahead of its use
     auto len_at = [&](const UnitWalk &at, int n) -> int {
@@ -309,258 +309,249 @@ __global__ void __launch_bounds__(kThreads, 1)
         len_n2 = len_at(ahead, n + 2);
       }
       uint32_t bytes = 0;
-      if (has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
-      if (has_pair && rows_k) bytes += 2 * box_bytes(len);
+      if (is_qk && has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
+      if (has_pair && rows_k) bytes += box_bytes(len);
       bytes = __reduce_add_sync(0xffffffffu, bytes);
-      if (!rows_q) bytes += g.P * g.Rq * 128;
-      if (!rows_k) bytes += 2 * g.P * g.Rk * 128;
-      if (!mbar_wait(&bars->empty[s], ((n / kStages) & 1) ^ 1, abort_flag)) break;
-      uint8_t *sq = stage_base + s * kStageBytes;
-      uint8_t *sk = sq + kTileBytes;
-      uint8_t *sv = sk + kTileBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&bars->full[s], bytes);
+      if (is_qk && !rows_q) bytes += g.P * g.Rq * 128;
+      if (!rows_k) bytes += g.P * g.Rk * 128;
+      uint64_t *full = is_qk ? &bars->qk_full[s] : &bars->v_full[s];
+      uint64_t *empty = is_qk ? &bars->qk_empty[s] : &bars->v_empty[s];
+      if (!mbar_wait(empty, ((n / kStages) & 1) ^ 1, abort_flag)) break;
+      uint8_t *dq = qk_base + s * 2 * kTileBytes;  // Q tile (Q|K stage)
+      uint8_t *dk = is_qk ? dq + kTileBytes : v_base + s * kTileBytes;  // K or V tile
+      const CUtensorMap *kv_full = is_qk ? &maps.k_full : &maps.v_full;
+      const CUtensorMap *kv_one = is_qk ? &maps.k_one : &maps.v_one;
+      const CUtensorMap *kv_rows = is_qk ? maps.k_rows : maps.v_rows;
+      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
+      if (is_qk) {
+        const int w = n % kWGs;
+        if (rot && w != 0) {
+          // rotated 32-row blocks (see above)
+          if (lane < 4)
+            tma_load_4d(dq + lane * 32 * 128, &maps.q_blk32, full, 0, ((lane + w) & 3) * 32, h0,
+                        b);
+        } else if (lane == 0 && !rows_q) {
+          tma_load_4d(dq, &maps.q_full, full, 0, 0, h0, b);
+        }
+        if (has_pair && rows_q)
+          load_rows(dq + pp * g.Rq * 128, maps.q_rows, full, min(len, p.Lq), h0 + pp, b);
+      }
       // whole tiles: one box of P heads, or with shared key/value heads one
       // box per pair (heads past H read as zeros and are never stored)
-      if (rev && (n & 1)) {
-        // warpgroup 1 of a causal tile: reversed 32-row blocks (see above)
-        if (lane < 4)
-          tma_load_4d(sq + lane * 32 * 128, &maps.q_blk32, &bars->full[s], 0, (3 - lane) * 32, h0,
-                      b);
-      } else if (lane == 0 && !rows_q) {
-        tma_load_4d(sq, &maps.q_full, &bars->full[s], 0, 0, h0, b);
-      }
-      if (lane == 0) {
-        if (!rows_k && group == 1) {
-          tma_load_4d(sk, &maps.k_full, &bars->full[s], 0, 0, h0, b);
-          tma_load_4d(sv, &maps.v_full, &bars->full[s], 0, 0, h0, b);
-        }
-      }
-      if (!rows_k && group != 1 && pp < g.P) {
-        tma_load_4d(sk + pp * g.Rk * 128, &maps.k_one, &bars->full[s], 0, 0, hkv, b);
-        tma_load_4d(sv + pp * g.Rk * 128, &maps.v_one, &bars->full[s], 0, 0, hkv, b);
-      }
-      if (has_pair && rows_q) load_rows(sq + pp * g.Rq * 128, maps.q_rows, &bars->full[s],
-                                        min(len, p.Lq), h0 + pp, b);
-      if (has_pair && rows_k) {
-        load_rows(sk + pp * g.Rk * 128, maps.k_rows, &bars->full[s], len, hkv, b);
-        load_rows(sv + pp * g.Rk * 128, maps.v_rows, &bars->full[s], len, hkv, b);
-      }
+      if (!rows_k && group == 1 && lane == 0) tma_load_4d(dk, kv_full, full, 0, 0, h0, b);
+      if (!rows_k && group != 1 && pp < g.P)
+        tma_load_4d(dk + pp * g.Rk * 128, kv_one, full, 0, 0, hkv, b);
+      if (has_pair && rows_k) load_rows(dk + pp * g.Rk * 128, kv_rows, full, len, hkv, b);
       __syncwarp();
       issued = n + 1;
     }
-  } else if (warp == 9) {
+   } else if (warp == kWarpMma) {
     // ---- MMA issuer (lane 0) ----------------------------------------------
     const uint32_t n_keys = static_cast<uint32_t>(g.P * g.Rk);  // multiple of 16, <= 128
     const uint32_t idesc_s = idesc_bf16_f32(128, n_keys, 0);
     const uint32_t idesc_o = idesc_bf16_f32(128, kD, 1);
-    // Fixed order S_0, S_1, then for each unit n: S for n + 2 (warpgroup
-    // n % 2 is done reading S_n once it posted P_n), then P V for n (its O
-    // columns are free once the warpgroup read O of unit n - 2).  Every wait
-    // suspends in hardware until its phase completes.
-    auto issue_s = [&](int ns) -> bool {
-      const int s = ns % kStages, w = ns & 1;
-      if (!mbar_wait(&bars->full[s], (ns / kStages) & 1, abort_flag)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sq = smem_addr(stage_base + s * kStageBytes);
-        const uint32_t sk = sq + kTileBytes;
+    // S for unit ns needs its Q|K stage and its warpgroup's columns (free
+    // once O of unit ns - 4 was read); P V for unit np needs P and the V
+    // stage.  Issue whichever is ready; each stream stays in unit order.
+    int ns = 0, np = 0;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t idle = 0;
+    while (np < n_local) {
+      bool did = false;
+      if (ns < n_local) {
+        const int s = ns % kStages, w = ns % kWGs;
+        if (mbar_probe(&bars->qk_full[s], (ns / kStages) & 1) &&
+            (ns < kWGs || mbar_probe(&bars->o_free[w], ((ns - kWGs) / kWGs) & 1))) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sq = smem_addr(qk_base + s * 2 * kTileBytes);
+            const uint32_t sk = sq + kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          tc_mma_ss(tmem + kSCol0 + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
-                    smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
-        tc_commit(&bars->s_full[w]);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              tc_mma_ss(tmem + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
+                        smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
+            tc_commit(&bars->s_full[w]);
+            tc_commit(&bars->qk_empty[s]);
+          }
+          __syncwarp();
+          last_commit = &bars->qk_empty[s];
+          last_commit_parity = (ns / kStages) & 1;
+          ++ns;
+          did = true;
+        }
       }
-      __syncwarp();
-      last_commit = &bars->s_full[w];
-      last_commit_parity = (ns >> 1) & 1;
-      return true;
-    };
-    bool ok = true;
-    for (int ns = 0; ok && ns < 2 && ns < n_local; ++ns) ok = issue_s(ns);
-    for (int n = 0; ok && n < n_local; ++n) {
-      const int s = n % kStages, w = n & 1;
-      if (!mbar_wait(&bars->p_full[w], (n >> 1) & 1, abort_flag)) break;
-      if (n + 2 < n_local && !(ok = issue_s(n + 2))) break;
-      if (n >= 2 && !mbar_wait(&bars->o_free[w], ((n - 2) >> 1) & 1, abort_flag)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sv = smem_addr(stage_base + s * kStageBytes + 2 * kTileBytes);
-        for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
-          // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
-          tc_mma_ts(tmem + kOCol0 + w * kD, tmem + kPCol0 + w * 64 + kk * 8,
-                    smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
-        tc_commit(&bars->pv_done[w]);
-        tc_commit(&bars->empty[s]);
+      if (np < ns) {
+        const int s = np % kStages, w = np % kWGs;
+        if (mbar_probe(&bars->p_full[w], (np / kWGs) & 1) &&
+            mbar_probe(&bars->v_full[s], (np / kStages) & 1)) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sv = smem_addr(v_base + s * kTileBytes);
+            for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
+              // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
+              tc_mma_ts(tmem + w * 128 + 64, tmem + w * 128 + kk * 8,
+                        smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
+            tc_commit(&bars->pv_done[w]);
+            tc_commit(&bars->v_empty[s]);
+          }
+          __syncwarp();
+          last_commit = &bars->v_empty[s];
+          last_commit_parity = (np / kStages) & 1;
+          ++np;
+          did = true;
+        }
       }
-      __syncwarp();
-      last_commit = &bars->empty[s];
-      last_commit_parity = (n / kStages) & 1;
+      if (!did && (++idle & 63u) == 0) {
+        if (*abort_flag) break;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          break;
+        }
+      }
     }
    }
   } else {
-    regs_inc<kRegsSoftmax>();
-    // ---- softmax + epilogue: warpgroup w takes units n = w, w + 2, ... -----
+    // ---- softmax + epilogue: warpgroup w takes units n = w, w + 4, ... -----
     const int w = warp >> 2;
     const int r = threadIdx.x & 127;  // tile row = TMEM lane
-    const bool my_rev = rev && w == 1;  // query row of tile row r
-    const int pr = r / g.Rq, i = my_rev ? ((3 - (r >> 5)) << 5) | (r & 31) : r % g.Rq;
+    const bool my_rot = rot && w != 0;  // query row of tile row r
+    const int pr = r / g.Rq;
+    const int i = my_rot ? ((((r >> 5) + w) & 3) << 5) | (r & 31) : r % g.Rq;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_base + kSCol0 + w * 128;
-    const uint32_t p_tmem = tmem + lane_base + kPCol0 + w * 64;
-    const uint32_t o_tmem = tmem + lane_base + kOCol0 + w * kD;
-    // output rows: this lane stores 16-byte piece (lane & 7) of warp rows
-    // 4 t + (lane >> 3), t = 0..7, so each store instruction writes four
-    // whole 128-byte rows
+    const uint32_t s_tmem = tmem + lane_base + w * 128;  // S; P over its first 64
+    const uint32_t o_tmem = s_tmem + 64;                 // O
+    // a negative scale is applied as |scale| to sign-flipped scores
+    const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
+    const float sl = fabsf(p.scale_log2);
     const int rq_shift = __ffs(g.Rq) - 1;
     const long long row_stride = p.layout == kLayoutBHSD ? 128 : 128LL * p.H;
     const long long head_stride = p.layout == kLayoutBHSD ? 128LL * p.Lq : 128;
     const long long batch_stride = 128LL * p.Lq * p.H;
-    // a negative scale is applied as |scale| to sign-flipped scores
-    const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
-    const float sl = fabsf(p.scale_log2);
+    const uint32_t so = smem_addr(staging + warp * kStagingBytes);
 
-    // this thread's row is real in the unit at `at`
     auto row_valid = [&](const UnitWalk &at) -> bool {
       return pr < g.P && at.hu * g.P + pr < p.H && i < p.Lq;
     };
-    UnitWalk cur(blockIdx.x + w * gridDim.x, 2 * gridDim.x, g.units_per_b);
-    UnitWalk nxt = cur;
-    nxt.next();
+    UnitWalk cur(blockIdx.x + w * gridDim.x, kWGs * gridDim.x, g.units_per_b);
     int len_cur = (w < n_local && row_valid(cur)) ? clamp_len(p, cur.b) : 0;
-    float rowsum_prev = 0.f;  // row sum of the unit whose epilogue is pending
-    bool pending_zero = true;
-    int prev_b = 0, prev_h0 = 0;  // the pending unit's batch element and first head
-    for (int n = w; n < n_local + 2; n += 2, cur.next(), nxt.next()) {
-      float rowsum = 0.f;
-      bool zero_row = true;
-      // load ahead of its use
-      const int len_next = (n + 2 < n_local && row_valid(nxt)) ? clamp_len(p, nxt.b) : 0;
-      if (n < n_local) {
-        const int k = n >> 1;  // this warpgroup's k-th unit
-        const bool valid = row_valid(cur);
-        const int len = len_cur;
-        int jmax = p.Lk;
-        if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
-        if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
-        const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
-        if (!valid || qpad) jmax = 0;
-        const int col_lo = pr * g.Rk;
-        // 32-column chunks any row of this warp can use
-        const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
-        const unsigned hi = __reduce_max_sync(0xffffffffu, jmax > 0 ? col_lo + jmax : 0);
-        const int ch_lo = hi > 0 ? static_cast<int>(lo / 32) : 4;
-        const int ch_hi = hi > 0 ? static_cast<int>((hi + 31) / 32) : 0;
+    for (int n = w; n < n_local; n += kWGs) {
+      const int k = n / kWGs;  // this warpgroup's k-th unit
+      const bool valid = row_valid(cur);
+      const int len = len_cur;
+      int jmax = p.Lk;
+      if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
+      if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
+      const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
+      if (!valid || qpad) jmax = 0;
+      const int col_lo = pr * g.Rk;
+      // 32-column chunks any row of this warp can use
+      const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
+      const unsigned hi = __reduce_max_sync(0xffffffffu, jmax > 0 ? col_lo + jmax : 0);
+      const int ch_lo = hi > 0 ? static_cast<int>(lo / 32) : 4;
+      const int ch_hi = hi > 0 ? static_cast<int>((hi + 31) / 32) : 0;
 
-        if (!mbar_wait(&bars->s_full[w], k & 1, abort_flag)) break;
-        tc_fence_after();
-        // keep only this row's keys [col_lo, col_lo + jmax).  One pass over
-        // the chunks: exponents are taken against the first chunk's max m;
-        // a later chunk may exceed m by up to 2^8 (P stays far from bf16
-        // overflow, and numerator and denominator share m, so the quotient
-        // is unchanged).  A row whose max grows further rescales the P it
-        // already wrote (rare: the scores would have to climb steeply along
-        // the keys).
-        const int lo_c = col_lo, hi_c = col_lo + jmax;
-        float ms = -INFINITY;  // reference max, scaled (log2 units)
-        bool gave_up = false;
+      if (!mbar_wait(&bars->s_full[w], k & 1, abort_flag)) break;
+      tc_fence_after();
+      // keep only this row's keys [col_lo, col_lo + jmax).  One pass over
+      // the chunks: exponents are taken against the first chunk's max m;
+      // a later chunk may exceed m by up to 2^8 (P stays far from bf16
+      // overflow, and numerator and denominator share m, so the quotient
+      // is unchanged).  A row whose max grows further rescales the P it
+      // already wrote (rare: the scores would have to climb steeply along
+      // the keys).  P of chunk ch goes to columns [16 ch, 16 ch + 16), which
+      // hold scores already read.
+      const int lo_c = col_lo, hi_c = col_lo + jmax;
+      float ms = -INFINITY;  // reference max, scaled (log2 units)
+      float rowsum = 0.f;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
-          if (ch >= ch_lo && ch < ch_hi) {
-            uint32_t v[32];
-            tmem_ld32(s_tmem + ch * 32, v);
-            tmem_wait_ld();
-            const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
-            chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
-            const float cm = chunk_max(v) * sl;  // -inf when no key of the chunk is kept
-            if (ms == -INFINITY) ms = cm;
-            const bool climb = cm > ms + 8.f;
-            if (__any_sync(0xffffffffu, climb)) {
-              const float f = climb ? ex2_approx(ms - cm) : 1.f;
-              rowsum *= f;
-              for (int c = ch_lo; c < ch; ++c) rescale_p(p_tmem + c * 16, f);
-              if (climb) ms = cm;
-            }
-            const float cs = chunk_exp_pack(v, sl, ms == -INFINITY ? 0.f : ms, pk);
-            rowsum += cs;
-          } else {
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+        if (ch >= ch_lo && ch < ch_hi) {
+          uint32_t v[32];
+          tmem_ld32(s_tmem + ch * 32, v);
+          tmem_wait_ld();
+          const bool mask = __any_sync(0xffffffffu, ch * 32 < lo_c || ch * 32 + 32 > hi_c);
+          chunk_prepare(v, ch * 32, sgn, mask, lo_c, hi_c);
+          const float cm = chunk_max(v) * sl;  // -inf when no key of the chunk is kept
+          if (ms == -INFINITY) ms = cm;
+          const bool climb = cm > ms + 8.f;
+          if (__any_sync(0xffffffffu, climb)) {
+            const float f = climb ? ex2_approx(ms - cm) : 1.f;
+            rowsum *= f;
+            for (int c = ch_lo; c < ch; ++c) rescale_p(s_tmem + c * 16, f);
+            if (climb) ms = cm;
+          }
+          rowsum += chunk_exp_pack(v, sl, ms == -INFINITY ? 0.f : ms, pk);
+        } else {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) pk[t] = 0u;
-          }
-          // the P columns are free once P V of this warpgroup's previous unit ran
-          if (ch == 0 && k > 0 && !mbar_wait(&bars->pv_done[w], (k - 1) & 1, abort_flag)) {
-            gave_up = true;
-            break;
-          }
-          if (ch == 0) tc_fence_after();
-          tmem_st16(p_tmem + ch * 16, pk);
+          for (int t = 0; t < 16; ++t) pk[t] = 0u;
         }
-        if (gave_up) break;
-        zero_row = ms == -INFINITY;
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[w]);
+        tmem_st16(s_tmem + ch * 16, pk);
       }
-      // epilogue of this warpgroup's previous unit (its P V ran meanwhile)
-      if (n - 2 >= 0 && n - 2 < n_local) {
-        const int pn = n - 2;
-        if (!mbar_wait(&bars->pv_done[w], (pn >> 1) & 1, abort_flag)) break;
-        tc_fence_after();
-        uint32_t o[2][32];
-        tmem_ld32(o_tmem, o[0]);
-        tmem_ld32(o_tmem + 32, o[1]);
+      const bool zero_row = ms == -INFINITY;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[w]);
+
+      // ---- epilogue: O / rowsum -> bf16 -> global, 32 columns at a time ----
+      if (!mbar_wait(&bars->pv_done[w], k & 1, abort_flag)) break;
+      tc_fence_after();
+      const float inv = zero_row ? 0.f : 1.f / rowsum;
+      const int b = cur.b, h0 = cur.hu * g.P;
+      uint8_t *obase = static_cast<uint8_t *>(out) + b * batch_stride;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+        tmem_ld32(o_tmem + 32 * half, o);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->o_free[w]);
-        // bf16 row into this warp's staging rows (128-byte swizzle), then
-        // read back row-major so every store covers four whole rows
-        const float inv = pending_zero ? 0.f : 1.f / rowsum_prev;
-        uint8_t *stg = staging + warp * kStagingBytes;
-        const uint32_t so = smem_addr(stg);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->o_free[w]);
+        }
+        // this lane's row, 64 bytes, into the warp's staging rows
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t wv[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const int c = c8 * 8 + 2 * t;
-            wv[t] = pending_zero ? 0u
-                                 : pack_bf16x2(__uint_as_float(o[c >> 5][c & 31]) * inv,
-                                               __uint_as_float(o[c >> 5][(c + 1) & 31]) * inv);
+            const int c = c4 * 8 + 2 * t;
+            wv[t] = zero_row ? 0u
+                             : pack_bf16x2(__uint_as_float(o[c]) * inv,
+                                           __uint_as_float(o[c + 1]) * inv);
           }
-          st_shared_v4(so + sw128_offset(lane, c8), wv[0], wv[1], wv[2], wv[3]);
+          st_shared_v4(so + stage64_offset(lane, c4), wv[0], wv[1], wv[2], wv[3]);
         }
         __syncwarp();
-        const int b = prev_b, h0 = prev_h0;
-        uint8_t *obase = static_cast<uint8_t *>(out) + b * batch_stride;
+        // eight rows per store instruction, 64 contiguous bytes of each
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const int rr = 4 * t + (lane >> 3);           // warp row
-          const int row = (warp & 3) * 32 + rr;          // tile row
+        for (int t = 0; t < 4; ++t) {
+          const int rr = 8 * t + (lane >> 2);   // warp row
+          const int row = (warp & 3) * 32 + rr;  // tile row
           const int pr_o = row >> rq_shift;
-          const int i_o = my_rev ? ((3 - (row >> 5)) << 5) | (row & 31) : row & (g.Rq - 1);
-          const uint4 val = ld_shared_v4(so + sw128_offset(rr, lane & 7));
+          const int i_o = my_rot ? ((((row >> 5) + w) & 3) << 5) | (row & 31) : row & (g.Rq - 1);
+          const uint4 val = ld_shared_v4(so + stage64_offset(rr, lane & 3));
           if (pr_o < g.P && h0 + pr_o < p.H && i_o < p.Lq)
-            st_global_v4(obase + (h0 + pr_o) * head_stride + i_o * row_stride + (lane & 7) * 16,
+            st_global_v4(obase + (h0 + pr_o) * head_stride + i_o * row_stride + half * 64 +
+                             (lane & 3) * 16,
                          val);
         }
         __syncwarp();
       }
-      rowsum_prev = rowsum;
-      pending_zero = zero_row;
-      len_cur = len_next;
-      prev_b = cur.b;
-      prev_h0 = cur.hu * g.P;
+      // the next unit's length, loaded while its scores are computed
+      cur.next();
+      len_cur = (n + kWGs < n_local && row_valid(cur)) ? clamp_len(p, cur.b) : 0;
     }
   }
 
   // ---- teardown ------------------------------------------------------------
-  if (*abort_flag && warp == 8 && lane == 0) {
+  if (*abort_flag && (warp == kWarpProdQK || warp == kWarpProdV) && lane == 0) {
     // let copies already in flight land before the CTA's shared memory goes away
+    uint64_t *fulls = warp == kWarpProdQK ? bars->qk_full : bars->v_full;
     for (int n = issued - kStages; n < issued; ++n)
-      if (n >= 0) (void)wait_teardown(&bars->full[n % kStages], (n / kStages) & 1);
+      if (n >= 0) (void)wait_teardown(&fulls[n % kStages], (n / kStages) & 1);
   }
-  if (*abort_flag && warp == 9 && lane == 0 && last_commit != nullptr) {
+  if (*abort_flag && warp == kWarpMma && lane == 0 && last_commit != nullptr) {
     // tcgen05 ops complete in order: the last commit covers all of them
     (void)wait_teardown(last_commit, last_commit_parity);
   }
@@ -568,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -576,17 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             void *out, int num_sms, cudaStream_t stream) {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // setmaxnreg.inc only succeeds if the launch reserved the registers it hands
-  // out; refuse to launch a build whose register count would not cover them.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, attn_short_tc_kernel);
-  if (e != cudaSuccess) return e;
-  if (static_cast<long long>(fa.numRegs) * kThreads <
-      2LL * 128 * kRegsSoftmax + 128LL * kRegsControl)
-    return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(attn_short_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(attn_short_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = g.units < num_sms ? g.units : num_sms;
   if (grid <= 0) return cudaSuccess;
