@@ -281,17 +281,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_qk = warp == kWarpProdQK;
     const int pp = lane;
     const bool need_len = is_qk ? (g.rows_q || g.rows_k) : g.rows_k != 0;
-    // lane pp's pair length for the unit at `at` (unit n), read two units
-    // ahead of its use
-    auto len_at = [&](const UnitWalk &at, int n) -> int {
-      return (need_len && n < n_local && pp < g.P && at.hu * g.P + pp < p.H) ? clamp_len(p, at.b)
-                                                                           : 0;
+    // lane l holds the length of unit n0 + l (all pairs of a unit share a
+    // batch element); read 32 units at a time, well ahead of use
+    auto load_lens = [&](int n0) -> int {
+      const int nl = n0 + lane;
+      if (!need_len || nl >= n_local) return 0;
+      return clamp_len(p, (static_cast<int>(blockIdx.x) + nl * static_cast<int>(gridDim.x)) /
+                              g.units_per_b);
     };
+    int lens = load_lens(0);
     UnitWalk cur(blockIdx.x, gridDim.x, g.units_per_b);
-    UnitWalk ahead(blockIdx.x + gridDim.x, gridDim.x, g.units_per_b);
-    int len_n1 = len_at(ahead, 1);
-    ahead.next();
-    int len_n2 = len_at(ahead, 2);
     for (int n = 0; n < n_local; ++n, cur.next()) {
       const int s = n % kStages;
       const int b = cur.b, h0 = cur.hu * g.P;
@@ -302,16 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the first unit loads whole tiles: no wait for the lengths
       const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
       const bool has_pair = pp < g.P && h0 + pp < p.H;
-      const int len = n > 0 ? len_n1 : 0;
-      if (n > 0) {
-        ahead.next();
-        len_n1 = len_n2;
-        len_n2 = len_at(ahead, n + 2);
-      }
+      if (n > 0 && (n & 31) == 0) lens = load_lens(n);
+      const int len = n > 0 ? __shfl_sync(0xffffffffu, lens, n & 31) : 0;
+      // with unshared key/value heads the P pairs' first ceil8(len) key rows
+      // come in as one box, packed back to back (see the softmax)
+      const bool packed = rows_k && group == 1;
       uint32_t bytes = 0;
       if (is_qk && has_pair && rows_q) bytes += box_bytes(min(len, p.Lq));
-      if (has_pair && rows_k) bytes += box_bytes(len);
+      if (has_pair && rows_k && !packed) bytes += box_bytes(len);
       bytes = __reduce_add_sync(0xffffffffu, bytes);
+      if (packed) bytes += g.P * box_bytes(len);
       if (is_qk && !rows_q) bytes += g.P * g.Rq * 128;
       if (!rows_k) bytes += g.P * g.Rk * 128;
       uint64_t *full = is_qk ? &bars->qk_full[s] : &bars->v_full[s];
@@ -342,7 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!rows_k && group == 1 && lane == 0) tma_load_4d(dk, kv_full, full, 0, 0, h0, b);
       if (!rows_k && group != 1 && pp < g.P)
         tma_load_4d(dk + pp * g.Rk * 128, kv_one, full, 0, 0, hkv, b);
-      if (has_pair && rows_k) load_rows(dk + pp * g.Rk * 128, kv_rows, full, len, hkv, b);
+      if (packed && lane == 0) load_rows(dk, kv_rows, full, len, h0, b);
+      if (!packed && has_pair && rows_k)
+        load_rows(dk + pp * g.Rk * 128, kv_rows, full, len, hkv, b);
       __syncwarp();
       issued = n + 1;
     }
@@ -425,8 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
     const float sl = fabsf(p.scale_log2);
     const int rq_shift = __ffs(g.Rq) - 1;
-    const long long row_stride = p.layout == kLayoutBHSD ? 128 : 128LL * p.H;
-    const long long head_stride = p.layout == kLayoutBHSD ? 128LL * p.Lq : 128;
+    // byte strides of a query row and a head (below 2^31: this path takes
+    // Lq <= 128 and H <= 2^24)
+    const int row_stride = p.layout == kLayoutBHSD ? 128 : 128 * p.H;
+    const int head_stride = p.layout == kLayoutBHSD ? 128 * p.Lq : 128;
     const long long batch_stride = 128LL * p.Lq * p.H;
     const uint32_t so = smem_addr(staging + warp * kStagingBytes);
 
@@ -444,7 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
       const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
       if (!valid || qpad) jmax = 0;
-      const int col_lo = pr * g.Rk;
+      // key columns of this row's pair: packed units hold pair pr's keys at
+      // [pr * ceil8(len), ...); whole-tile units (a CTA's first) at pr * Rk
+      const bool packed = g.rows_k && group == 1 && n > 0;
+      const int col_lo = pr * (packed ? ((len + 7) & ~7) : g.Rk);
       // 32-column chunks any row of this warp can use
       const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
       const unsigned hi = __reduce_max_sync(0xffffffffu, jmax > 0 ? col_lo + jmax : 0);
@@ -532,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i_o = my_rot ? ((((row >> 5) + w) & 3) << 5) | (row & 31) : row & (g.Rq - 1);
           const uint4 val = ld_shared_v4(so + stage64_offset(rr, lane & 3));
           if (pr_o < g.P && h0 + pr_o < p.H && i_o < p.Lq)
-            st_global_v4(obase + (h0 + pr_o) * head_stride + i_o * row_stride + half * 64 +
-                             (lane & 3) * 16,
+            st_global_v4(obase + static_cast<long long>(h0 + pr_o) * head_stride +
+                             static_cast<long long>(i_o) * row_stride + half * 64 + (lane & 3) * 16,
                          val);
         }
         __syncwarp();

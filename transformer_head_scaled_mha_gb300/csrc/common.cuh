@@ -45,7 +45,7 @@ struct ShortMaps {
   CUtensorMap k_full, v_full;          // box (64, Rk, P, 1) (key/value heads not shared)
   CUtensorMap k_one, v_one;            // box (64, Rk, 1, 1) (shared key/value heads)
   CUtensorMap q_rows[kRowBoxes];       // box (64, 8 (h + 1), 1, 1), for padded tensors
-  CUtensorMap k_rows[kRowBoxes];
+  CUtensorMap k_rows[kRowBoxes];       // box (64, 8 (h + 1), P, 1) (1 head if shared)
   CUtensorMap v_rows[kRowBoxes];
   CUtensorMap q_blk32;                 // box (64, 32, 1, 1): causal row-block order
 };

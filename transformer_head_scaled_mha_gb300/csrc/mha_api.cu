@@ -111,7 +111,8 @@ int select_path(int B, int H, int Lq, int Lk, int dk, int dv, int mask, int dtyp
   if (static_cast<long long>(B) * H * Lq == 0) return kPathNone;
   if (Lk == 0) return kPathZero;
   if (dtype == MHA_DTYPE_F32) return kPathF32;
-  if (dk == 64 && Lq <= 128 && Lk <= 128) return kPathShort;
+  // the packed kernel's 32-bit row strides need H <= 2^24
+  if (dk == 64 && Lq <= 128 && Lk <= 128 && H <= (1 << 24)) return kPathShort;
   return kPathLong;
 }
 
@@ -203,9 +204,12 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
         ok = make_map(&m.q_blk32, q, 64, Lq, H, B, layout, 32, 1);
       for (int h = 0; ok && g.rows_q && h < g.Rq / 8; ++h)
         ok = make_map(&m.q_rows[h], q, 64, Lq, H, B, layout, 8 * (h + 1), 1);
+      // key/value row boxes: all P pairs of a unit at once when the heads
+      // are not shared (the kernel packs their rows back to back)
+      const int kv_box_heads = shared_kv ? 1 : g.P;
       for (int h = 0; ok && g.rows_k && h < g.Rk / 8; ++h)
-        ok = make_map(&m.k_rows[h], k, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1) &&
-             make_map(&m.v_rows[h], v, 64, Lk, H_kv, B, layout, 8 * (h + 1), 1);
+        ok = make_map(&m.k_rows[h], k, 64, Lk, H_kv, B, layout, 8 * (h + 1), kv_box_heads) &&
+             make_map(&m.v_rows[h], v, 64, Lk, H_kv, B, layout, 8 * (h + 1), kv_box_heads);
       if (!ok) return MHA_ERR_CUDA;
       err = launch_short_tc(m, g, p, out, sms, stream);
     } else {
