@@ -12,6 +12,13 @@ compiles it with gcc and marshals numpy arrays.
 Every function here is pinned by ``tests/test_oracle.py`` against values the
 pages print (the three-token worked example), closed forms, invariants and a
 50-digit brute force.
+
+``linear`` and ``mha_sublayer`` add the steps on either side of the attention:
+the learned projections with their biases, the head split and concatenation,
+and the output projection (trishampatil.com, "Multi-Head Attention" and "The
+Output Projection W^O"; aicassindra.com, "A faithful layer in code").  The
+matrix products there are numpy float64 matmuls (a library primitive used as
+one step); the attention step is the C oracle above.
 """
 from __future__ import annotations
 
@@ -138,3 +145,59 @@ def mha_fwd(q, k, v, *, mask_kind: int = 0, key_lengths=None, scale: float,
     if return_scores:
         res.append(s)
     return res[0] if len(res) == 1 else tuple(res)
+
+
+def _f64(a):
+    """Stored values (float64, float32, or uint16 bfloat16 bits) widened exactly."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def linear(x, w, b=None):
+    """y = x W + b in float64.
+
+    x [..., d_in], W [d_in, d_out], b [d_out] (or None): the learned projection
+    of a token vector, written input-major as in "Q · W_i^Q" with
+    W_i^Q of shape d_model x d_k; the bias is the one every linear layer of the
+    faithful layer carries.  Inputs may be float64, float32 or bfloat16 bits.
+    """
+    y = _f64(x) @ _f64(w)
+    if b is not None:
+        y = y + _f64(b)
+    return y
+
+
+def mha_sublayer(x, mem, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=None, *,
+                 H: int, H_kv: int = None, mask_kind: int = 0, key_lengths=None, scale=None):
+    """Multi-head attention sublayer in float64.
+
+    x [B, T, d_model] (queries), mem [B, S, d_model] (keys and values; pass x
+    for self-attention); W_q [d_model, H d_k], W_k and W_v [d_model, H_kv d_k],
+    W_o [H d_v, d_model]; biases of the output widths (or None).
+      1. q = x W_q + b_q, k = mem W_k + b_k, v = mem W_v + b_v
+      2. head i of q is columns [i d_k, (i + 1) d_k) (same for k, v), i.e. the
+         projections viewed as [B, L, heads, d]
+      3. head_i = Attention(q_i, k_g, v_g), g = i / (H / H_kv)  (the C oracle)
+      4. concatenate the heads back to [B, T, H d_v] and project:
+         out = concat W_o + b_o
+    ``scale`` defaults to 1/sqrt(d_k).  Returns float64 [B, T, d_out].
+    """
+    H_kv = H if H_kv is None else H_kv
+    q = linear(x, w_q, b_q)
+    k = linear(mem, w_k, b_k)
+    v = linear(mem, w_v, b_v)
+    B, T, hq = q.shape
+    S = k.shape[1]
+    if hq % H or k.shape[2] % H_kv or v.shape[2] % H_kv:
+        raise ValueError("projection widths must split into heads")
+    dk, dv = hq // H, v.shape[2] // H_kv
+    if k.shape[2] // H_kv != dk:
+        raise ValueError("query and key head widths differ")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    heads = mha_fwd(q.reshape(B, T, H, dk), k.reshape(B, S, H_kv, dk),
+                    v.reshape(B, S, H_kv, dv), mask_kind=mask_kind, key_lengths=key_lengths,
+                    scale=scale, layout="bshd")
+    return linear(heads.reshape(B, T, H * dv), w_o, b_o)

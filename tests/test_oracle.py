@@ -365,3 +365,128 @@ def test_grouped_heads_reject_non_divisor(oracle_lib):
     k = np.zeros((1, 3, 3, 2))
     with pytest.raises(ValueError):
         oracle.mha_fwd(q, k, k, scale=1.0)
+
+
+# --------------------------------------------------------------------------
+# the sublayer around the attention: projections with biases, head split,
+# concatenation and the output projection
+# --------------------------------------------------------------------------
+def _sub_inputs(B, T, S, d, H, H_kv, seed=3):
+    rng = np.random.default_rng(seed)
+    dk = d // H
+    x = rng.normal(size=(B, T, d))
+    mem = rng.normal(size=(B, S, d))
+    w_q = rng.normal(size=(d, H * dk)) / math.sqrt(d)
+    w_k = rng.normal(size=(d, H_kv * dk)) / math.sqrt(d)
+    w_v = rng.normal(size=(d, H_kv * dk)) / math.sqrt(d)
+    w_o = rng.normal(size=(H * dk, d)) / math.sqrt(d)
+    b = [rng.normal(size=n) * 0.1 for n in (H * dk, H_kv * dk, H_kv * dk, d)]
+    return x, mem, w_q, w_k, w_v, w_o, b
+
+
+def test_linear_brute_force():
+    rng = np.random.default_rng(0)
+    x, w, b = rng.normal(size=(2, 3, 4)), rng.normal(size=(4, 5)), rng.normal(size=5)
+    y = oracle.linear(x, w, b)
+    for i in range(2):
+        for t in range(3):
+            for o in range(5):
+                acc = b[o]
+                for c in range(4):
+                    acc += x[i, t, c] * w[c, o]
+                assert abs(y[i, t, o] - acc) < 1e-12
+
+
+def test_linear_identity_adds_bias():
+    x = np.random.default_rng(1).normal(size=(3, 6))
+    b = np.arange(6.0)
+    np.testing.assert_array_equal(oracle.linear(x, np.eye(6), b), x + b)
+    np.testing.assert_array_equal(oracle.linear(x, np.eye(6)), x)
+
+
+def test_linear_reads_bf16_bits_exactly():
+    vals = np.array([[1.0, -2.5], [0.15625, 3.0]])
+    bits = gen.f64_to_bf16_bits(vals)
+    np.testing.assert_array_equal(oracle.linear(bits, gen.f64_to_bf16_bits(np.eye(2))),
+                                  gen.bf16_bits_to_f64(bits))
+
+
+@pytest.mark.parametrize("mask", [0, MASK_KEY_PADDING, MASK_CAUSAL])
+def test_sublayer_zero_query_key_projections_average_values(oracle_lib, mask):
+    # W_q = W_k = 0 and no q/k bias: every score is 0, each head averages the
+    # value rows it may see, and the output is that average projected by W_o
+    B, T, d, H = 2, 5, 8, 2
+    S = T if mask & MASK_CAUSAL else 7
+    x, mem, w_q, w_k, w_v, w_o, b = _sub_inputs(B, T, S, d, H, H)
+    if mask & MASK_CAUSAL:
+        mem = x
+    lens = np.array([3, S], dtype=np.int32) if mask & MASK_KEY_PADDING else None
+    out = oracle.mha_sublayer(x, mem, 0 * w_q, 0 * w_k, w_v, w_o, None, None, b[2], b[3], H=H,
+                              mask_kind=mask, key_lengths=lens)
+    v = mem @ w_v + b[2]
+    for bi in range(B):
+        for t in range(T):
+            n = S
+            if mask & MASK_KEY_PADDING:
+                n = lens[bi]
+            if mask & MASK_CAUSAL:
+                n = t + 1
+            mean = v[bi, :n].mean(axis=0)
+            np.testing.assert_allclose(out[bi, t], mean @ w_o + b[3], rtol=0, atol=1e-12)
+
+
+def test_sublayer_head_split_and_concat_order(oracle_lib):
+    # with W_o = I and no output bias, output columns [i d_k, (i+1) d_k) are
+    # head i: attention over the projections' columns [i d_k, (i+1) d_k)
+    B, T, S, d, H = 2, 4, 6, 12, 3
+    dk = d // H
+    x, mem, w_q, w_k, w_v, _, b = _sub_inputs(B, T, S, d, H, H)
+    out = oracle.mha_sublayer(x, mem, w_q, w_k, w_v, np.eye(d), b[0], b[1], b[2], None, H=H)
+    for i in range(H):
+        cols = slice(i * dk, (i + 1) * dk)
+        q = (x @ w_q[:, cols] + b[0][cols])[:, None]
+        k = (mem @ w_k[:, cols] + b[1][cols])[:, None]
+        v = (mem @ w_v[:, cols] + b[2][cols])[:, None]
+        head = oracle.mha_fwd(q, k, v, scale=1 / math.sqrt(dk))[:, 0]
+        np.testing.assert_allclose(out[:, :, cols], head, rtol=0, atol=1e-12)
+
+
+def test_sublayer_brute_force_tiny():
+    # the whole sublayer from the definition with plain Python loops
+    B, T, S, d, H = 1, 3, 4, 4, 2
+    dk = d // H
+    x, mem, w_q, w_k, w_v, w_o, b = _sub_inputs(B, T, S, d, H, H, seed=9)
+    lens = np.array([3], dtype=np.int32)
+    out = oracle.mha_sublayer(x, mem, w_q, w_k, w_v, w_o, *b, H=H, mask_kind=MASK_KEY_PADDING,
+                              key_lengths=lens)
+
+    def proj(rows, w, bias):
+        return [[bias[o] + sum(r[c] * w[c][o] for c in range(len(r))) for o in range(len(bias))]
+                for r in rows]
+    q = proj(x[0].tolist(), w_q.tolist(), b[0].tolist())
+    k = proj(mem[0].tolist(), w_k.tolist(), b[1].tolist())
+    v = proj(mem[0].tolist(), w_v.tolist(), b[2].tolist())
+    for t in range(T):
+        concat = []
+        for h in range(H):
+            cs = range(h * dk, (h + 1) * dk)
+            sc = [sum(q[t][c] * k[j][c] for c in cs) / math.sqrt(dk) for j in range(3)]
+            e = [math.exp(z) for z in sc]
+            wts = [z / sum(e) for z in e]
+            concat += [sum(wts[j] * v[j][c] for j in range(3)) for c in cs]
+        want = [b[3][o] + sum(concat[c] * w_o[c][o] for c in range(d)) for o in range(d)]
+        np.testing.assert_allclose(out[0, t], want, rtol=0, atol=1e-12)
+
+
+def test_sublayer_grouped_heads_equal_repeated_projections(oracle_lib):
+    # sharing key/value heads equals giving every query head its own copy of
+    # its group's key/value projection columns
+    B, T, S, d, H, H_kv = 2, 5, 6, 16, 4, 2
+    dk = d // H
+    x, mem, w_q, w_k, w_v, w_o, b = _sub_inputs(B, T, S, d, H, H_kv)
+    out = oracle.mha_sublayer(x, mem, w_q, w_k, w_v, w_o, *b, H=H, H_kv=H_kv)
+    rep = lambda w: np.concatenate([w[..., (h // 2) * dk:(h // 2 + 1) * dk] for h in range(H)],
+                                   axis=-1)
+    out2 = oracle.mha_sublayer(x, mem, w_q, rep(w_k), rep(w_v), w_o, b[0], rep(b[1]), rep(b[2]),
+                               b[3], H=H)
+    np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
