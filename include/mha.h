@@ -29,6 +29,7 @@
 #ifndef MHA_GB300_H
 #define MHA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -142,6 +143,68 @@ int mha_fwd_ex(const void *q, const void *k, const void *v, void *out,
                int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
                int mask_kind, const int32_t *key_lengths,
                float scale, int dtype, void *stream);
+
+/*
+ * mha_linear_fwd -- y = x W + b, asynchronous on `stream`.
+ *
+ * The learned projection of token vectors that surrounds the attention
+ * (trishampatil.com, "Multi-Head Attention": Q · W_i^Q with W_i^Q of shape
+ * d_model x d_k; aicassindra.com, "A faithful layer in code": every linear
+ * layer carries a bias).  Tensor-core products, fp32 accumulation, bf16 out.
+ *
+ * x    [M, K]  device pointer, row-major bf16, 16-byte aligned
+ * w    [K, N]  device pointer, row-major bf16 (input-major), 16-byte aligned
+ * b    [N]     device pointer, bf16, or NULL for no bias
+ * y    [M, N]  device pointer, row-major bf16, 16-byte aligned; written in full;
+ *              must not overlap x, w or b
+ * M >= 0 (0 is a no-op); K, N > 0 and multiples of 8 (16-byte rows), else
+ * MHA_ERR_UNSUPPORTED; dtype must be MHA_DTYPE_BF16 (F32: MHA_ERR_UNSUPPORTED).
+ * Ownership and errors as for mha_fwd.
+ */
+int mha_linear_fwd(const void *x, const void *w, const void *b, void *y,
+                   int M, int K, int N, int dtype, void *stream);
+
+/* Bytes of device workspace mha_sublayer_fwd needs for these shapes (the
+   projected q, k, v and the concatenated heads, bf16, each 256-byte aligned);
+   0 for negative arguments. */
+size_t mha_sublayer_workspace_size(int B, int T, int S, int d_model, int H, int H_kv,
+                                   int d_k, int d_v);
+
+/*
+ * mha_sublayer_fwd -- the multi-head attention sublayer, asynchronous on
+ * `stream`:
+ *
+ *     q = x W_q + b_q,  k = mem W_k + b_k,  v = mem W_v + b_v
+ *     head_i = Attention(q_i, k_g, v_g),  g = i / (H / H_kv)
+ *     out = Concat(head_1, ..., head_H) W_o + b_o
+ *
+ * (trishampatil.com, "Multi-Head Attention" and "The Output Projection W^O";
+ * aicassindra.com, "A faithful layer in code").  Head i of a projection is its
+ * columns [i d, (i + 1) d), so q, k, v are the [B, L, heads, d] layout of
+ * mha_fwd_ex and the attention output is already the concatenation.
+ *
+ * x      [B, T, d_model] queries' token vectors
+ * mem    [B, S, d_model] keys' and values' token vectors (encoder memory for
+ *        cross-attention), or NULL for self-attention (then S must equal T)
+ * out    [B, T, d_model]
+ * w_q    [d_model, H d_k],   w_k [d_model, H_kv d_k],   w_v [d_model, H_kv d_v],
+ * w_o    [H d_v, d_model];   b_* their output widths, each may be NULL
+ * mask_kind, key_lengths, scale: as for mha_fwd (masks apply to the
+ *        attention step; key_lengths [B] on the device)
+ * workspace  device memory of at least mha_sublayer_workspace_size(...) bytes,
+ *        256-byte aligned, owned by the caller, not overlapping any argument;
+ *        the call uses it until the enqueued work has run
+ * All matrices bf16 (dtype MHA_DTYPE_BF16), 16-byte aligned; d_model, H d_k,
+ * H_kv d_k, H_kv d_v, H d_v multiples of 8; d_k = d_v in {64, 128} (the
+ * attention step's rule).  Validation covers every step before anything is
+ * enqueued.  Ownership and errors as for mha_fwd.
+ */
+int mha_sublayer_fwd(const void *x, const void *mem, void *out,
+                     const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                     const void *b_q, const void *b_k, const void *b_v, const void *b_o,
+                     int B, int T, int S, int d_model, int H, int H_kv, int d_k, int d_v,
+                     int mask_kind, const int32_t *key_lengths, float scale, int dtype,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed

@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["mha_fwd", "mha_fwd_ex", "mha_fwd_path", "mha_status_string", "mha_debug_status",
+        ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
+         "mha_sublayer_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status",
          "mha_version"])
 
 
@@ -134,3 +135,53 @@ def test_binding_refuses_cpu_tensors(mha):
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mha.mha_fwd(q, q, q)
+
+
+def test_linear_rejects_before_launch(mha):
+    E_ARG, E_UNS = mha.MHA_ERR_INVALID_ARGUMENT, mha.MHA_ERR_UNSUPPORTED
+    L = mha.lib.mha_linear_fwd
+    x, w, y = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+    assert L(x, w, None, y, -1, 512, 512, 1, None) == E_ARG
+    assert L(x, w, None, y, 64, 0, 512, 1, None) == E_ARG
+    assert L(x, w, None, y, 64, 512, 512, 0, None) == E_UNS  # fp32
+    assert L(x, w, None, y, 64, 500, 512, 1, None) == E_UNS  # K not a multiple of 8
+    assert L(x, w, None, y, 64, 512, 100, 1, None) == E_UNS
+    assert L(x + 8, w, None, y, 64, 512, 512, 1, None) == E_ARG  # alignment
+    assert L(x, w, FAKE + (3 << 24) + 1, y, 64, 512, 512, 1, None) == E_ARG
+    assert L(x, w, None, x + 4096, 64, 512, 512, 1, None) == E_ARG  # y overlaps x
+    assert L(x, w, None, y, 0, 512, 512, 1, None) == mha.MHA_OK  # empty: nothing to do
+
+
+def test_sublayer_workspace_size(mha):
+    n = mha.mha_sublayer_workspace_size(2, 64, 64, 512, 8, 8, 64, 64)
+    assert n == 4 * 2 * 64 * 512 * 2
+    assert mha.mha_sublayer_workspace_size(2, 64, 96, 512, 8, 2, 64, 64) == \
+        2 * 64 * 512 * 2 * 2 + 2 * 2 * 96 * 128 * 2
+    assert mha.mha_sublayer_workspace_size(-1, 64, 64, 512, 8, 8, 64, 64) == 0
+
+
+def test_sublayer_rejects_before_launch(mha):
+    E_ARG, E_UNS = mha.MHA_ERR_INVALID_ARGUMENT, mha.MHA_ERR_UNSUPPORTED
+    S_ = mha.lib.mha_sublayer_fwd
+    ws_n = mha.mha_sublayer_workspace_size(2, 64, 64, 512, 8, 8, 64, 64)
+    p = [FAKE + (i << 24) for i in range(12)]
+    x, mem, out, wq, wk, wv, wo, ws = p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]
+
+    def call(B=2, T=64, S=64, d=512, H=8, Hkv=8, dk=64, dv=64, mask=0, kl=None, scale=0.125,
+             dtype=1, mem_=mem, work=ws, work_n=ws_n):
+        return S_(x, mem_, out, wq, wk, wv, wo, None, None, None, None, B, T, S, d, H, Hkv, dk,
+                  dv, mask, kl, scale, dtype, work, work_n, None)
+    assert call(mem_=None, S=32) == E_ARG  # self-attention needs S == T
+    assert call(H=8, Hkv=3) == E_ARG
+    assert call(dtype=0) == E_UNS
+    assert call(dk=96, dv=96) == E_UNS
+    assert call(d=500) == E_UNS
+    assert call(mask=2) == E_ARG  # key lengths missing
+    assert call(mask=1, S=32) == E_ARG  # causal needs T == S
+    assert call(work=None) == E_ARG
+    assert call(work_n=ws_n - 1) == E_ARG
+    assert call(work=ws + 64) == E_ARG  # workspace alignment
+    assert call(work=out) == E_ARG  # workspace overlaps out
+    assert call(scale=math.nan) == E_ARG
+    assert call(mask=2, kl=ws + 512) == E_ARG  # lengths inside the workspace
+    assert call(B=0) == mha.MHA_OK

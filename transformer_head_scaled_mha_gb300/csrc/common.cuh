@@ -67,4 +67,13 @@ cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
 
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
 
+// y = x W + b (bf16): x viewed as (K, M), W as (N, K), 128-byte swizzle;
+// boxes (64, 128) and (64, 64)
+struct LinearMaps {
+  CUtensorMap x;
+  CUtensorMap w;
+};
+cudaError_t launch_linear_tc(const LinearMaps &maps, const void *bias, void *y, int M, int N,
+                             int K, int *status, int num_sms, cudaStream_t stream);
+
 }  // namespace mha

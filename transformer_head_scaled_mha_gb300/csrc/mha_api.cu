@@ -88,6 +88,21 @@ bool make_map(CUtensorMap *map, const void *base, int d, int L, int heads, int B
   return r == CUDA_SUCCESS;
 }
 
+// 2-D view (cols, rows) of a row-major bf16 matrix, 128-byte swizzle
+bool make_map_2d(CUtensorMap *map, const void *base, int cols, int rows, int box_cols,
+                 int box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -231,6 +246,139 @@ extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, i
                        const int32_t *key_lengths, float scale, int dtype, void *stream) {
   return mha_fwd_ex(q, k, v, out, B, H, H, Lq, Lk, d_k, d_v, kLayoutBHSD, mask_kind, key_lengths,
                     scale, dtype, stream);
+}
+
+namespace {
+
+// Validation shared by mha_linear_fwd and the sublayer's projections.
+int check_linear(const void *x, const void *w, const void *b, const void *y, long long M, int K,
+                 int N, int dtype) {
+  if (M < 0 || K <= 0 || N <= 0) return MHA_ERR_INVALID_ARGUMENT;
+  if (dtype != MHA_DTYPE_F32 && dtype != MHA_DTYPE_BF16) return MHA_ERR_INVALID_ARGUMENT;
+  if (dtype != MHA_DTYPE_BF16) return MHA_ERR_UNSUPPORTED;
+  // the copy engine needs 16-byte row strides
+  if (K % 8 != 0 || N % 8 != 0) return MHA_ERR_UNSUPPORTED;
+  if (M > 0x7fffffffLL) return MHA_ERR_UNSUPPORTED;
+  if (M == 0) return MHA_OK;
+  if (x == nullptr || w == nullptr || y == nullptr) return MHA_ERR_INVALID_ARGUMENT;
+  for (const void *ptr : {x, w, y})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return MHA_ERR_INVALID_ARGUMENT;
+  if (b != nullptr && reinterpret_cast<uintptr_t>(b) % 2 != 0) return MHA_ERR_INVALID_ARGUMENT;
+  const size_t ny = static_cast<size_t>(M) * N * 2;
+  if (overlaps(y, ny, x, static_cast<size_t>(M) * K * 2) ||
+      overlaps(y, ny, w, static_cast<size_t>(K) * N * 2) || overlaps(y, ny, b, N * 2))
+    return MHA_ERR_INVALID_ARGUMENT;
+  return MHA_OK;
+}
+
+// Launch of a validated linear layer (M > 0).
+int run_linear(const void *x, const void *w, const void *b, void *y, int M, int K, int N,
+               cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+  const int sms = sm_count(dev);
+  int *status = status_ptr(dev);
+  if (sms <= 0 || status == nullptr) return MHA_ERR_CUDA;
+  LinearMaps m;
+  std::memset(&m, 0, sizeof m);
+  if (!make_map_2d(&m.x, x, K, M, 64, 128) || !make_map_2d(&m.w, w, N, K, 64, 64))
+    return MHA_ERR_CUDA;
+  return launch_linear_tc(m, b, y, M, N, K, status, sms, stream) == cudaSuccess ? MHA_OK
+                                                                              : MHA_ERR_CUDA;
+}
+
+constexpr size_t kWsAlign = 256;
+size_t ws_round(size_t n) { return (n + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+// Byte offsets of q, k, v and the concatenated heads in a sublayer workspace.
+struct SublayerWs {
+  size_t q, k, v, heads, total;
+};
+SublayerWs sublayer_ws(long long B, long long T, long long S, long long H, long long H_kv,
+                       long long d_k, long long d_v) {
+  SublayerWs w;
+  w.q = 0;
+  w.k = w.q + ws_round(static_cast<size_t>(B * T * H * d_k * 2));
+  w.v = w.k + ws_round(static_cast<size_t>(B * S * H_kv * d_k * 2));
+  w.heads = w.v + ws_round(static_cast<size_t>(B * S * H_kv * d_v * 2));
+  w.total = w.heads + ws_round(static_cast<size_t>(B * T * H * d_v * 2));
+  return w;
+}
+
+}  // namespace
+
+extern "C" int mha_linear_fwd(const void *x, const void *w, const void *b, void *y, int M, int K,
+                              int N, int dtype, void *stream) {
+  const int st = check_linear(x, w, b, y, M, K, N, dtype);
+  if (st != MHA_OK || M == 0) return st;
+  return run_linear(x, w, b, y, M, K, N, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t mha_sublayer_workspace_size(int B, int T, int S, int d_model, int H, int H_kv,
+                                              int d_k, int d_v) {
+  (void)d_model;
+  if (B < 0 || T < 0 || S < 0 || H < 0 || H_kv < 0 || d_k < 0 || d_v < 0) return 0;
+  return sublayer_ws(B, T, S, H, H_kv, d_k, d_v).total;
+}
+
+extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const void *w_q,
+                                const void *w_k, const void *w_v, const void *w_o,
+                                const void *b_q, const void *b_k, const void *b_v,
+                                const void *b_o, int B, int T, int S, int d_model, int H,
+                                int H_kv, int d_k, int d_v, int mask_kind,
+                                const int32_t *key_lengths, float scale, int dtype,
+                                void *workspace, size_t workspace_bytes, void *stream_) {
+  if (mem == nullptr) {  // self-attention: keys and values come from x
+    mem = x;
+    if (S != T) return MHA_ERR_INVALID_ARGUMENT;
+  }
+  if (B < 0 || T < 0 || S < 0 || d_model <= 0 || H <= 0 || H_kv <= 0 || d_k <= 0 || d_v <= 0)
+    return MHA_ERR_INVALID_ARGUMENT;
+  if (H % H_kv != 0) return MHA_ERR_INVALID_ARGUMENT;
+  const long long Mq = static_cast<long long>(B) * T, Mk = static_cast<long long>(B) * S;
+  // every step's shape rules, before anything is enqueued
+  int st;
+  const SublayerWs ws = sublayer_ws(B, T, S, H, H_kv, d_k, d_v);
+  uint8_t *wsb = static_cast<uint8_t *>(workspace);
+  void *q = wsb + ws.q, *k = wsb + ws.k, *v = wsb + ws.v, *heads = wsb + ws.heads;
+  if ((st = check_linear(x, w_q, b_q, out, Mq, d_model, H * d_k, dtype)) != MHA_OK ||
+      (st = check_linear(mem, w_k, b_k, out, Mk, d_model, H_kv * d_k, dtype)) != MHA_OK ||
+      (st = check_linear(mem, w_v, b_v, out, Mk, d_model, H_kv * d_v, dtype)) != MHA_OK ||
+      (st = check_linear(heads, w_o, b_o, out, Mq, H * d_v, d_model, dtype)) != MHA_OK)
+    return st;
+  const int path = select_path(B, H, T, S, d_k, d_v, mask_kind, dtype);
+  if (path < 0) return -path;
+  if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
+  if (Mq == 0) return MHA_OK;
+  const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
+  if (padded && key_lengths == nullptr) return MHA_ERR_INVALID_ARGUMENT;
+  if (workspace == nullptr || workspace_bytes < ws.total ||
+      reinterpret_cast<uintptr_t>(workspace) % kWsAlign != 0)
+    return MHA_ERR_INVALID_ARGUMENT;
+  const size_t n_out = static_cast<size_t>(Mq) * d_model * 2;
+  if (overlaps(workspace, ws.total, out, n_out) ||
+      overlaps(workspace, ws.total, x, static_cast<size_t>(Mq) * d_model * 2) ||
+      overlaps(workspace, ws.total, mem, static_cast<size_t>(Mk) * d_model * 2) ||
+      (padded && (overlaps(workspace, ws.total, key_lengths, sizeof(int32_t) * B) ||
+                  overlaps(out, n_out, key_lengths, sizeof(int32_t) * B))))
+    return MHA_ERR_INVALID_ARGUMENT;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // 1. projections (head i of each is columns [i d, (i + 1) d): [B, L, heads, d])
+  if ((st = run_linear(x, w_q, b_q, q, static_cast<int>(Mq), d_model, H * d_k, stream)) != MHA_OK)
+    return st;
+  if (Mk > 0) {
+    if ((st = run_linear(mem, w_k, b_k, k, static_cast<int>(Mk), d_model, H_kv * d_k, stream)) !=
+            MHA_OK ||
+        (st = run_linear(mem, w_v, b_v, v, static_cast<int>(Mk), d_model, H_kv * d_v, stream)) !=
+            MHA_OK)
+      return st;
+  }
+  // 2. attention per head, in the [B, L, heads, d] layout
+  if ((st = mha_fwd_ex(q, k, v, heads, B, H, H_kv, T, S, d_k, d_v, kLayoutBSHD, mask_kind,
+                       key_lengths, scale, dtype, stream)) != MHA_OK)
+    return st;
+  // 3. concatenated heads [B, T, H d_v] times W_o
+  return run_linear(heads, w_o, b_o, out, static_cast<int>(Mq), H * d_v, d_model, stream);
 }
 
 extern "C" const char *mha_status_string(int status) {

@@ -18,7 +18,8 @@ PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fi
 
 MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 
-EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
+EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
+            "mha_sublayer_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
 
 
 class MhaError(RuntimeError):
@@ -40,6 +41,13 @@ def _load() -> ctypes.CDLL:
     lib.mha_fwd_ex.restype = i32
     lib.mha_fwd_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp,
                                ctypes.c_float, i32, vp]
+    lib.mha_linear_fwd.restype = i32
+    lib.mha_linear_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.mha_sublayer_workspace_size.restype = ctypes.c_size_t
+    lib.mha_sublayer_workspace_size.argtypes = [i32] * 8
+    lib.mha_sublayer_fwd.restype = i32
+    lib.mha_sublayer_fwd.argtypes = [vp] * 11 + [i32] * 9 + [vp, ctypes.c_float, i32, vp,
+                                                            ctypes.c_size_t, vp]
     lib.mha_fwd_path.restype = i32
     lib.mha_fwd_path.argtypes = [i32] * 8
     lib.mha_status_string.restype = ctypes.c_char_p
@@ -164,4 +172,91 @@ def mha_fwd_ex(q, k, v, out=None, *, layout: str = "bhsd", mask_kind: int = 0,
                             _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st, "mha_fwd_ex")
+    return out
+
+
+def _bf16_cuda(name, t, ndim=None):
+    import torch
+    if t is None:
+        return None
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous bfloat16 CUDA tensor" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions" % (name, ndim))
+    return t
+
+
+def mha_linear_fwd(x, w, b=None, out=None, *, stream=None):
+    """y = x W + b: x [..., K], W [K, N] (input-major), b [N] or None; bfloat16."""
+    import torch
+    _bf16_cuda("x", x)
+    _bf16_cuda("w", w, 2)
+    _bf16_cuda("b", b, 1)
+    K, N = w.shape
+    if x.shape[-1] != K or (b is not None and b.shape[0] != N):
+        raise ValueError("shape mismatch: x %s w %s" % (tuple(x.shape), tuple(w.shape)))
+    M = x.numel() // K if K else 0
+    if out is None:
+        out = torch.empty(tuple(x.shape[:-1]) + (N,), dtype=x.dtype, device=x.device)
+    else:
+        _bf16_cuda("out", out)
+        if tuple(out.shape) != tuple(x.shape[:-1]) + (N,):
+            raise ValueError("out must have shape %s" % ((tuple(x.shape[:-1]) + (N,)),))
+    with torch.cuda.device(x.device):
+        st = lib.mha_linear_fwd(x.data_ptr(), w.data_ptr(), b.data_ptr() if b is not None else None,
+                                out.data_ptr(), M, K, N, MHA_DTYPE_BF16, _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_linear_fwd")
+    return out
+
+
+def mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v) -> int:
+    return int(lib.mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v))
+
+
+def mha_sublayer_fwd(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=None, *, mem=None,
+                     H, H_kv=None, mask_kind: int = 0, key_lengths=None, scale=None,
+                     workspace=None, out=None, stream=None):
+    """Multi-head attention sublayer (projections, attention, output projection).
+
+    x [B, T, d_model]; mem [B, S, d_model] or None (self-attention); weights
+    input-major: W_q [d_model, H d_k], W_k/W_v [d_model, H_kv d], W_o [H d_v,
+    d_model]; biases optional.  ``workspace``: a uint8 CUDA tensor of at least
+    mha_sublayer_workspace_size(...) bytes (allocated here when None).
+    """
+    import torch
+    H_kv = H if H_kv is None else H_kv
+    _bf16_cuda("x", x, 3)
+    _bf16_cuda("mem", mem, 3)
+    for name, t in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v), ("w_o", w_o)):
+        _bf16_cuda(name, t, 2)
+    for name, t in (("b_q", b_q), ("b_k", b_k), ("b_v", b_v), ("b_o", b_o)):
+        _bf16_cuda(name, t, 1)
+    B, T, d_model = x.shape
+    S = mem.shape[1] if mem is not None else T
+    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H_kv
+    if out is None:
+        out = torch.empty((B, T, w_o.shape[1]), dtype=x.dtype, device=x.device)
+    need = mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    kl_ptr = None
+    if key_lengths is not None:
+        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
+            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
+        kl_ptr = key_lengths.data_ptr()
+    if scale is None:
+        scale = float(d_k) ** -0.5
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    # an empty memory (S = 0) is never read; pass a non-null stand-in so it is
+    # not taken for self-attention
+    mem_ptr = None if mem is None else (mem.data_ptr() if mem.numel() else x.data_ptr())
+    with torch.cuda.device(x.device):
+        st = lib.mha_sublayer_fwd(ptr(x), mem_ptr, ptr(out), ptr(w_q), ptr(w_k), ptr(w_v),
+                                  ptr(w_o), ptr(b_q), ptr(b_k), ptr(b_v), ptr(b_o), B, T, S,
+                                  d_model, H, H_kv, d_k, d_v, int(mask_kind), kl_ptr,
+                                  float(scale), MHA_DTYPE_BF16, workspace.data_ptr(),
+                                  workspace.numel(), _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_sublayer_fwd")
     return out
