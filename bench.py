@@ -6,7 +6,9 @@ softmax, P V, normalise + store) over one batch of the workload.  Default
 workload: Transformer-base encoder self-attention, bf16, B=256, H=8, L=64,
 d=64, key + query padding with lengths uniform in [8, 64] (HBM-bound; metric
 GB/s).  ``--workload`` picks another (see gen.WORKLOADS); the long causal one
-reports TFLOP/s.
+reports TFLOP/s.  The ``sublayer_*`` workloads (gen.SUBLAYERS) time the whole
+multi-head sublayer per step (projections with biases, attention, output
+projection; TFLOP/s), with the projection kernel as the roofline kernel.
 
 value  device throughput, inputs resident in HBM; K launches captured in one
        CUDA graph and replayed between CUDA events; consecutive launches read
@@ -451,6 +453,249 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# multi-head sublayer workloads (projections + attention + output projection)
+# ---------------------------------------------------------------------------
+def sublayer_flops(spec, lens):
+    """Projection flops (2 M K N each, with the realised shapes) plus the
+    attention step's algorithmic flops."""
+    B, T, S, d = spec["B"], spec["T"], spec["S"], spec["d_model"]
+    H, Hkv, dk, dv = spec["H"], spec["H_kv"], spec["dk"], spec["dv"]
+    proj = 2 * B * (T * d * H * dk + S * d * Hkv * dk + S * d * Hkv * dv + T * H * dv * d)
+    _, att = algorithmic(gen.sublayer_attention_spec(spec), lens)
+    return int(proj), int(att)
+
+
+def sublayer_oracle_time(spec, inp, frac_b):
+    """Oracle seconds for the first ceil(frac_b * B) batch elements."""
+    import oracle
+    nb = max(1, int(math.ceil(spec["B"] * frac_b)))
+    sl = slice(0, nb)
+    x = inp["x"][sl]
+    mem = inp["mem"][sl] if inp["mem"] is not None else x
+    lens = inp["lens"][sl] if inp["lens"] is not None else None
+    t0 = time.perf_counter()
+    oracle.mha_sublayer(x, mem, *inp["w"], *inp["b"], H=spec["H"], H_kv=spec["H_kv"],
+                        mask_kind=spec["mask"], key_lengths=lens,
+                        scale=gen.default_scale(spec["dk"]))
+    return time.perf_counter() - t0, nb / spec["B"]
+
+
+def sublayer_oracle_baseline(spec, inp, flops, budget_s):
+    import oracle
+    oracle.build()
+    t1, f1 = sublayer_oracle_time(spec, inp, 1.0 / spec["B"])
+    frac = min(1.0, budget_s / max(t1 / f1, 1e-9))
+    t, frac = sublayer_oracle_time(spec, inp, frac)
+    nb = int(round(frac * spec["B"]))
+    return {"value": flops * frac / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "the first %d of %d batch elements (%.3g%%), %.1f s; work scaled by the "
+                      "sampled share" % (nb, spec["B"], 100 * frac, t)}
+
+
+def run_sublayer(args):
+    import torch
+
+    import transformer_head_scaled_mha_gb300 as mha
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    spec = gen.SUBLAYERS[args.workload]
+    inp = gen.make_sublayer_inputs(spec, seed=args.seed)
+    lens = inp["lens"]
+    proj_flops, att_flops = sublayer_flops(spec, lens)
+    flops = proj_flops + att_flops
+    B, T, S, d = spec["B"], spec["T"], spec["S"], spec["d_model"]
+    H, Hkv, dk, dv = spec["H"], spec["H_kv"], spec["dk"], spec["dv"]
+    scale = gen.default_scale(dk)
+    mask = spec["mask"]
+
+    def host(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+
+    hx = host(inp["x"])
+    hm = host(inp["mem"]) if inp["mem"] is not None else None
+    w = [host(a).to(dev) for a in inp["w"]]
+    bias = [host(a).to(dev) for a in inp["b"]]
+    kl = torch.from_numpy(lens).to(dev) if lens is not None else None
+    set_bytes = hx.numel() * 2 * 2 + (hm.numel() * 2 if hm is not None else 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes))
+    sets = [(hx.to(dev), hm.to(dev) if hm is not None else None,
+             torch.empty((B, T, d), dtype=torch.bfloat16, device=dev)) for _ in range(n_sets)]
+    ws = torch.empty(mha.mha_sublayer_workspace_size(B, T, S, d, H, Hkv, dk, dv),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        xx, mm, oo = sets[i % n_sets]
+        mha.mha_sublayer_fwd(xx, *w, *bias, mem=mm, H=H, H_kv=Hkv, mask_kind=mask,
+                             key_lengths=kl, scale=scale, workspace=ws, out=oo, stream=s)
+
+    def timed(fn, steps):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                fn(i, stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(steps):
+                fn(i, stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.time()
+    per_step = timed(step, args.steps)
+    per_step = max_over_ranks(per_step, world, dev)
+    t_wall1 = time.time()
+    sampler.mark(t_soak, t_wall1)
+    clocks = sampler.stop()
+    value = flops / per_step / 1e12 * world
+    st = mha.mha_debug_status(stream)
+    if st != mha.MHA_OK:
+        raise RuntimeError("device status after timing: %s" % mha.mha_status_string(st))
+
+    # the dominant kernel, the projection, timed alone on the query projection
+    xq = [s_[0].view(B * T, d) for s_ in sets]
+    yq = torch.empty((B * T, H * dk), dtype=torch.bfloat16, device=dev)
+
+    def lin(i, s):
+        mha.mha_linear_fwd(xq[i % n_sets], w[0], bias[0], yq, stream=s)
+    lin_t = timed(lin, args.steps)
+    lin_flops = 2 * B * T * d * H * dk
+    peaks, peak_src = read_peaks()
+    achieved = lin_flops / lin_t / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": recorded_traffic(args.workload + ":linear"),
+                "kernel": "linear_tc_kernel (query projection %dx%dx%d, timed alone)" % (
+                    B * T, d, H * dk),
+                "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback", "algorithmic_flops": lin_flops,
+                "sublayer_share": {"projections_flops": proj_flops, "attention_flops": att_flops}}
+
+    # e2e: token vectors (and lengths) in, sublayer output back, every step;
+    # the weights stay resident like a model's parameters
+    px = hx.pin_memory()
+    pm = hm.pin_memory() if hm is not None else None
+    pl = torch.from_numpy(lens).pin_memory() if lens is not None else None
+    pout = torch.empty((B, T, d), dtype=torch.bfloat16).pin_memory()
+    dx, dm, do = sets[0]
+    dl = torch.empty_like(kl) if kl is not None else None
+    h2d = px.numel() * 2 + (pm.numel() * 2 if pm is not None else 0) + (
+        pl.numel() * 4 if pl is not None else 0)
+    d2h = pout.numel() * 2
+
+    def e2e_step():
+        dx.copy_(px, non_blocking=True)
+        if pm is not None:
+            dm.copy_(pm, non_blocking=True)
+        if pl is not None:
+            dl.copy_(pl, non_blocking=True)
+        mha.mha_sublayer_fwd(dx, *w, *bias, mem=dm, H=H, H_kv=Hkv, mask_kind=mask,
+                             key_lengths=dl, scale=scale, workspace=ws, out=do, stream=stream)
+        pout.copy_(do, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = sublayer_oracle_baseline(spec, inp, flops, args.cpu_budget)
+    if rank == 0:
+        line = {
+            "metric": "multi-head sublayer TFLOP/s", "value": round(value, 3),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded: x, mem N(0,1); W N(0,1/fan_in); b N(0,0.01); seed %d)"
+                    % args.seed,
+            "config": {"workload": args.workload, "B": B, "T": T, "S": S, "d_model": d,
+                       "H": H, "H_kv": Hkv, "d_k": dk, "d_v": dv, "mask_kind": mask,
+                       "len_range": spec["len_range"], "cross": spec["cross"],
+                       "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
+                             % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+                       "timing": "CUDA graph of %d calls (5 launches each), CUDA events"
+                                 % args.steps,
+                       "parallelism": "weak: same workload per rank, no collective"
+                       if world > 1 else "1 GPU"},
+            "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "note": "weights resident on the device"},
+            "gpu_launches": 5 * args.steps,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference_sublayer(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    spec = gen.SUBLAYERS[args.workload]
+    inp = gen.make_sublayer_inputs(spec, seed=args.seed)
+    proj, att = sublayer_flops(spec, inp["lens"])
+    flops = proj + att
+    import oracle
+    oracle.build()
+    t1, f1 = sublayer_oracle_time(spec, inp, 1.0 / spec["B"])
+    frac = min(1.0, args.ref_step_budget / max(t1 / f1, 1e-9))
+    for _ in range(args.warmup):
+        sublayer_oracle_time(spec, inp, frac)
+    runs = [sublayer_oracle_time(spec, inp, frac) for _ in range(args.steps)]
+    t = sum(r[0] for r in runs)
+    frac = runs[0][1]
+    value = flops * frac * args.steps / t / 1e12
+    sample = "each step: the first %d of %d batch elements, scaled by the sampled share" % (
+        int(round(frac * spec["B"])), spec["B"])
+    line = {"impl": "reference", "metric": "multi-head sublayer TFLOP/s",
+            "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, seed %d)" % args.seed,
+            "config": {"workload": args.workload, "B": spec["B"], "T": spec["T"],
+                       "S": spec["S"], "d_model": spec["d_model"], "H": spec["H"],
+                       "H_kv": spec["H_kv"], "mask_kind": spec["mask"]},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                             "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -497,7 +742,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(gen.WORKLOADS) + sorted(gen.SUBLAYERS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a graph")
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing, s")
@@ -513,10 +759,11 @@ def main(argv=None):
         if not (world == 1 and args.gpus == 1):
             print("warning: --gpus %d but WORLD_SIZE %d; using WORLD_SIZE" % (args.gpus, world),
                   file=sys.stderr)
+    sub = args.workload in gen.SUBLAYERS
     if args.impl == "reference":
-        run_reference(args)
+        (run_reference_sublayer if sub else run_reference)(args)
     else:
-        run_ours(args)
+        (run_sublayer if sub else run_ours)(args)
 
 
 if __name__ == "__main__":

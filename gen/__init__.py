@@ -171,6 +171,52 @@ WORKLOADS = {
 }
 
 
+# Multi-head attention sublayers (projections + attention + output projection)
+# of the same three Transformer roles: x, mem ~ N(0, 1); weights ~ N(0, 1/fan_in)
+# (unit-variance projections); biases ~ N(0, 0.1^2).
+STREAM_X, STREAM_MEM, STREAM_W, STREAM_B = 4, 5, 6, 10  # W: 6..9, b: 10..13 (q, k, v, o)
+
+SUBLAYERS = {
+    # Transformer-base encoder self-attention sublayer, key + query padding
+    "sublayer_enc_bf16_b256_t64_d512_h8": dict(B=256, T=64, S=64, d_model=512, H=8, H_kv=8,
+                                               dk=64, dv=64, mask=MASK_KEY_PADDING |
+                                               MASK_QUERY_PADDING, len_range=(8, 64),
+                                               cross=False),
+    # Transformer-base decoder causal self-attention sublayer
+    "sublayer_dec_causal_bf16_b128_t128_d512_h8": dict(B=128, T=128, S=128, d_model=512, H=8,
+                                                       H_kv=8, dk=64, dv=64, mask=MASK_CAUSAL,
+                                                       len_range=None, cross=False),
+    # Transformer-big cross-attention sublayer, source key padding
+    "sublayer_cross_bf16_b64_t96_s128_d1024_h16": dict(B=64, T=96, S=128, d_model=1024, H=16,
+                                                       H_kv=16, dk=64, dv=64,
+                                                       mask=MASK_KEY_PADDING,
+                                                       len_range=(16, 128), cross=True),
+}
+
+
+def make_sublayer_inputs(spec: dict, seed: int = 0) -> dict:
+    """bf16 bits of x, mem (None for self-attention), W_q, W_k, W_v, W_o, their
+    biases, and the key lengths (or None) of a sublayer spec."""
+    B, T, S, d = spec["B"], spec["T"], spec["S"], spec["d_model"]
+    H, Hkv, dk, dv = spec["H"], spec["H_kv"], spec["dk"], spec["dv"]
+    x = tensor(seed, STREAM_X, (B, T, d), "bf16")
+    mem = tensor(seed, STREAM_MEM, (B, S, d), "bf16") if spec["cross"] else None
+    shapes = [(d, H * dk), (d, Hkv * dk), (d, Hkv * dv), (H * dv, d)]
+    w = [tensor(seed, STREAM_W + i, sh, "bf16", amp=float(1.0 / np.sqrt(sh[0])))
+         for i, sh in enumerate(shapes)]
+    b = [tensor(seed, STREAM_B + i, (sh[1],), "bf16", amp=0.1) for i, sh in enumerate(shapes)]
+    lr = spec.get("len_range")
+    lens = lengths(seed, B, lr[0], lr[1]) if lr is not None else None
+    return dict(x=x, mem=mem, w=w, b=b, lens=lens)
+
+
+def sublayer_attention_spec(spec: dict) -> dict:
+    """The attention step of a sublayer spec, as an attention workload spec."""
+    return dict(B=spec["B"], H=spec["H"], Lq=spec["T"], Lk=spec["S"], dk=spec["dk"],
+                dv=spec["dv"], dtype="bf16", amp=1.0, mask=spec["mask"],
+                len_range=spec.get("len_range"), Hkv=spec["H_kv"], layout="bshd")
+
+
 def default_scale(dk: int) -> float:
     """1/sqrt(d_k) as the float32 value a caller passes through the C ABI."""
     return float(np.float32(1.0 / np.sqrt(np.float64(dk))))
