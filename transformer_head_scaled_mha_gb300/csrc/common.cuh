@@ -67,13 +67,14 @@ cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
 
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
 
-// y = x W + b (bf16): x viewed as (K, M), W as (N, K), 128-byte swizzle;
-// boxes (64, 128) and (64, 64)
+// y = x W + b (bf16), 128-byte swizzle.  Slab tiling (K, N multiples of 64):
+// x viewed as (64, M, K/64) box (64, 128, 2), W as (64, K, N/64) box
+// (64, 128, 2); otherwise x as (K, M) box (64, 128), W as (N, K) box (64, 64).
 struct LinearMaps {
   CUtensorMap x;
   CUtensorMap w;
 };
 cudaError_t launch_linear_tc(const LinearMaps &maps, const void *bias, void *y, int M, int N,
-                             int K, int *status, int num_sms, cudaStream_t stream);
+                             int K, bool slabs, int *status, int num_sms, cudaStream_t stream);
 
 }  // namespace mha

@@ -103,6 +103,23 @@ bool make_map_2d(CUtensorMap *map, const void *base, int cols, int rows, int box
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view (64, rows, cols / 64) of a row-major bf16 matrix whose column
+// count is a multiple of 64: 64-wide column slabs, 128-byte swizzle; box
+// (64, box_rows, 2) -- two slabs per copy
+bool make_map_slabs(CUtensorMap *map, const void *base, int cols, int rows, int box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 2u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -281,10 +298,13 @@ int run_linear(const void *x, const void *w, const void *b, void *y, int M, int 
   if (sms <= 0 || status == nullptr) return MHA_ERR_CUDA;
   LinearMaps m;
   std::memset(&m, 0, sizeof m);
-  if (!make_map_2d(&m.x, x, K, M, 64, 128) || !make_map_2d(&m.w, w, N, K, 64, 64))
-    return MHA_ERR_CUDA;
-  return launch_linear_tc(m, b, y, M, N, K, status, sms, stream) == cudaSuccess ? MHA_OK
-                                                                              : MHA_ERR_CUDA;
+  const bool slabs = K % 64 == 0 && N % 64 == 0;
+  const bool ok = slabs ? make_map_slabs(&m.x, x, K, M, 128) && make_map_slabs(&m.w, w, N, K, 128)
+                        : make_map_2d(&m.x, x, K, M, 64, 128) && make_map_2d(&m.w, w, N, K, 64, 64);
+  if (!ok) return MHA_ERR_CUDA;
+  return launch_linear_tc(m, b, y, M, N, K, slabs, status, sms, stream) == cudaSuccess
+             ? MHA_OK
+             : MHA_ERR_CUDA;
 }
 
 constexpr size_t kWsAlign = 256;
