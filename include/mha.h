@@ -206,6 +206,29 @@ int mha_sublayer_fwd(const void *x, const void *mem, void *out,
                      int mask_kind, const int32_t *key_lengths, float scale, int dtype,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * mha_sublayer_fwd_static -- mha_sublayer_fwd without a caller workspace.
+ *
+ * The pages have no counterpart: this is an interface convenience.  For
+ * callers that cannot provide device memory for the intermediates (hosts whose
+ * device memory is budgeted up front and must not allocate on their serving
+ * path, C callers without a device allocator of their own).  The library uses
+ * its own static device scratch of 64 MiB per device (reserved when the
+ * library's device code is loaded); nothing is allocated per call.  Shapes
+ * whose mha_sublayer_workspace_size exceeds 64 MiB return MHA_ERR_UNSUPPORTED
+ * (use mha_sublayer_fwd).  The first call on a device looks the scratch up
+ * (make that call before any stream capture).  All calls on a device share the
+ * one scratch: calls that overlap in time, on other streams or threads, race
+ * on it and must be serialised by the caller.  Arguments and errors otherwise
+ * as for mha_sublayer_fwd.
+ */
+int mha_sublayer_fwd_static(const void *x, const void *mem, void *out,
+                            const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                            const void *b_q, const void *b_k, const void *b_v, const void *b_o,
+                            int B, int T, int S, int d_model, int H, int H_kv, int d_k, int d_v,
+                            int mask_kind, const int32_t *key_lengths, float scale, int dtype,
+                            void *stream);
+
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed
    short-sequence tensor-core kernel (Lq, Lk <= 128), 3 = long-sequence

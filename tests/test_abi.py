@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-         "mha_sublayer_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status",
+         "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_status_string",
+         "mha_debug_status",
          "mha_version"])
 
 
@@ -185,3 +186,16 @@ def test_sublayer_rejects_before_launch(mha):
     assert call(scale=math.nan) == E_ARG
     assert call(mask=2, kl=ws + 512) == E_ARG  # lengths inside the workspace
     assert call(B=0) == mha.MHA_OK
+
+
+def test_static_sublayer_rejects_shapes_beyond_its_scratch(mha):
+    # 64 MiB of static scratch: the Transformer-base encoder sublayer at
+    # B=256, T=64 needs exactly that; one more batch element does not fit
+    S_ = mha.lib.mha_sublayer_fwd_static
+    p = [FAKE + (i << 24) for i in range(12)]
+    call = lambda B: S_(p[0], None, p[2], p[3], p[4], p[5], p[6], None, None, None, None, B, 64,
+                        64, 512, 8, 8, 64, 64, 0, None, 0.125, 1, None)
+    assert mha.mha_sublayer_workspace_size(256, 64, 64, 512, 8, 8, 64, 64) == 64 << 20
+    assert call(257) == mha.MHA_ERR_UNSUPPORTED
+    assert call(-1) == mha.MHA_ERR_INVALID_ARGUMENT
+    assert call(0) == mha.MHA_OK

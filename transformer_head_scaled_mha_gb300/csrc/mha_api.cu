@@ -401,6 +401,62 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
   return run_linear(heads, w_o, b_o, out, static_cast<int>(Mq), H * d_v, d_model, stream);
 }
 
+namespace {
+
+// Scratch for mha_sublayer_fwd_static: the library's own device memory for the
+// projected q, k, v and the concatenated heads, a fixed 64 MiB per device
+// (enough for the Transformer-base encoder sublayer at B = 256, T = 64,
+// d_model = 512).  It is reserved when the module is loaded, never by a call.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(64) << 20;
+__device__ __align__(256) uint8_t g_sublayer_scratch[kStaticScratchBytes];
+
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
+
+// Device address of this device's scratch, looked up once per device (a
+// symbol lookup, not an allocation).
+void *scratch_ptr(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  void *v = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (v != nullptr) return v;
+  if (cudaGetSymbolAddress(&v, g_sublayer_scratch) != cudaSuccess) return nullptr;
+  g_scratch_ptr[dev].store(v, std::memory_order_release);
+  return v;
+}
+
+}  // namespace
+
+// For callers that cannot hand the sublayer a workspace: hosts whose device
+// memory is budgeted up front and that must not allocate on their serving
+// path, or C callers without a device allocator of their own.  Same
+// computation as mha_sublayer_fwd, with the library's static scratch as the
+// workspace; no allocation and no allocating library call.  Nothing in the
+// scratch must start at zero: every step writes its output in full before the
+// next reads it.  All calls on a device share the one scratch, so calls that
+// overlap in time (other streams, other threads) race on it.
+extern "C" int mha_sublayer_fwd_static(const void *x, const void *mem, void *out,
+                                       const void *w_q, const void *w_k, const void *w_v,
+                                       const void *w_o, const void *b_q, const void *b_k,
+                                       const void *b_v, const void *b_o, int B, int T, int S,
+                                       int d_model, int H, int H_kv, int d_k, int d_v,
+                                       int mask_kind, const int32_t *key_lengths, float scale,
+                                       int dtype, void *stream) {
+  if (B < 0 || T < 0 || S < 0 || H < 0 || H_kv < 0 || d_k < 0 || d_v < 0)
+    return MHA_ERR_INVALID_ARGUMENT;
+  if (sublayer_ws(B, T, S, H, H_kv, d_k, d_v).total > kStaticScratchBytes)
+    return MHA_ERR_UNSUPPORTED;  // larger than the static scratch: use mha_sublayer_fwd
+  if (static_cast<long long>(B) * T == 0)
+    return mha_sublayer_fwd(x, mem, out, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, B, T, S,
+                            d_model, H, H_kv, d_k, d_v, mask_kind, key_lengths, scale, dtype,
+                            nullptr, 0, stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+  void *scratch = scratch_ptr(dev);
+  if (scratch == nullptr) return MHA_ERR_CUDA;
+  return mha_sublayer_fwd(x, mem, out, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, B, T, S, d_model,
+                          H, H_kv, d_k, d_v, mask_kind, key_lengths, scale, dtype, scratch,
+                          kStaticScratchBytes, stream);
+}
+
 extern "C" const char *mha_status_string(int status) {
   switch (status) {
     case MHA_OK: return "ok";

@@ -19,7 +19,7 @@ PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fi
 MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 
 EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-            "mha_sublayer_fwd", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
+            "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
 
 
 class MhaError(RuntimeError):
@@ -48,6 +48,8 @@ def _load() -> ctypes.CDLL:
     lib.mha_sublayer_fwd.restype = i32
     lib.mha_sublayer_fwd.argtypes = [vp] * 11 + [i32] * 9 + [vp, ctypes.c_float, i32, vp,
                                                             ctypes.c_size_t, vp]
+    lib.mha_sublayer_fwd_static.restype = i32
+    lib.mha_sublayer_fwd_static.argtypes = [vp] * 11 + [i32] * 9 + [vp, ctypes.c_float, i32, vp]
     lib.mha_fwd_path.restype = i32
     lib.mha_fwd_path.argtypes = [i32] * 8
     lib.mha_status_string.restype = ctypes.c_char_p
@@ -259,4 +261,43 @@ def mha_sublayer_fwd(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=No
                                   workspace.numel(), _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st, "mha_sublayer_fwd")
+    return out
+
+
+def mha_sublayer_fwd_static(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=None, *,
+                            mem=None, H, H_kv=None, mask_kind: int = 0, key_lengths=None,
+                            scale=None, out=None, stream=None):
+    """mha_sublayer_fwd on the library's static device scratch (no workspace,
+    nothing allocated per call; calls that overlap in time race on the
+    scratch).  Raises MhaError (unsupported) above 64 MiB of intermediates."""
+    import torch
+    H_kv = H if H_kv is None else H_kv
+    _bf16_cuda("x", x, 3)
+    _bf16_cuda("mem", mem, 3)
+    for name, t in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v), ("w_o", w_o)):
+        _bf16_cuda(name, t, 2)
+    for name, t in (("b_q", b_q), ("b_k", b_k), ("b_v", b_v), ("b_o", b_o)):
+        _bf16_cuda(name, t, 1)
+    B, T, d_model = x.shape
+    S = mem.shape[1] if mem is not None else T
+    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H_kv
+    if out is None:
+        out = torch.empty((B, T, w_o.shape[1]), dtype=x.dtype, device=x.device)
+    kl_ptr = None
+    if key_lengths is not None:
+        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
+            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
+        kl_ptr = key_lengths.data_ptr()
+    if scale is None:
+        scale = float(d_k) ** -0.5
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    mem_ptr = None if mem is None else (mem.data_ptr() if mem.numel() else x.data_ptr())
+    with torch.cuda.device(x.device):
+        st = lib.mha_sublayer_fwd_static(ptr(x), mem_ptr, ptr(out), ptr(w_q), ptr(w_k),
+                                         ptr(w_v), ptr(w_o), ptr(b_q), ptr(b_k), ptr(b_v),
+                                         ptr(b_o), B, T, S, d_model, H, H_kv, d_k, d_v,
+                                         int(mask_kind), kl_ptr, float(scale), MHA_DTYPE_BF16,
+                                         _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_sublayer_fwd_static")
     return out
