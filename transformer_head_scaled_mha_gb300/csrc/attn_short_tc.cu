@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // Everything above overlaps the previous launch's tail when launched as a
-  // programmatic dependent; global memory is touched only after this wait.
-  griddep_wait();
+  // Launched as a programmatic dependent, the kernel overlaps the previous
+  // launch's tail up to griddep_wait: each role does its own set-up first and
+  // waits just before its first global-memory access, so no warp's set-up
+  // delays another's first copy once the dependency resolves.
   griddep_launch_dependents();
 
   int issued = 0;                   // producers: units whose loads were issued
@@ -289,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       return clamp_len(p, (static_cast<int>(blockIdx.x) + nl * static_cast<int>(gridDim.x)) /
                               g.units_per_b);
     };
-    int lens = load_lens(0);
     UnitWalk cur(blockIdx.x, gridDim.x, g.units_per_b);
+    griddep_wait();
+    int lens = load_lens(0);
     for (int n = 0; n < n_local; ++n, cur.next()) {
       const int s = n % kStages;
       const int b = cur.b, h0 = cur.hu * g.P;
@@ -437,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return pr < g.P && at.hu * g.P + pr < p.H && i < p.Lq;
     };
     UnitWalk cur(blockIdx.x + w * gridDim.x, kWGs * gridDim.x, g.units_per_b);
+    griddep_wait();
     int len_cur = (w < n_local && row_valid(cur)) ? clamp_len(p, cur.b) : 0;
     for (int n = w; n < n_local; n += kWGs) {
       const int k = n / kWGs;  // this warpgroup's k-th unit
