@@ -146,7 +146,7 @@ def lengths(seed: int, count: int, lo: int, hi: int, stream: int = STREAM_LENGTH
 # Workloads (shapes, value distributions and masks of the five attention
 # settings: Transformer-base/big sentence lengths and one long causal context).
 # ---------------------------------------------------------------------------
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_QUERY_PADDING = 0, 1, 2, 4
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_QUERY_PADDING, MASK_CAUSAL_TAIL = 0, 1, 2, 4, 8
 
 WORKLOADS = {
     # fp32 encoder self-attention, no mask

@@ -34,7 +34,7 @@ _SRC = os.path.join(_HERE, "mha_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "libmha_oracle.so")
 
-MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_QUERY_PADDING = 0, 1, 2, 4
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_QUERY_PADDING, MASK_CAUSAL_TAIL = 0, 1, 2, 4, 8
 _IN_CODES = {np.dtype(np.float64): 0, np.dtype(np.float32): 1, np.dtype(np.uint16): 2}
 
 _lock = threading.Lock()

@@ -21,7 +21,14 @@
  *   0. len_b = clamp(key_lengths[b], 0, Lk) when a padding bit is set.
  *   1. QUERY_PADDING and i >= len_b: the row is padding, output +0.  Stop.
  *   2. Allowed keys A_i = { j < Lk : (!CAUSAL or j <= i) and
- *                                    (!KEY_PADDING or j < len_b) }.
+ *                                    (!KEY_PADDING or j < len_b) and
+ *                                    (!CAUSAL_TAIL or j <= len_b - Lq + i) }.
+ *      CAUSAL_TAIL is generation with a key/value cache (alexdo.xyz, "How
+ *      predictions are generated": the keys and values of earlier positions
+ *      are cached, only the new positions are computed): the Lq queries are
+ *      the last Lq positions len_b - Lq .. len_b - 1 of a sequence whose
+ *      len_b keys are in the cache (len_b = Lk without KEY_PADDING), and each
+ *      sees the keys up to its own position.
  *   3. A_i empty: output +0 (the pages leave this row undefined -- NaN -- and
  *      ask that no query attend to nothing; zero is the convention here).
  *   4. s_j = scale * sum_c q[i,c] k[j,c]                (step 1 and step 2)
@@ -52,7 +59,7 @@
 #endif
 
 enum { ORACLE_IN_F64 = 0, ORACLE_IN_F32 = 1, ORACLE_IN_BF16 = 2 };
-enum { ORACLE_CAUSAL = 1, ORACLE_KEY_PADDING = 2, ORACLE_QUERY_PADDING = 4 };
+enum { ORACLE_CAUSAL = 1, ORACLE_KEY_PADDING = 2, ORACLE_QUERY_PADDING = 4, ORACLE_CAUSAL_TAIL = 8 };
 
 static double widen(const void *base, int in_dtype, int64_t idx) {
   if (in_dtype == ORACLE_IN_F64) return ((const double *)base)[idx];
@@ -98,8 +105,11 @@ int oracle_mha_rows_ex_f64(const void *q, const void *k, const void *v, int in_d
   if (Hkv <= 0 ? H > 0 : (H % Hkv) != 0) return 1;
   if (layout != 0 && layout != 1) return 1;
   if (in_dtype < ORACLE_IN_F64 || in_dtype > ORACLE_IN_BF16) return 1;
-  if (mask_kind & ~(ORACLE_CAUSAL | ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) return 1;
+  if (mask_kind & ~(ORACLE_CAUSAL | ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING | ORACLE_CAUSAL_TAIL))
+    return 1;
   if ((mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)) && Lq != Lk) return 1;
+  if ((mask_kind & ORACLE_CAUSAL_TAIL) && (mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)))
+    return 1;
   if ((mask_kind & (ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) && key_lengths == NULL && B > 0)
     return 1;
   const int64_t total = (int64_t)B * H * Lq;
@@ -148,6 +158,7 @@ int oracle_mha_rows_ex_f64(const void *q, const void *k, const void *v, int in_d
         int ok = 1;
         if ((mask_kind & ORACLE_CAUSAL) && j > i) ok = 0;
         if ((mask_kind & ORACLE_KEY_PADDING) && j >= len_b) ok = 0;
+        if ((mask_kind & ORACLE_CAUSAL_TAIL) && j > len_b - Lq + i) ok = 0;
         allowed[j] = (char)ok;
         n_allowed += ok;
       }

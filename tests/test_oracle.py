@@ -289,7 +289,8 @@ def test_empty_shapes(oracle_lib):
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("mask,lens", [(0, None), (MASK_CAUSAL, None),
                                        (MASK_KEY_PADDING | MASK_QUERY_PADDING, [2, 5]),
-                                       (MASK_KEY_PADDING, [0, 3])])
+                                       (MASK_KEY_PADDING, [0, 3]),
+                                       (8 | MASK_KEY_PADDING, [4, 2]), (8, None)])
 def test_brute_force_high_precision(oracle_lib, mask, lens):
     mp = pytest.importorskip("mpmath")
     mp.mp.dps = 50
@@ -303,7 +304,8 @@ def test_brute_force_high_precision(oracle_lib, mask, lens):
             for i in range(L):
                 logits = []
                 for j in range(L):
-                    masked = (mask & MASK_CAUSAL and j > i) or (mask & MASK_KEY_PADDING and j >= lb)
+                    masked = ((mask & MASK_CAUSAL and j > i) or (mask & MASK_KEY_PADDING and j >= lb)
+                              or (mask & 8 and j > lb - L + i))
                     if masked:
                         logits.append(None)
                     else:
@@ -490,3 +492,58 @@ def test_sublayer_grouped_heads_equal_repeated_projections(oracle_lib):
     out2 = oracle.mha_sublayer(x, mem, w_q, rep(w_k), rep(w_v), w_o, b[0], rep(b[1]), rep(b[2]),
                                b[3], H=H)
     np.testing.assert_allclose(out, out2, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# generation with a key/value cache: the queries are the last Lq positions
+# --------------------------------------------------------------------------
+from oracle import MASK_CAUSAL_TAIL  # noqa: E402
+
+
+@pytest.mark.parametrize("Lq", [1, 3, 7])
+def test_cached_decoding_equals_full_causal_rows(oracle_lib, Lq):
+    # attending from the last Lq positions of a length-L sequence whose keys
+    # and values are all cached gives exactly the last Lq rows of full causal
+    # self-attention over the L positions
+    B, H, L, d = 2, 3, 20, 8
+    q, k, v = _rand(B, H, L, L, d, d, seed=11)
+    full = oracle.mha_fwd(q, k, v, mask_kind=MASK_CAUSAL, scale=0.4)
+    tail = oracle.mha_fwd(q[:, :, L - Lq:], k, v, mask_kind=MASK_CAUSAL_TAIL, scale=0.4)
+    np.testing.assert_allclose(tail, full[:, :, L - Lq:], rtol=0, atol=1e-14)
+
+
+def test_cached_decoding_with_lengths(oracle_lib):
+    # per-sequence cache lengths: sequence b's queries sit at positions
+    # len_b - Lq .. len_b - 1 and equal causal attention over its first len_b
+    # positions; a cache shorter than Lq leaves the early queries without keys
+    B, H, Lk, Lq, d = 3, 2, 16, 4, 8
+    q, k, v = _rand(B, H, Lq, Lk, d, d, seed=12)
+    lens = np.array([16, 9, 2], dtype=np.int32)
+    out = oracle.mha_fwd(q, k, v, mask_kind=MASK_CAUSAL_TAIL | MASK_KEY_PADDING,
+                         key_lengths=lens, scale=0.5)
+    for b, lb in enumerate(lens):
+        for i in range(Lq):
+            pos = lb - Lq + i
+            if pos < 0:
+                assert np.all(out[b, :, i] == 0)
+                continue
+            one = oracle.mha_fwd(q[b:b + 1, :, i:i + 1], k[b:b + 1, :, :pos + 1],
+                                 v[b:b + 1, :, :pos + 1], scale=0.5)
+            np.testing.assert_allclose(out[b, :, i], one[0, :, 0], rtol=0, atol=1e-14)
+
+
+def test_cached_decoding_single_query_is_key_padding(oracle_lib):
+    B, H, Lk, d = 3, 2, 16, 8
+    q, k, v = _rand(B, H, 1, Lk, d, d, seed=13)
+    lens = np.array([16, 5, 1], dtype=np.int32)
+    a = oracle.mha_fwd(q, k, v, mask_kind=MASK_CAUSAL_TAIL | MASK_KEY_PADDING, key_lengths=lens,
+                       scale=0.3)
+    b = oracle.mha_fwd(q, k, v, mask_kind=MASK_KEY_PADDING, key_lengths=lens, scale=0.3)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_cached_decoding_rejects_mixed_causal(oracle_lib):
+    q, k, v = _rand(1, 1, 4, 4, 4, 4)
+    for m in (MASK_CAUSAL_TAIL | MASK_CAUSAL, MASK_CAUSAL_TAIL | MASK_QUERY_PADDING):
+        with pytest.raises(ValueError):
+            oracle.mha_fwd(q, k, v, mask_kind=m, key_lengths=np.array([4], np.int32), scale=1.0)
