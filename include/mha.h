@@ -53,10 +53,18 @@ enum {
   MHA_MASK_KEY_PADDING = 2,
   /* query rows i >= key_lengths[b] are padding: written as +0.0; requires
      Lq == Lk (self-attention over one padded sequence) */
-  MHA_MASK_QUERY_PADDING = 4
+  MHA_MASK_QUERY_PADDING = 4,
+  /* generation with a key/value cache (alexdo.xyz, "How predictions are
+     generated"): the Lq queries are the last Lq positions len - Lq .. len - 1
+     of a sequence whose len keys are cached (len = key_lengths[b] with
+     KEY_PADDING, else Lk); query i sees keys j <= len - Lq + i.  Any Lq, Lk;
+     not combined with CAUSAL or QUERY_PADDING.  Queries before the cache's
+     first position (len < Lq) have no key and are written as +0.0. */
+  MHA_MASK_CAUSAL_TAIL = 8
 };
 /* encoder self-attention over padded sentences: KEY_PADDING | QUERY_PADDING;
-   cross-attention over a padded source: KEY_PADDING; decoder: CAUSAL. */
+   cross-attention over a padded source: KEY_PADDING; decoder: CAUSAL;
+   decoder step over a key/value cache: CAUSAL_TAIL | KEY_PADDING. */
 
 /* Memory layout of q, k, v and out (mha_fwd_ex; all four share it). */
 enum {

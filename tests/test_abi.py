@@ -63,7 +63,11 @@ def test_path_selection(mha):
     assert P(2, 2, 64, 64, 129, 64, 0, 0) == -2
     assert P(2, 2, 64, 65, 64, 64, 1, 1) == -1  # causal needs Lq == Lk
     assert P(2, 2, 64, 65, 64, 64, 4, 1) == -1  # query padding needs Lq == Lk
-    assert P(2, 2, 64, 64, 64, 64, 8, 1) == -1  # unknown mask bit
+    assert P(2, 2, 1, 4096, 128, 128, 8 | 2, 1) == 3  # cached decoding: any Lq, Lk
+    assert P(2, 2, 1, 100, 64, 64, 8, 1) == 2
+    assert P(2, 2, 64, 64, 64, 64, 8 | 1, 1) == -1  # not with CAUSAL
+    assert P(2, 2, 64, 64, 64, 64, 8 | 4, 1) == -1  # not with QUERY_PADDING
+    assert P(2, 2, 64, 64, 64, 64, 16, 1) == -1  # unknown mask bit
     assert P(-1, 2, 64, 64, 64, 64, 0, 1) == -1
     assert P(2, 2, 64, 64, 0, 64, 0, 1) == -1
     assert P(2, 2, 64, 64, 64, 64, 0, 7) == -1  # unknown dtype

@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   int kv_end = p.Lk;
   if (p.mask & kMaskKeyPadding) kv_end = len;
   if (p.mask & kMaskCausal) kv_end = min(kv_end, min(q0 + kRowsPerCta, p.Lq));
+  // cached decoding: the block's last query sits at position len - Lq + its row
+  if (p.mask & kMaskCausalTail)
+    kv_end = max(min(kv_end, len - p.Lq + min(q0 + kRowsPerCta, p.Lq)), 0);
 
   const HeadView vq = head_view(p.layout, b, h, p.H, p.Lq, dk);
   const HeadView vk = head_view(p.layout, b, hkv, p.Hkv, p.Lk, dk);
@@ -126,6 +129,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int c = 0; c < dk; ++c) dot = fmaf(qr[c], kr[c], dot);
       bool ok = (j < kv_end) && (i < p.Lq);
       if (p.mask & kMaskCausal) ok = ok && (j <= i);
+      if (p.mask & kMaskCausalTail) ok = ok && (j <= len - p.Lq + i);
       // step 2 (scale, in log2 units) and step 3 (online softmax)
       const float x = ok ? dot * p.scale_log2 : -INFINITY;
       const float m_new = fmaxf(m[r], warp_max(x));

@@ -118,7 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kv_end = p.Lk;
     if (p.mask & kMaskKeyPadding) kv_end = min(kv_end, len);
     if (p.mask & kMaskCausal) kv_end = min(kv_end, min(r0 + kBM, p.Lq));
-    n_tiles[w] = wg_rows[w] ? (kv_end + kBN - 1) / kBN : 0;
+    // the tile's last query sits at position len - Lq + its row
+    if (p.mask & kMaskCausalTail) kv_end = min(kv_end, len - p.Lq + min(r0 + kBM, p.Lq));
+    n_tiles[w] = wg_rows[w] && kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
   }
   const int n_kv = max(n_tiles[0], n_tiles[1]);
 
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int jmax = p.Lk;  // keys j < jmax are allowed for row i
     if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
     if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
+    if (p.mask & kMaskCausalTail) jmax = max(min(jmax, len - p.Lq + i + 1), 0);
     const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
 
     float m_use = -INFINITY;  // max used for the exponentials (log2 units)
@@ -269,7 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, sr[ch]);
       tmem_wait_ld();
 
-      const int lim = jmax - j * kBN;  // columns c < lim are allowed
+      // columns c < lim are allowed; a row may allow none of this tile's
+      // columns (rows of one tile see different key counts under the
+      // cached-decoding mask), so clamp to [0, kBN]
+      const int lim = min(max(jmax - j * kBN, 0), kBN);
       const bool need_mask = __any_sync(0xffffffffu, lim < kBN);
       // positive scale: max over the raw scores, then one FMA per score;
       // otherwise scale first (the max of scale * s is not scale * max s)

@@ -448,6 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jmax = p.Lk;
       if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
       if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
+      // cached decoding: query i sits at position len - Lq + i
+      if (p.mask & kMaskCausalTail) jmax = max(min(jmax, len - p.Lq + i + 1), 0);
       const bool qpad = (p.mask & kMaskQueryPadding) && i >= len;
       if (!valid || qpad) jmax = 0;
       // key columns of this row's pair: packed units hold pair pr's keys at

@@ -9,6 +9,7 @@ namespace mha {
 constexpr int kMaskCausal = 1;
 constexpr int kMaskKeyPadding = 2;
 constexpr int kMaskQueryPadding = 4;
+constexpr int kMaskCausalTail = 8;  // queries are the last Lq of len keys (cached decoding)
 
 constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = 4;

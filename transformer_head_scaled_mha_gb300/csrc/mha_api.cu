@@ -129,7 +129,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 // Validates and picks a path; returns a non-negative Path or -(mha_status).
 int select_path(int B, int H, int Lq, int Lk, int dk, int dv, int mask, int dtype) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk <= 0 || dv <= 0) return -MHA_ERR_INVALID_ARGUMENT;
-  if (mask & ~(kMaskCausal | kMaskKeyPadding | kMaskQueryPadding))
+  if (mask & ~(kMaskCausal | kMaskKeyPadding | kMaskQueryPadding | kMaskCausalTail))
+    return -MHA_ERR_INVALID_ARGUMENT;
+  if ((mask & kMaskCausalTail) && (mask & (kMaskCausal | kMaskQueryPadding)))
     return -MHA_ERR_INVALID_ARGUMENT;
   if ((mask & (kMaskCausal | kMaskQueryPadding)) && Lq != Lk) return -MHA_ERR_INVALID_ARGUMENT;
   if (dtype != MHA_DTYPE_F32 && dtype != MHA_DTYPE_BF16) return -MHA_ERR_INVALID_ARGUMENT;

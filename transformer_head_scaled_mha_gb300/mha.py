@@ -13,6 +13,7 @@ from . import _build
 
 MHA_DTYPE_F32, MHA_DTYPE_BF16 = 0, 1
 MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_QUERY_PADDING = 0, 1, 2, 4
+MHA_MASK_CAUSAL_TAIL = 8
 MHA_OK, MHA_ERR_INVALID_ARGUMENT, MHA_ERR_UNSUPPORTED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = range(5)
 PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fill"}
 
