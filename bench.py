@@ -61,11 +61,12 @@ def algorithmic(spec, lens):
     flops: 2 * (d_k + d_v) per allowed (query, key) pair.
     """
     B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
+    Hkv = spec.get("Hkv", H)
     esz = 4 if spec["dtype"] == "f32" else 2
     m = spec["mask"]
     L = np.full(B, Lk, dtype=np.int64) if lens is None else np.clip(lens.astype(np.int64), 0, Lk)
     q_rows = (np.minimum(L, Lq) if m & gen.MASK_QUERY_PADDING else np.full(B, Lq)).sum() * H
-    kv_rows = (L if m & gen.MASK_KEY_PADDING else np.full(B, Lk)).sum() * H
+    kv_rows = (L if m & gen.MASK_KEY_PADDING else np.full(B, Lk)).sum() * Hkv
     nbytes = esz * (q_rows * dk + kv_rows * (dk + dv) + B * H * Lq * dv)
     if lens is not None and m & (gen.MASK_KEY_PADDING | gen.MASK_QUERY_PADDING):
         nbytes += 4 * B
@@ -76,6 +77,9 @@ def algorithmic(spec, lens):
         if m & gen.MASK_CAUSAL:
             i = np.arange(nq)
             pairs += int(np.minimum(i + 1, kmax).sum())
+        elif m & gen.MASK_CAUSAL_TAIL:
+            i = np.arange(nq)
+            pairs += int(np.clip(kmax - Lq + i + 1, 0, kmax).sum())
         else:
             pairs += nq * kmax
     flops = 2 * (dk + dv) * pairs * H
@@ -83,7 +87,10 @@ def algorithmic(spec, lens):
 
 
 def bound_of(spec):
-    return "tensor" if spec["Lq"] > 128 or spec["Lk"] > 128 else "hbm"
+    """Tensor-bound when the work is long in both the query and the key
+    direction (about 2 (d_k + d_v) min(Lq, Lk) / (2 d) flop per byte); HBM-bound
+    for sentence-length attention and for generation steps (few queries)."""
+    return "tensor" if min(spec["Lq"], spec["Lk"]) > 128 else "hbm"
 
 
 def metric_of(spec):
@@ -250,7 +257,7 @@ def time_oracle(spec, q, k, v, lens, rows, threads=0, reps=1):
     t0 = time.perf_counter()
     for _ in range(reps):
         oracle.mha_fwd(q, k, v, mask_kind=spec["mask"], key_lengths=lens, scale=scale,
-                       rows=rows, threads=threads)
+                       rows=rows, threads=threads, layout=spec.get("layout", "bhsd"))
     return time.perf_counter() - t0
 
 
@@ -310,6 +317,7 @@ def run_ours(args):
         return t.view(torch.bfloat16) if dt == "bf16" else t
 
     hq, hk, hv = host_tensor(q), host_tensor(k), host_tensor(v)
+    out_shape = (B, Lq, H, dv) if spec.get("layout", "bhsd") == "bshd" else (B, H, Lq, dv)
     set_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     set_bytes += B * H * Lq * dv * hq.element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -317,13 +325,23 @@ def run_ours(args):
     sets = []
     for _ in range(n_sets):
         sets.append((hq.to(dev), hk.to(dev), hv.to(dev),
-                     torch.empty((B, H, Lq, dv), dtype=hq.dtype, device=dev)))
+                     torch.empty(out_shape, dtype=hq.dtype, device=dev)))
     kl = torch.from_numpy(lens).to(dev) if lens is not None else None
     stream = torch.cuda.Stream(device=dev)
 
+    plain = spec.get("Hkv", H) == H and spec.get("layout", "bhsd") == "bhsd"
+
+    def call(qq, kk, vv, oo, lens_dev, s):
+        if plain:
+            mha.mha_fwd(qq, kk, vv, oo, mask_kind=mask, key_lengths=lens_dev, scale=scale,
+                        stream=s)
+        else:
+            mha.mha_fwd_ex(qq, kk, vv, oo, layout=spec["layout"], mask_kind=mask,
+                           key_lengths=lens_dev, scale=scale, stream=s)
+
     def step(i, s=None):
         qq, kk, vv, oo = sets[i % n_sets]
-        mha.mha_fwd(qq, kk, vv, oo, mask_kind=mask, key_lengths=kl, scale=scale, stream=s)
+        call(qq, kk, vv, oo, kl, s)
 
     # warm-up (eager): W steps
     with torch.cuda.stream(stream):
@@ -377,7 +395,7 @@ def run_ours(args):
 
     # e2e: pinned host buffers, copies inside the timed region
     pq, pk, pv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
-    pout = torch.empty((B, H, Lq, dv), dtype=hq.dtype).pin_memory()
+    pout = torch.empty(out_shape, dtype=hq.dtype).pin_memory()
     plen = torch.from_numpy(lens).pin_memory() if lens is not None else None
     dq, dk_, dv_, do = sets[0]
     dl = torch.empty_like(kl) if kl is not None else None
@@ -392,7 +410,7 @@ def run_ours(args):
         dv_.copy_(pv, non_blocking=True)
         if plen is not None:
             dl.copy_(plen, non_blocking=True)
-        mha.mha_fwd(dq, dk_, dv_, do, mask_kind=mask, key_lengths=dl, scale=scale, stream=stream)
+        call(dq, dk_, dv_, do, dl, stream)
         pout.copy_(do, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -431,7 +449,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dt, "data": "synthetic (seeded N(0,1)%s inputs, seed %d)" % (
                 "*%g" % spec["amp"] if spec["amp"] != 1.0 else "", args.seed),
-            "config": {"workload": args.workload, "B": B, "H": H, "Lq": Lq, "Lk": Lk,
+            "config": {"workload": args.workload, "B": B, "H": H, "H_kv": spec.get("Hkv", H),
+                       "layout": spec.get("layout", "bhsd"), "Lq": Lq, "Lk": Lk,
                        "d_k": dk, "d_v": dv, "mask_kind": mask,
                        "len_range": spec["len_range"], "scale": scale,
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"

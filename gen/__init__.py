@@ -168,6 +168,18 @@ WORKLOADS = {
     "long_causal_bf16_b4_h16_l8192_d128": dict(B=4, H=16, Lq=8192, Lk=8192, dk=128, dv=128,
                                                dtype="bf16", amp=0.5, mask=MASK_CAUSAL,
                                                len_range=None),
+    # one generation step of the Transformer-base decoder: one new token per
+    # sequence against its cached keys/values (cache lengths U{128..1024})
+    "decode_bf16_b256_h8_lk1024_d64": dict(B=256, H=8, Lq=1, Lk=1024, dk=64, dv=64,
+                                           dtype="bf16", amp=1.0,
+                                           mask=MASK_CAUSAL_TAIL | MASK_KEY_PADDING,
+                                           len_range=(128, 1024), layout="bshd"),
+    # a generation step with grouped key/value heads and long caches
+    # (32 query heads over 8 key/value heads, d=128, lengths U{4096..8192})
+    "decode_gqa_bf16_b64_h32_kv8_lk8192_d128": dict(B=64, H=32, Hkv=8, Lq=1, Lk=8192, dk=128,
+                                                    dv=128, dtype="bf16", amp=1.0,
+                                                    mask=MASK_CAUSAL_TAIL | MASK_KEY_PADDING,
+                                                    len_range=(4096, 8192), layout="bshd"),
 }
 
 
