@@ -144,8 +144,9 @@ int mha_fwd(const void *q, const void *k, const void *v, void *out,
  * Every other argument, the ownership rules and the error behaviour are those
  * of mha_fwd; an H_kv that does not divide H, or another layout value, is
  * MHA_ERR_INVALID_ARGUMENT.  mha_fwd(...) equals mha_fwd_ex with H_kv = H and
- * MHA_LAYOUT_BHSD.  The kernel choice does not depend on H_kv or the layout
- * (mha_fwd_path applies).
+ * MHA_LAYOUT_BHSD.  The kernel choice depends on H_kv only through the
+ * number of query rows per key/value head, (H / H_kv) * Lq (mha_fwd_path_ex),
+ * and not on the layout.
  */
 int mha_fwd_ex(const void *q, const void *k, const void *v, void *out,
                int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
@@ -240,9 +241,18 @@ int mha_sublayer_fwd_static(const void *x, const void *mem, void *out,
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed
    short-sequence tensor-core kernel (Lq, Lk <= 128), 3 = long-sequence
-   tensor-core kernel, 4 = zero fill (Lk == 0); negative = -(mha_status) for
-   arguments mha_fwd would reject.  Host only, launches nothing. */
+   tensor-core kernel, 4 = zero fill (Lk == 0), 5 = few-query tensor-core
+   kernel (decoding steps: at most 16 query rows per key/value head, mask
+   NONE, KEY_PADDING and/or CAUSAL_TAIL, Lk > 128 or d = 128); negative =
+   -(mha_status) for arguments mha_fwd would reject.  Host only, launches
+   nothing. */
 int mha_fwd_path(int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind, int dtype);
+
+/* The same for mha_fwd_ex with H_kv key/value heads (mha_fwd_path is this
+   with H_kv = H); an H_kv that does not divide H gives
+   -MHA_ERR_INVALID_ARGUMENT. */
+int mha_fwd_path_ex(int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                    int dtype);
 
 /* Static text for a status code. */
 const char *mha_status_string(int status);

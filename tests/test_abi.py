@@ -27,8 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-         "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_status_string",
-         "mha_debug_status",
+         "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_fwd_path_ex",
+         "mha_status_string", "mha_debug_status",
          "mha_version"])
 
 
@@ -63,14 +63,36 @@ def test_path_selection(mha):
     assert P(2, 2, 64, 64, 129, 64, 0, 0) == -2
     assert P(2, 2, 64, 65, 64, 64, 1, 1) == -1  # causal needs Lq == Lk
     assert P(2, 2, 64, 65, 64, 64, 4, 1) == -1  # query padding needs Lq == Lk
-    assert P(2, 2, 1, 4096, 128, 128, 8 | 2, 1) == 3  # cached decoding: any Lq, Lk
-    assert P(2, 2, 1, 100, 64, 64, 8, 1) == 2
+    assert P(2, 2, 1, 4096, 128, 128, 8 | 2, 1) == 5  # cached decoding: few query rows
+    assert P(2, 2, 16, 4096, 64, 64, 8, 1) == 5
+    assert P(2, 2, 1, 129, 64, 64, 0, 1) == 5
+    assert P(2, 2, 1, 100, 128, 128, 2, 1) == 5
+    assert P(2, 2, 17, 4096, 64, 64, 8, 1) == 3  # more than 16 rows: long kernel
+    assert P(2, 2, 1, 100, 64, 64, 8, 1) == 2  # d = 64, Lk <= 128: packed kernel
+    assert P(2, 2, 4, 4096, 128, 128, 8 | 2, 0) == 1  # fp32
     assert P(2, 2, 64, 64, 64, 64, 8 | 1, 1) == -1  # not with CAUSAL
     assert P(2, 2, 64, 64, 64, 64, 8 | 4, 1) == -1  # not with QUERY_PADDING
     assert P(2, 2, 64, 64, 64, 64, 16, 1) == -1  # unknown mask bit
     assert P(-1, 2, 64, 64, 64, 64, 0, 1) == -1
     assert P(2, 2, 64, 64, 0, 64, 0, 1) == -1
     assert P(2, 2, 64, 64, 64, 64, 0, 7) == -1  # unknown dtype
+
+
+def test_path_selection_with_shared_heads(mha):
+    # the few-query kernel takes (H / H_kv) * Lq <= 16 query rows per key/value head
+    PX = mha.mha_fwd_path_ex
+    assert PX(64, 32, 8, 1, 8192, 128, 128, 8 | 2, 1) == 5  # 4 rows
+    assert PX(2, 32, 2, 1, 8192, 128, 128, 8 | 2, 1) == 5  # 16 rows
+    assert PX(2, 32, 1, 1, 8192, 128, 128, 8 | 2, 1) == 3  # 32 rows: long kernel
+    assert PX(2, 8, 2, 4, 1000, 64, 64, 8, 1) == 5
+    assert PX(2, 8, 2, 5, 1000, 64, 64, 8, 1) == 3
+    assert PX(2, 8, 8, 1, 1000, 64, 64, 1, 1) == -1  # causal needs Lq == Lk
+    assert PX(2, 8, 3, 1, 1000, 64, 64, 0, 1) == -1  # H_kv must divide H
+    assert PX(2, 8, 0, 1, 1000, 64, 64, 0, 1) == -1
+    for args in [(2, 8, 1000, 1000, 64, 64, 1, 1), (256, 8, 1, 1024, 64, 64, 10, 1),
+                 (2, 2, 64, 64, 96, 96, 0, 1)]:
+        B, H = args[:2]
+        assert PX(B, H, H, *args[2:]) == mha.mha_fwd_path(*args)
 
 
 FAKE = 0x7F0000000000  # never dereferenced: every call below fails validation first

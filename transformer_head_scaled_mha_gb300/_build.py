@@ -16,7 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmha.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["mha_api.cu", "attn_f32_simt.cu", "attn_short_tc.cu", "attn_long_tc.cu", "linear_tc.cu"]
+SOURCES = ["mha_api.cu", "attn_f32_simt.cu", "attn_short_tc.cu", "attn_long_tc.cu", "attn_decode_tc.cu",
+           "linear_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

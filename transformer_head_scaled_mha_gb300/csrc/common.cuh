@@ -66,6 +66,15 @@ struct LongMaps {
 cudaError_t launch_long_tc(const LongMaps &maps, const Problem &p, int num_sms,
                            cudaStream_t stream);
 
+// few query rows (R = (H / Hkv) * Lq <= 16) against many keys: Q box
+// (64, Lq, H / Hkv, 1) -- a key/value head's whole group of query heads --,
+// K and V boxes (64, 128, 1, 1)
+struct DecodeMaps {
+  CUtensorMap q, k, v;
+};
+cudaError_t launch_decode_tc(const DecodeMaps &maps, const Problem &p, void *out, int num_sms,
+                             cudaStream_t stream);
+
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
 
 // y = x W + b (bf16), 128-byte swizzle.  Slab tiling (K, N multiples of 64):

@@ -20,7 +20,7 @@ namespace {
 // kStatusTimeout here.  One per device, in the module's static memory.
 __device__ int g_status = 0;
 
-enum Path { kPathNone = 0, kPathF32 = 1, kPathShort = 2, kPathLong = 3, kPathZero = 4 };
+enum Path { kPathNone = 0, kPathF32 = 1, kPathShort = 2, kPathLong = 3, kPathZero = 4, kPathDecode = 5 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -127,8 +127,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 // Validates and picks a path; returns a non-negative Path or -(mha_status).
-int select_path(int B, int H, int Lq, int Lk, int dk, int dv, int mask, int dtype) {
+int select_path(int B, int H, int H_kv, int Lq, int Lk, int dk, int dv, int mask, int dtype) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk <= 0 || dv <= 0) return -MHA_ERR_INVALID_ARGUMENT;
+  if (H_kv <= 0 ? H > 0 : (H % H_kv) != 0) return -MHA_ERR_INVALID_ARGUMENT;
   if (mask & ~(kMaskCausal | kMaskKeyPadding | kMaskQueryPadding | kMaskCausalTail))
     return -MHA_ERR_INVALID_ARGUMENT;
   if ((mask & kMaskCausalTail) && (mask & (kMaskCausal | kMaskQueryPadding)))
@@ -145,6 +146,11 @@ int select_path(int B, int H, int Lq, int Lk, int dk, int dv, int mask, int dtyp
   if (static_cast<long long>(B) * H * Lq == 0) return kPathNone;
   if (Lk == 0) return kPathZero;
   if (dtype == MHA_DTYPE_F32) return kPathF32;
+  // a few query rows per key/value head (decoding steps): keys on the lanes
+  const long long rows_per_kv = static_cast<long long>(H / H_kv) * Lq;
+  if ((mask & ~(kMaskKeyPadding | kMaskCausalTail)) == 0 && rows_per_kv <= 16 &&
+      (Lk > 128 || dk == 128))
+    return kPathDecode;
   // the packed kernel's 32-bit row strides need H <= 2^24
   if (dk == 64 && Lq <= 128 && Lk <= 128 && H <= (1 << 24)) return kPathShort;
   return kPathLong;
@@ -157,16 +163,20 @@ using namespace mha;
 
 extern "C" int mha_fwd_path(int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
                             int dtype) {
-  return select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
+  return select_path(B, H, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
+}
+
+extern "C" int mha_fwd_path_ex(int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v,
+                               int mask_kind, int dtype) {
+  return select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
 }
 
 extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H,
                           int H_kv, int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
                           const int32_t *key_lengths, float scale, int dtype, void *stream_) {
-  const int path = select_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype);
+  const int path = select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
   if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
-  if (H_kv <= 0 ? H > 0 : (H % H_kv) != 0) return MHA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   if (path == kPathNone) return MHA_OK;
   const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
@@ -246,6 +256,14 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
              make_map(&m.v_rows[h], v, 64, Lk, H_kv, B, layout, 8 * (h + 1), kv_box_heads);
       if (!ok) return MHA_ERR_CUDA;
       err = launch_short_tc(m, g, p, out, sms, stream);
+    } else if (path == kPathDecode) {
+      DecodeMaps m;
+      std::memset(&m, 0, sizeof m);
+      bool ok = make_map(&m.q, q, d_k, Lq, H, B, layout, Lq, H / H_kv) &&
+                make_map(&m.k, k, d_k, Lk, H_kv, B, layout, 128, 1) &&
+                make_map(&m.v, v, d_v, Lk, H_kv, B, layout, 128, 1);
+      if (!ok) return MHA_ERR_CUDA;
+      err = launch_decode_tc(m, p, out, sms, stream);
     } else {
       LongMaps m;
       std::memset(&m, 0, sizeof m);
@@ -368,7 +386,7 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
       (st = check_linear(mem, w_v, b_v, out, Mk, d_model, H_kv * d_v, dtype)) != MHA_OK ||
       (st = check_linear(heads, w_o, b_o, out, Mq, H * d_v, d_model, dtype)) != MHA_OK)
     return st;
-  const int path = select_path(B, H, T, S, d_k, d_v, mask_kind, dtype);
+  const int path = select_path(B, H, H_kv, T, S, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   if (Mq == 0) return MHA_OK;

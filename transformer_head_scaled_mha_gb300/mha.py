@@ -15,12 +15,14 @@ MHA_DTYPE_F32, MHA_DTYPE_BF16 = 0, 1
 MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_QUERY_PADDING = 0, 1, 2, 4
 MHA_MASK_CAUSAL_TAIL = 8
 MHA_OK, MHA_ERR_INVALID_ARGUMENT, MHA_ERR_UNSUPPORTED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = range(5)
-PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fill"}
+PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fill",
+              5: "decode_tc"}
 
 MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 
 EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-            "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_status_string", "mha_debug_status", "mha_version")
+            "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_fwd_path_ex",
+            "mha_status_string", "mha_debug_status", "mha_version")
 
 
 class MhaError(RuntimeError):
@@ -53,6 +55,8 @@ def _load() -> ctypes.CDLL:
     lib.mha_sublayer_fwd_static.argtypes = [vp] * 11 + [i32] * 9 + [vp, ctypes.c_float, i32, vp]
     lib.mha_fwd_path.restype = i32
     lib.mha_fwd_path.argtypes = [i32] * 8
+    lib.mha_fwd_path_ex.restype = i32
+    lib.mha_fwd_path_ex.argtypes = [i32] * 9
     lib.mha_status_string.restype = ctypes.c_char_p
     lib.mha_status_string.argtypes = [i32]
     lib.mha_debug_status.restype = i32
@@ -79,6 +83,10 @@ def mha_version() -> int:
 
 def mha_fwd_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype) -> int:
     return int(lib.mha_fwd_path(B, H, Lq, Lk, d_k, d_v, mask_kind, dtype))
+
+
+def mha_fwd_path_ex(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype) -> int:
+    return int(lib.mha_fwd_path_ex(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype))
 
 
 def _stream_handle(stream):
