@@ -8,7 +8,8 @@
 // R = group x Lq query rows -- the `group` query heads that share key/value
 // head g, Lq positions each, row r = (head within the group) * Lq + position;
 // R <= 16.  Persistent CTAs, one per SM, each take a contiguous range of
-// pairs holding an equal share of all key tiles (lengths read on the device);
+// pairs holding an equal share of the work (key tiles plus a fixed cost per
+// pair; lengths read on the device);
 // the K/V stream runs ahead across pair boundaries.
 //
 // With so few query rows, the usual orientation (query rows on the 128 TMEM
@@ -135,12 +136,17 @@ __device__ __forceinline__ int key_len(const Problem &p, int b) {
   return l < 0 ? 0 : (l > p.Lk ? p.Lk : l);
 }
 
-// This CTA's pairs [lo, hi).  Pair (b, g) = b * Hkv + g starts at tile
-// s = Hkv * (tiles of the batch elements before b) + g * tiles(b) of the
-// concatenation of all pairs' key tiles, T tiles in all; CTA c takes the pairs
-// whose start lies in [ceil(c T / G), ceil((c + 1) T / G)) -- contiguous
-// ranges whose tile counts differ by at most one pair's.  The whole warp
-// calls it and gets the same answer in every lane.
+// Cost of a pair in half-tile units: its key tiles plus a fixed 1.5 tiles
+// for the pair's own work (Q load, row sums, output), which costs about that
+// much when pairs are short.
+__device__ __forceinline__ int pair_cost(int tiles) { return 2 * tiles + 3; }
+
+// This CTA's pairs [lo, hi).  Pair (b, g) = b * Hkv + g starts at
+// s = Hkv * (cost of the batch elements' pairs before b) + g * cost(b) in the
+// concatenation of all pairs' costs, T in all; CTA c takes the pairs whose
+// start lies in [ceil(c T / G), ceil((c + 1) T / G)) -- contiguous ranges whose
+// costs differ by at most one pair's.  The whole warp calls it and gets the
+// same answer in every lane.
 __device__ void pair_range(const Problem &p, int lane, int &lo, int &hi) {
   const long long G = gridDim.x, c = blockIdx.x;
   const int npairs = p.B * p.Hkv;
@@ -152,7 +158,7 @@ __device__ void pair_range(const Problem &p, int lane, int &lo, int &hi) {
   long long total = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     const int b = b0 + lane;
-    const int t = b < p.B ? (key_len(p, b) + kBN - 1) / kBN : 0;
+    const int t = b < p.B ? pair_cost((key_len(p, b) + kBN - 1) / kBN) : 0;
     total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(t));
   }
   total *= p.Hkv;
@@ -163,8 +169,8 @@ __device__ void pair_range(const Problem &p, int lane, int &lo, int &hi) {
   long long carry = 0;  // s of the first pair of this chunk of batch elements
   for (int b0 = 0; b0 < p.B && !(found_lo && found_hi); b0 += 32) {
     const int b = b0 + lane;
-    const int t = b < p.B ? (key_len(p, b) + kBN - 1) / kBN : 0;
-    int inc = t;  // inclusive scan of the tile counts over the chunk
+    const int t = b < p.B ? pair_cost((key_len(p, b) + kBN - 1) / kBN) : 0;
+    int inc = t;  // inclusive scan of the pair costs over the chunk
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, inc, o);
@@ -175,7 +181,6 @@ __device__ void pair_range(const Problem &p, int lane, int &lo, int &hi) {
     auto first_g = [&](long long x) -> int {
       if (b >= p.B) return p.Hkv;
       if (s0 >= x) return 0;
-      if (t == 0) return p.Hkv;
       const long long g = (x - s0 + t - 1) / t;
       return g < p.Hkv ? static_cast<int>(g) : p.Hkv;
     };
