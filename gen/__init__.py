@@ -255,6 +255,18 @@ def make_inputs(spec: dict, seed: int = 0):
     return q, k, v, lens
 
 
+# The incoming gradient of the attention output for the backward pass: N(0, 1)
+# in the output's layout and dtype (a loss whose gradient is unit-variance noise).
+STREAM_DOUT = 14
+
+
+def make_dout(spec: dict, seed: int = 0) -> np.ndarray:
+    """dL/dout for a workload spec: the output's shape and layout, dtype spec["dtype"]."""
+    B, H, Lq, dv = spec["B"], spec["H"], spec["Lq"], spec["dv"]
+    shape = (B, Lq, H, dv) if spec.get("layout", "bhsd") == "bshd" else (B, H, Lq, dv)
+    return tensor(seed, STREAM_DOUT, shape, spec["dtype"])
+
+
 def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     """Exact widening of stored values to float64."""
     if dtype == "bf16":

@@ -13,6 +13,10 @@ Every function here is pinned by ``tests/test_oracle.py`` against values the
 pages print (the three-token worked example), closed forms, invariants and a
 50-digit brute force.
 
+``mha_bwd`` is the backward pass: the gradients of a loss through the
+attention, by the chain rule through the same steps (for training, as the
+pages describe it; ``mha_oracle.c`` states the formulas).
+
 ``linear`` and ``mha_sublayer`` add the steps on either side of the attention:
 the learned projections with their biases, the head split and concatenation,
 and the output projection (trishampatil.com, "Multi-Head Attention" and "The
@@ -66,6 +70,14 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_mha_bwd_f64.restype = ctypes.c_int
+            lib.oracle_mha_bwd_f64.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -145,6 +157,58 @@ def mha_fwd(q, k, v, *, mask_kind: int = 0, key_lengths=None, scale: float,
     if return_scores:
         res.append(s)
     return res[0] if len(res) == 1 else tuple(res)
+
+
+def mha_bwd(q, k, v, dout, *, mask_kind: int = 0, key_lengths=None, scale: float,
+            layout: str = "bhsd", units=None, rows=None, threads: int = 0):
+    """Gradients (dq, dk, dv) in float64 of L = sum(out * dout) through ``mha_fwd``.
+
+    Same shapes, layouts, dtypes and masks as ``mha_fwd``; ``dout`` has the
+    output's shape and the inputs' dtype.  The steps are the chain rule through
+    the forward (see ``mha_oracle.c``).  ``units``: optional logical (batch
+    element, key/value head) indices b * Hkv + g to compute (others stay 0);
+    ``rows``: optional (lo, hi) range of query rows taken in each unit (a
+    timing sample; gradients are then partial sums).
+    """
+    q, k, v, dout = (np.ascontiguousarray(a) for a in (q, k, v, dout))
+    if not (q.dtype == k.dtype == v.dtype == dout.dtype) or q.dtype not in _IN_CODES:
+        raise TypeError("q, k, v, dout must share one of float64, float32, uint16(bf16)")
+    if layout not in ("bhsd", "bshd"):
+        raise ValueError("layout must be 'bhsd' or 'bshd'")
+    bshd = layout == "bshd"
+    if bshd:
+        B, Lq, H, dk = q.shape
+        Bk, Lk, Hkv, dk2 = k.shape
+        Bv, Lk2, Hv, dv = v.shape
+        oshape = (B, Lq, H, dv)
+    else:
+        B, H, Lq, dk = q.shape
+        Bk, Hkv, Lk, dk2 = k.shape
+        Bv, Hv, Lk2, dv = v.shape
+        oshape = (B, H, Lq, dv)
+    if (Bk, dk2) != (B, dk) or (Bv, Hv, Lk2) != (B, Hkv, Lk) or dout.shape != oshape:
+        raise ValueError("shape mismatch")
+    if Hkv <= 0 and H > 0 or (Hkv > 0 and H % Hkv):
+        raise ValueError("key/value heads must divide query heads")
+    kl = None
+    if key_lengths is not None:
+        kl = np.ascontiguousarray(key_lengths, dtype=np.int32)
+        if kl.shape != (B,):
+            raise ValueError("key_lengths must have shape [B]")
+    units_a = None if units is None else np.ascontiguousarray(units, dtype=np.int64)
+    nunits = B * Hkv if units_a is None else units_a.shape[0]
+    i_lo, i_hi = (0, Lq) if rows is None else (int(rows[0]), int(rows[1]))
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dkk = np.zeros(k.shape, dtype=np.float64)
+    dvv = np.zeros(v.shape, dtype=np.float64)
+    rc = _load().oracle_mha_bwd_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _IN_CODES[q.dtype], B, H,
+        max(Hkv, 1) if H == 0 else Hkv, Lq, Lk, dk, dv, 1 if bshd else 0, int(mask_kind),
+        _ptr(kl), float(scale), _ptr(units_a), nunits, i_lo, i_hi, _ptr(dq), _ptr(dkk), _ptr(dvv),
+        int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (rc=%d)" % rc)
+    return dq, dkk, dvv
 
 
 def _f64(a):

@@ -1,5 +1,6 @@
 /*
- * fp64 CPU oracle for multi-head scaled dot-product attention (forward).
+ * fp64 CPU oracle for multi-head scaled dot-product attention (forward and
+ * backward).
  *
  * TEST INFRASTRUCTURE ONLY.  This file is compiled into a host library that
  * the tests, the package's smoke check and the bench's CPU-baseline leg load to
@@ -209,4 +210,158 @@ int oracle_mha_rows_f64(const void *q, const void *k, const void *v, int in_dtyp
                         double *out, double *weights, double *scores, int nthreads) {
   return oracle_mha_rows_ex_f64(q, k, v, in_dtype, B, H, H, Lq, Lk, dk, dv, 0, mask_kind,
                                 key_lengths, scale, rows, nrows, out, weights, scores, nthreads);
+}
+
+/*
+ * Backward pass: the gradients of a scalar loss L through the forward above,
+ * for training (trishampatil.com, "Training (Teacher Forcing + Masking)": the
+ * whole target sequence goes through one parallel forward pass under the
+ * causal mask and the gradients flow back through every layer at once;
+ * aicomputerinstitute.com, "The core idea: attention as a lookup, not a
+ * summary": the gradient through a saturated softmax vanishes, which is why
+ * the scores are scaled).  The pages print no backward formulas; these are
+ * the derivatives of steps 4-6 as written, by the chain rule.  Given
+ * dout = dL/dout, for each computed row i of query head h (key/value head g):
+ *
+ *   g_j = sum_c dout[i,c] v[j,c]              dL/dw_j            (step 6)
+ *   D   = sum_{j in A_i} w_j g_j
+ *   t_j = w_j (g_j - D)                       dL/ds_j, from the softmax
+ *                                              Jacobian dw_j/ds_l =
+ *                                              w_j (delta_jl - w_l) (step 5)
+ *   dq[i,c]  = scale sum_{j in A_i} t_j k[j,c]                     (step 4)
+ *   dk[j,c] += scale t_j q[i,c]
+ *   dv[j,c] += w_j dout[i,c]                                       (step 6)
+ *
+ * Rows whose output is fixed at +0 (steps 1 and 3) depend on no input: they
+ * contribute nothing and their dq is 0.  Keys outside A_i get nothing from
+ * row i.  With shared key/value heads, dk and dv of head g sum over the query
+ * heads that read g.  Sums run in index order (heads, then rows, then keys),
+ * in IEEE double.
+ *
+ * Work is split by (batch element, key/value head) units, so each unit's dk
+ * and dv are written by one thread.  units / nunits: the logical units
+ * b * Hkv + g to compute (NULL: all B * Hkv); [i_lo, i_hi): the query rows
+ * taken in each (a timing sample; 0, Lq for the whole pass).  dq, dk, dv are
+ * full tensors in the inputs' layout; only the listed units' parts are
+ * written.  Returns 0, or 1 on an invalid argument.
+ */
+int oracle_mha_bwd_f64(const void *q, const void *k, const void *v, const void *dout,
+                       int in_dtype, int B, int H, int Hkv, int Lq, int Lk, int dk, int dv,
+                       int layout, int mask_kind, const int32_t *key_lengths, double scale,
+                       const int64_t *units, int64_t nunits, int i_lo, int i_hi, double *dq,
+                       double *dk_out, double *dv_out, int nthreads) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || dk < 0 || dv < 0) return 1;
+  if (Hkv <= 0 ? H > 0 : (H % Hkv) != 0) return 1;
+  if (layout != 0 && layout != 1) return 1;
+  if (in_dtype < ORACLE_IN_F64 || in_dtype > ORACLE_IN_BF16) return 1;
+  if (mask_kind & ~(ORACLE_CAUSAL | ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING | ORACLE_CAUSAL_TAIL))
+    return 1;
+  if ((mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)) && Lq != Lk) return 1;
+  if ((mask_kind & ORACLE_CAUSAL_TAIL) && (mask_kind & (ORACLE_CAUSAL | ORACLE_QUERY_PADDING)))
+    return 1;
+  if ((mask_kind & (ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) && key_lengths == NULL && B > 0)
+    return 1;
+  if (i_lo < 0 || i_hi > Lq || i_lo > i_hi) return 1;
+  const int64_t total_units = Hkv > 0 ? (int64_t)B * Hkv : 0;
+  if (units == NULL && nunits != total_units) return 1;
+  if (nunits < 0) return 1;
+  for (int64_t u = 0; units != NULL && u < nunits; ++u)
+    if (units[u] < 0 || units[u] >= total_units) return 1;
+  if (nthreads <= 0) nthreads = oracle_max_threads();
+  const int group = Hkv > 0 ? H / Hkv : 0;
+
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+  {
+    const size_t n = (size_t)(Lk > 0 ? Lk : 1);
+    double *w = (double *)malloc(sizeof(double) * n);
+    double *g = (double *)malloc(sizeof(double) * n);
+    char *allowed = (char *)malloc(n);
+    if (w == NULL || g == NULL || allowed == NULL) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t u = 0; u < nunits; ++u) {
+      if (w == NULL || g == NULL || allowed == NULL) continue;
+      const int64_t unit = units ? units[u] : u;
+      const int b = (int)(unit / Hkv), hk = (int)(unit % Hkv);
+      /* this unit's gradients start at zero */
+      for (int j = 0; j < Lk; ++j) {
+        for (int c = 0; c < dk; ++c) dk_out[offset(layout, b, hk, j, c, Hkv, Lk, dk)] = 0.0;
+        for (int c = 0; c < dv; ++c) dv_out[offset(layout, b, hk, j, c, Hkv, Lk, dv)] = 0.0;
+      }
+      for (int h = hk * group; h < (hk + 1) * group; ++h)
+        for (int i = 0; i < Lq; ++i)
+          for (int c = 0; c < dk; ++c) dq[offset(layout, b, h, i, c, H, Lq, dk)] = 0.0;
+      int len_b = Lk;
+      if (mask_kind & (ORACLE_KEY_PADDING | ORACLE_QUERY_PADDING)) {
+        int32_t l = key_lengths[b];
+        len_b = l < 0 ? 0 : (l > Lk ? Lk : (int)l);
+      }
+      for (int h = hk * group; h < (hk + 1) * group; ++h) {
+        for (int i = i_lo; i < i_hi; ++i) {
+          /* steps 1-3: rows whose output is fixed contribute nothing */
+          if ((mask_kind & ORACLE_QUERY_PADDING) && i >= len_b) continue;
+          int n_allowed = 0;
+          for (int j = 0; j < Lk; ++j) {
+            int ok = 1;
+            if ((mask_kind & ORACLE_CAUSAL) && j > i) ok = 0;
+            if ((mask_kind & ORACLE_KEY_PADDING) && j >= len_b) ok = 0;
+            if ((mask_kind & ORACLE_CAUSAL_TAIL) && j > len_b - Lq + i) ok = 0;
+            allowed[j] = (char)ok;
+            n_allowed += ok;
+          }
+          if (n_allowed == 0) continue;
+          /* steps 4-5 again: the weights w_j */
+          double m = -INFINITY;
+          for (int j = 0; j < Lk; ++j) {
+            if (!allowed[j]) continue;
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c)
+              dot += widen(q, in_dtype, offset(layout, b, h, i, c, H, Lq, dk)) *
+                     widen(k, in_dtype, offset(layout, b, hk, j, c, Hkv, Lk, dk));
+            w[j] = scale * dot;
+            if (w[j] > m) m = w[j];
+          }
+          double denom = 0.0;
+          for (int j = 0; j < Lk; ++j)
+            if (allowed[j]) {
+              w[j] = exp(w[j] - m);
+              denom += w[j];
+            }
+          for (int j = 0; j < Lk; ++j) w[j] = allowed[j] ? w[j] / denom : 0.0;
+          /* g_j and D */
+          double D = 0.0;
+          for (int j = 0; j < Lk; ++j) {
+            if (!allowed[j]) continue;
+            double gj = 0.0;
+            for (int c = 0; c < dv; ++c)
+              gj += widen(dout, in_dtype, offset(layout, b, h, i, c, H, Lq, dv)) *
+                    widen(v, in_dtype, offset(layout, b, hk, j, c, Hkv, Lk, dv));
+            g[j] = gj;
+            D += w[j] * gj;
+          }
+          /* t_j, then the three gradients */
+          for (int j = 0; j < Lk; ++j) {
+            if (!allowed[j]) continue;
+            const double t = w[j] * (g[j] - D);
+            for (int c = 0; c < dk; ++c) {
+              dq[offset(layout, b, h, i, c, H, Lq, dk)] +=
+                  scale * t * widen(k, in_dtype, offset(layout, b, hk, j, c, Hkv, Lk, dk));
+              dk_out[offset(layout, b, hk, j, c, Hkv, Lk, dk)] +=
+                  scale * t * widen(q, in_dtype, offset(layout, b, h, i, c, H, Lq, dk));
+            }
+            for (int c = 0; c < dv; ++c)
+              dv_out[offset(layout, b, hk, j, c, Hkv, Lk, dv)] +=
+                  w[j] * widen(dout, in_dtype, offset(layout, b, h, i, c, H, Lq, dv));
+          }
+        }
+      }
+    }
+    free(w);
+    free(g);
+    free(allowed);
+  }
+  return bad ? 1 : 0;
 }
