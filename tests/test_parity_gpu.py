@@ -183,6 +183,9 @@ def test_other_scales(scale):
     check_case(spec(2, 2, 96, 128, 64), scale=scale, seed=8)
     check_case(spec(1, 2, 300, 300, 128, mask=C), scale=scale, seed=8)
     check_case(spec(2, 2, 40, 40, 64, "f32", mask=C), scale=scale, seed=8)
+    # masked rows on the packed kernel (a zero scale must not meet a masked -inf)
+    check_case(spec(2, 2, 128, 128, 64, mask=C), scale=scale, seed=8)
+    check_case(spec(3, 2, 64, 64, 64, mask=KP | QP, len_range=(0, 64)), scale=scale, seed=8)
 
 
 def test_deterministic():

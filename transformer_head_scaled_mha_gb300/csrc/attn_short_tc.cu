@@ -424,9 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tmem = tmem + lane_base + w * 128;  // S; P over its first 64
     const uint32_t o_tmem = s_tmem + 64;                 // O
-    // a negative scale is applied as |scale| to sign-flipped scores
+    // a negative scale is applied as |scale| to sign-flipped scores.  Scores
+    // are scaled after masking, so a zero scale would turn a masked -inf into
+    // NaN; it is applied as the smallest normal float instead: every finite
+    // score then flushes to 0 (exactly the zero-scale scores) and -inf stays
     const uint32_t sgn = p.scale_log2 < 0.f ? 0x80000000u : 0u;
-    const float sl = fabsf(p.scale_log2);
+    const float sl = p.scale_log2 != 0.f ? fabsf(p.scale_log2) : 1.17549435e-38f;
     const int rq_shift = __ffs(g.Rq) - 1;
     // byte strides of a query row and a head (below 2^31: this path takes
     // Lq <= 128 and H <= 2^24)
