@@ -238,6 +238,52 @@ int mha_sublayer_fwd_static(const void *x, const void *mem, void *out,
                             int mask_kind, const int32_t *key_lengths, float scale, int dtype,
                             void *stream);
 
+/* Bytes of device workspace mha_bwd needs: two fp32 values per query row
+   (the row's log-sum-exp and D = dout . out), 256-byte aligned parts; 0 for
+   an empty problem. */
+size_t mha_bwd_workspace_size(int B, int H, int Lq);
+
+/*
+ * mha_bwd -- gradients of a loss through the attention, for training,
+ * asynchronous on `stream`.
+ *
+ * The pages train the model end to end, every position of the target
+ * sequence at once under the causal mask, with the gradients flowing back
+ * through every layer (trishampatil.com, "Training (Teacher Forcing +
+ * Masking)"); they print no backward formulas.  These are the derivatives of
+ * the forward of mha_fwd_ex by the chain rule: with w_ij the softmax weights
+ * of the allowed keys,
+ *
+ *     dP_ij = dout_i . v_j,   D_i = dout_i . out_i,   dS_ij = w_ij (dP_ij - D_i)
+ *     dq_i = scale sum_j dS_ij k_j,   dk_j = scale sum_i dS_ij q_i,
+ *     dv_j = sum_i w_ij dout_i
+ *
+ * (with shared key/value heads, dk and dv of head g sum over the query heads
+ * that read g).  Rows whose output is fixed at +0 (query padding, no allowed
+ * key) have dq = 0 and contribute nothing; keys no row may read get dk = dv = 0.
+ *
+ * q, k, v, layout, mask_kind, key_lengths, scale, dtype, H_kv: as for
+ *                      mha_fwd_ex, the values of the forward call
+ * out                  that call's output (for D_i)
+ * dout                 dL/dout, out's shape and layout
+ * dq, dk, dv           results: the shapes and layout of q, k and v, dtype
+ *                      `dtype`; overwritten entirely
+ * workspace            device memory of at least mha_bwd_workspace_size(B, H,
+ *                      Lq) bytes, 256-byte aligned, caller-owned; its contents
+ *                      need not be initialised and are scratch afterwards
+ *
+ * All pointers are device pointers, 16-byte aligned; the gradients overlap no
+ * input, each other, the workspace or key_lengths.  Calls that share a
+ * workspace must not overlap in time.  Shapes, dtypes and masks supported
+ * and the errors returned are those of mha_fwd_ex; MHA_ERR_INVALID_ARGUMENT
+ * also for a missing or too small workspace.  The weights are recomputed
+ * from the inputs (nothing is kept from the forward call but `out`).
+ */
+int mha_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+            void *dq, void *dk, void *dv, int B, int H, int H_kv, int Lq, int Lk, int d_k,
+            int d_v, int layout, int mask_kind, const int32_t *key_lengths, float scale,
+            int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed
    short-sequence tensor-core kernel (Lq, Lk <= 128), 3 = long-sequence

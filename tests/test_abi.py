@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
         ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-         "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_fwd_path_ex",
+         "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
+         "mha_fwd_path", "mha_fwd_path_ex",
          "mha_status_string", "mha_debug_status",
          "mha_version"])
 

@@ -1,8 +1,9 @@
 // Attention of a few query rows against a long key/value cache on the
 // tcgen05 tensor cores (bf16, d in {64, 128}): the decoding step of
 // generation, where each new token attends to every cached key of its
-// sequence ("Attention Is All You Need", section 3.2.1 equation (1), with the
-// decoder's masking of section 3.2.3 applied to the last Lq positions).
+// sequence (trishampatil.com, "Scaled Dot-Product Attention: Step by Step",
+// with the decoder's causal masking of alexdo.xyz, "Decoder block", applied to
+// the last Lq positions as in "How predictions are generated").
 //
 // Work unit: one (batch element b, key/value head g) pair and its
 // R = group x Lq query rows -- the `group` query heads that share key/value

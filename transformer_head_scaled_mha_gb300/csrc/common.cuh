@@ -75,6 +75,17 @@ struct DecodeMaps {
 cudaError_t launch_decode_tc(const DecodeMaps &maps, const Problem &p, void *out, int num_sms,
                              cudaStream_t stream);
 
+// backward pass: tensors in the forward's layout and dtype; lse and dsum
+// (D = dout . out) are fp32 per query row [B * H * Lq], lse in log2 units of
+// the scaled scores (+inf for a row that attends to nothing)
+struct BwdArgs {
+  const void *q, *k, *v, *out, *dout;
+  void *dq, *dk, *dv;
+  float *lse, *dsum;
+  float scale;  // dq and dk carry this factor
+};
+cudaError_t launch_bwd_simt(const BwdArgs &a, const Problem &p, bool bf16, cudaStream_t stream);
+
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
 
 // y = x W + b (bf16), 128-byte swizzle.  Slab tiling (K, N multiples of 64):

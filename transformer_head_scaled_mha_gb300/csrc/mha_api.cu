@@ -287,6 +287,105 @@ extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, i
 
 namespace {
 
+constexpr size_t kBwdAlign = 256;
+size_t bwd_round(size_t n) { return (n + kBwdAlign - 1) / kBwdAlign * kBwdAlign; }
+
+}  // namespace
+
+extern "C" size_t mha_bwd_workspace_size(int B, int H, int Lq) {
+  if (B <= 0 || H <= 0 || Lq <= 0) return 0;
+  return 2 * bwd_round(static_cast<size_t>(B) * H * Lq * sizeof(float));
+}
+
+extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *out,
+                       const void *dout, void *dq, void *dk, void *dv, int B, int H, int H_kv,
+                       int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
+                       const int32_t *key_lengths, float scale, int dtype, void *workspace,
+                       size_t workspace_bytes, void *stream_) {
+  const int path = select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
+  if (path < 0) return -path;
+  if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
+  const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
+  if (padded && key_lengths == nullptr && B > 0) return MHA_ERR_INVALID_ARGUMENT;
+  const size_t esz = dtype == MHA_DTYPE_F32 ? 4 : 2;
+  const size_t nq = static_cast<size_t>(B) * H * Lq * d_k * esz;
+  const size_t nk = static_cast<size_t>(B) * H_kv * Lk * d_k * esz;
+  const size_t nv = static_cast<size_t>(B) * H_kv * Lk * d_v * esz;
+  const size_t no = static_cast<size_t>(B) * H * Lq * d_v * esz;
+  const size_t nws = mha_bwd_workspace_size(B, H, Lq);
+  if (nq == 0 && nk == 0) return MHA_OK;
+  const void *ins[5] = {q, k, v, out, dout};
+  const size_t in_n[5] = {nq, nk, nv, no, no};
+  void *outs[3] = {dq, dk, dv};
+  const size_t out_n[3] = {nq, nk, nv};
+  for (int i = 0; i < 5; ++i)
+    if (in_n[i] > 0 && (ins[i] == nullptr || reinterpret_cast<uintptr_t>(ins[i]) % 16 != 0))
+      return MHA_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < 3; ++i)
+    if (out_n[i] > 0 && (outs[i] == nullptr || reinterpret_cast<uintptr_t>(outs[i]) % 16 != 0))
+      return MHA_ERR_INVALID_ARGUMENT;
+  if (nws > 0 && (workspace == nullptr || workspace_bytes < nws ||
+                  reinterpret_cast<uintptr_t>(workspace) % kBwdAlign != 0))
+    return MHA_ERR_INVALID_ARGUMENT;
+  // the gradients overlap no input, each other, the workspace or the lengths
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 5; ++i)
+      if (overlaps(outs[o], out_n[o], ins[i], in_n[i])) return MHA_ERR_INVALID_ARGUMENT;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (overlaps(outs[o], out_n[o], outs[o2], out_n[o2])) return MHA_ERR_INVALID_ARGUMENT;
+    if (overlaps(outs[o], out_n[o], workspace, nws)) return MHA_ERR_INVALID_ARGUMENT;
+    if (padded && overlaps(outs[o], out_n[o], key_lengths, sizeof(int32_t) * B))
+      return MHA_ERR_INVALID_ARGUMENT;
+  }
+  for (int i = 0; i < 5; ++i)
+    if (overlaps(workspace, nws, ins[i], in_n[i])) return MHA_ERR_INVALID_ARGUMENT;
+  if (padded && overlaps(workspace, nws, key_lengths, sizeof(int32_t) * B))
+    return MHA_ERR_INVALID_ARGUMENT;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
+  Problem p;
+  p.B = B;
+  p.H = H;
+  p.Hkv = H_kv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.dk = d_k;
+  p.dv = d_v;
+  p.layout = layout;
+  p.mask = mask_kind;
+  p.key_lengths = padded ? key_lengths : nullptr;
+  p.scale_log2 = scale * kLog2e;
+  p.status = status_ptr(dev);
+  if (p.status == nullptr) return MHA_ERR_CUDA;
+  cudaError_t err = cudaSuccess;
+  if (Lk == 0 || nq == 0) {
+    // no keys: nothing reads q, k or v; every gradient is zero
+    for (int i = 0; i < 3 && err == cudaSuccess; ++i)
+      if (out_n[i] > 0) err = launch_zero_fill(outs[i], out_n[i], stream);
+    return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.lse = reinterpret_cast<float *>(ws);
+  a.dsum = reinterpret_cast<float *>(ws + nws / 2);
+  a.scale = scale;
+  err = launch_bwd_simt(a, p, dtype == MHA_DTYPE_BF16, stream);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+namespace {
+
 // Validation shared by mha_linear_fwd and the sublayer's projections.
 int check_linear(const void *x, const void *w, const void *b, const void *y, long long M, int K,
                  int N, int dtype) {

@@ -21,7 +21,8 @@ PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fi
 MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 
 EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
-            "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_fwd_path", "mha_fwd_path_ex",
+            "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
+            "mha_fwd_path", "mha_fwd_path_ex",
             "mha_status_string", "mha_debug_status", "mha_version")
 
 
@@ -53,6 +54,11 @@ def _load() -> ctypes.CDLL:
                                                             ctypes.c_size_t, vp]
     lib.mha_sublayer_fwd_static.restype = i32
     lib.mha_sublayer_fwd_static.argtypes = [vp] * 11 + [i32] * 9 + [vp, ctypes.c_float, i32, vp]
+    lib.mha_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.mha_bwd_workspace_size.argtypes = [i32] * 3
+    lib.mha_bwd.restype = i32
+    lib.mha_bwd.argtypes = [vp] * 8 + [i32] * 9 + [vp, ctypes.c_float, i32, vp, ctypes.c_size_t,
+                                                    vp]
     lib.mha_fwd_path.restype = i32
     lib.mha_fwd_path.argtypes = [i32] * 8
     lib.mha_fwd_path_ex.restype = i32
@@ -184,6 +190,44 @@ def mha_fwd_ex(q, k, v, out=None, *, layout: str = "bhsd", mask_kind: int = 0,
     if st != MHA_OK:
         raise MhaError(st, "mha_fwd_ex")
     return out
+
+
+def mha_bwd_workspace_size(B, H, Lq) -> int:
+    return int(lib.mha_bwd_workspace_size(B, H, Lq))
+
+
+def mha_bwd(q, k, v, out, dout, *, layout: str = "bhsd", mask_kind: int = 0, key_lengths=None,
+            scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of a loss through mha_fwd_ex, given its output
+    ``out`` and the incoming gradient ``dout`` (out's shape).  Same layouts,
+    shared key/value heads, masks and scale as mha_fwd_ex.  ``workspace``: a
+    uint8 CUDA tensor of at least mha_bwd_workspace_size(B, H, Lq) bytes, or
+    None to allocate one."""
+    import torch
+    _, (B, H, Hkv, Lq, Lk, dk_, dv_), kl_ptr, scale, dtype = _marshal(q, k, v, out, key_lengths,
+                                                                      scale, layout)
+    if dout.shape != out.shape or dout.dtype != q.dtype or not dout.is_contiguous() or \
+            dout.device != q.device:
+        raise ValueError("dout must be a contiguous tensor like out")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, g, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if g.shape != ref.shape or g.dtype != ref.dtype or not g.is_contiguous() or \
+                g.device != ref.device:
+            raise ValueError("%s must be a contiguous tensor like its input" % name)
+    n = mha_bwd_workspace_size(B, H, Lq)
+    if workspace is None:
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.mha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv,
+                         Lq, Lk, dk_, dv_, MHA_LAYOUT_BSHD if layout == "bshd" else MHA_LAYOUT_BHSD,
+                         int(mask_kind), kl_ptr, scale, dtype, workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_bwd")
+    return dq, dk, dv
 
 
 def _bf16_cuda(name, t, ndim=None):
