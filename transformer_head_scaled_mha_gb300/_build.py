@@ -17,7 +17,7 @@ LIB = os.path.join(BUILD, "libmha.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["mha_api.cu", "attn_f32_simt.cu", "attn_short_tc.cu", "attn_long_tc.cu", "attn_decode_tc.cu",
-           "attn_bwd_simt.cu", "linear_tc.cu"]
+           "attn_bwd_simt.cu", "attn_bwd_tc.cu", "linear_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

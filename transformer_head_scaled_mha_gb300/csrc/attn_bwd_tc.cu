@@ -1,0 +1,781 @@
+// Backward pass of scaled dot-product attention on the tcgen05 tensor cores
+// (bf16, d in {64, 128}): the gradients dq, dk, dv of a loss through
+// softmax(q k^T * scale) v, for training (trishampatil.com, "Training (Teacher
+// Forcing + Masking)": the whole target sequence goes through one parallel
+// forward pass under the causal mask and the gradients flow back through
+// every layer at once).  By the chain rule through the forward's steps, with
+// w_ij the softmax weights and dout the incoming gradient:
+//
+//   dP = dout V^T,  D_i = dout_i . out_i,  dS = w * (dP - D)  (row-wise D)
+//   dq = scale dS K,  dk = scale dS^T Q,  dv = w^T dout
+//
+// Three kernels, no atomics, every product on the tensor cores with fp32
+// accumulators in TMEM; the weights are recomputed from the per-row
+// log-sum-exp (log2 units), w_ij = 2^(s_ij * scale * log2(e) - lse_i):
+//
+//   stats  per 128 query rows: S = Q K^T tile by tile, the running max and
+//          sum (moved lazily, as in the forward), lse; D from out and dout
+//          (+inf lse for a row that attends to nothing: all its weights 0)
+//   dq     per 128 query rows: S = Q K_j^T and dP = dout V_j^T, then the
+//          softmax warpgroup (thread = row) forms dS (bf16) over dP in TMEM,
+//          and dQ += dS K_j reads it from TMEM as the A operand.  S is
+//          double-buffered, so S_{j+1} overlaps the softmax of tile j
+//   dkdv   per 128 keys of a key/value head, over the query tiles of every
+//          query head of the group: S^T = K Q^T and dP^T = V dout^T (keys on
+//          the lanes), then thread = key forms w^T and dS^T (bf16) over them
+//          in TMEM, and dV += w^T dout, dK += dS^T Q read them as A operands
+//
+// Warp roles (192 threads): warps 0-3 softmax (thread r = TMEM lane r),
+// warp 4 TMA producer, warp 5 TMEM owner and MMA issuer.  Operand tiles are
+// [128 rows x 64] 128B-swizzled blocks written by TMA; the row-major K, V,
+// Q and dout tiles serve as K-major operands of the score products and as
+// MN-major B operands of the gradient products.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kWg = 128;   // softmax threads
+constexpr int kT = 128;    // rows of every tile (queries or keys)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxSlots = 8;
+
+template <int D>
+struct Geo {
+  static constexpr int kBlk = 128 * 128;             // one [128 x 64] swizzle block
+  static constexpr int kTile = (D / 64) * kBlk;      // one [128 x D] tile
+};
+
+__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity))
+    if (global_timer_ns() - t0 > 100000000ull) return false;
+  return true;
+}
+
+__device__ __forceinline__ int clamp_len(const Problem &p, int b) {
+  if (!(p.mask & (kMaskKeyPadding | kMaskQueryPadding))) return p.Lk;
+  const int l = p.key_lengths[b];
+  return l < 0 ? 0 : (l > p.Lk ? p.Lk : l);
+}
+
+// keys j < row_limit(i) may be read by query row i (0: none)
+__device__ __forceinline__ int row_limit(const Problem &p, int len, int i) {
+  if ((p.mask & kMaskQueryPadding) && i >= len) return 0;
+  int jmax = p.Lk;
+  if (p.mask & kMaskKeyPadding) jmax = min(jmax, len);
+  if (p.mask & kMaskCausal) jmax = min(jmax, i + 1);
+  if (p.mask & kMaskCausalTail) jmax = max(min(jmax, len - p.Lq + i + 1), 0);
+  return jmax;
+}
+
+// key tiles [0, n) that the query rows [q0, q0 + 128) of one head can read
+__device__ __forceinline__ int key_tiles(const Problem &p, int len, int q0) {
+  if ((p.mask & kMaskQueryPadding) && q0 >= len) return 0;
+  const int q1 = min(q0 + kT, p.Lq);  // one past the tile's last row
+  int kv_end = p.Lk;
+  if (p.mask & kMaskKeyPadding) kv_end = min(kv_end, len);
+  if (p.mask & kMaskCausal) kv_end = min(kv_end, q1);
+  if (p.mask & kMaskCausalTail) kv_end = min(kv_end, len - p.Lq + q1);
+  return kv_end > 0 ? (kv_end + kT - 1) / kT : 0;
+}
+
+// element offset of row (b, head, pos) in a tensor of `heads` heads, `len`
+// positions and d columns
+__device__ __forceinline__ size_t row_at(int layout, int b, int head, int pos, int heads, int len,
+                                         int d) {
+  const size_t r = layout == kLayoutBHSD ? (static_cast<size_t>(b) * heads + head) * len + pos
+                                         : (static_cast<size_t>(b) * len + pos) * heads + head;
+  return r * d;
+}
+
+// 32 fp32 values * f -> bf16, 64 bytes at dst (16-byte aligned)
+__device__ __forceinline__ void store_row32(uint16_t *dst, const uint32_t (&v)[32], float f) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * f, __uint_as_float(v[8 * q + 1]) * f);
+    w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * f, __uint_as_float(v[8 * q + 3]) * f);
+    w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * f, __uint_as_float(v[8 * q + 5]) * f);
+    w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * f, __uint_as_float(v[8 * q + 7]) * f);
+    st_global_v4(dst + 8 * q, w);
+  }
+}
+__device__ __forceinline__ void store_zero32(uint16_t *dst) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) st_global_v4(dst + 8 * q, make_uint4(0u, 0u, 0u, 0u));
+}
+
+// D/16 steps of a [128 x D] x [128 x D]^T product, both operands K-major
+template <int D>
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t sa, uint32_t sb,
+                                           uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * Geo<D>::kBlk + (kk & 3) * 32;
+    tc_mma_ss(d_tmem, smem_desc_sw128(sa + off, 16, 1024), smem_desc_sw128(sb + off, 16, 1024),
+              idesc, kk > 0 ? 1u : 0u);
+  }
+}
+// 8 steps of A[128 x 128 bf16 in TMEM] x B[128 rows x D, MN-major smem]
+template <int D>
+__device__ __forceinline__ void mma_grad(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kT / 16; ++kk)
+    tc_mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(sb + kk * 16 * 128, Geo<D>::kBlk, 1024),
+              idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ============================================================================
+// stats: lse and D per query row
+// ============================================================================
+template <int D>
+struct StatsCfg {
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(1 + kSlots) * Geo<D>::kTile + 512;
+};
+struct StatsBars {
+  uint64_t q_full;
+  uint64_t k_full[kMaxSlots], k_empty[kMaxSlots];
+  uint64_t s_full[2], s_free[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_stats_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
+  using C = StatsCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *q_smem = smem;
+  uint8_t *k_smem = q_smem + Geo<D>::kTile;
+  StatsBars *bars = reinterpret_cast<StatsBars *>(k_smem + C::kSlots * Geo<D>::kTile);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int q0 = static_cast<int>(blockIdx.x / BH) * kT;
+  const int b = bh / p.H, h = bh % p.H, hk = h / (p.H / p.Hkv);
+  const int len = clamp_len(p, b);
+  const int nt = key_tiles(p, len, q0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], kWg);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int issued = 0;
+  uint64_t *last_commit = nullptr;
+  uint32_t last_parity = 0;
+
+  if (warp == 4) {
+    if (lane == 0 && nt > 0) {
+      mbar_arrive_expect_tx(&bars->q_full, Geo<D>::kTile);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d(q_smem + blk * Geo<D>::kBlk, &maps.q, &bars->q_full, blk * 64, q0, h, b);
+      for (int j = 0; j < nt; ++j) {
+        const int s = j % C::kSlots, r = j / C::kSlots;
+        if (!mbar_wait(&bars->k_empty[s], (r & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], Geo<D>::kTile);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(k_smem + s * Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.k, &bars->k_full[s],
+                      blk * 64, j * kT, hk, b);
+        issued = j + 1;
+      }
+    }
+  } else if (warp == 5) {
+    const uint32_t idesc = idesc_bf16_f32(128, kT, 0);
+    bool ok = nt == 0 || mbar_wait(&bars->q_full, 0, abort_flag);
+    for (int j = 0; ok && j < nt; ++j) {
+      const int s = j % C::kSlots, r = j / C::kSlots;
+      if (!(ok = mbar_wait(&bars->k_full[s], r & 1, abort_flag))) break;
+      // S buffer j % 2 held S_{j-2}: the softmax has read it
+      if (j >= 2 && !(ok = mbar_wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        mma_scores<D>(tmem + (j & 1) * kT, smem_addr(q_smem),
+                      smem_addr(k_smem + s * Geo<D>::kTile), idesc);
+        tc_commit(&bars->s_full[j & 1]);
+        tc_commit(&bars->k_empty[s]);
+      }
+      __syncwarp();
+      last_commit = &bars->k_empty[s];
+      last_parity = r & 1;
+    }
+  } else {
+    const int r = threadIdx.x;  // tile row = TMEM lane
+    const int i = q0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int jmax = i < p.Lq ? row_limit(p, len, i) : 0;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + (j & 1) * kT + ch * 32, sr[ch]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[j & 1]);
+      const int lim = min(max(jmax - j * kT, 0), kT);
+      const bool need_mask = __any_sync(0xffffffffu, lim < kT);
+      const float mt = scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
+      if (mt > m + kRescaleThreshold) {
+        if (m != -INFINITY) l *= ex2_approx(m - mt);
+        m = mt;
+      }
+      l += exp2_sum128(sr, m, m != -INFINITY);
+    }
+    if (ok && i < p.Lq) {
+      const size_t row = (static_cast<size_t>(b) * p.H + h) * p.Lq + i;
+      a.lse[row] = l > 0.f ? m + __log2f(l) : INFINITY;
+      const uint16_t *o = static_cast<const uint16_t *>(a.out) +
+                          row_at(p.layout, b, h, i, p.H, p.Lq, D);
+      const uint16_t *g = static_cast<const uint16_t *>(a.dout) +
+                          row_at(p.layout, b, h, i, p.H, p.Lq, D);
+      float dsum = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < D; c += 8) {
+        const uint4 ov = *reinterpret_cast<const uint4 *>(o + c);
+        const uint4 gv = *reinterpret_cast<const uint4 *>(g + c);
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          dsum = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), dsum);
+          dsum = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u),
+                      dsum);
+        }
+      }
+      a.dsum[row] = dsum;
+    }
+  }
+
+  if (*abort_flag && warp == 4 && lane == 0) {
+    for (int idx = issued - C::kSlots; idx < issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->k_full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    if (nt > 0) (void)wait_teardown(&bars->q_full, 0);
+  }
+  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
+    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// dq: per 128 query rows, over the key tiles
+// ============================================================================
+template <int D>
+struct DqCfg {
+  static constexpr int kSlots = D == 128 ? 2 : 4;  // ring of (K, V) tile pairs
+  static constexpr size_t kSmem =
+      1024 + static_cast<size_t>(2 + 2 * kSlots) * Geo<D>::kTile + 512;
+  // TMEM: S0, S1, dP (dS bf16 over its first 64 columns), dQ
+  static constexpr uint32_t kS = 0, kDp = 256, kDq = 384;
+};
+struct DqBars {
+  uint64_t qdo_full;
+  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
+  uint64_t sdp_full;  // S_j and dP_j in TMEM
+  uint64_t ds_full;   // dS_j in TMEM (softmax threads)
+  uint64_t dq_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *q_smem = smem;                           // Q tile
+  uint8_t *do_smem = q_smem + Geo<D>::kTile;        // dout tile
+  uint8_t *kv_smem = do_smem + Geo<D>::kTile;       // kSlots x (K tile, V tile)
+  DqBars *bars = reinterpret_cast<DqBars *>(kv_smem + 2 * C::kSlots * Geo<D>::kTile);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int nqb = (p.Lq + kT - 1) / kT;
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int qt = nqb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest (causal) first
+  const int q0 = qt * kT;
+  const int b = bh / p.H, h = bh % p.H, hk = h / (p.H / p.Hkv);
+  const int len = clamp_len(p, b);
+  const int nt = key_tiles(p, len, q0);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->qdo_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->sdp_full, 1);
+    mbar_init(&bars->ds_full, kWg);
+    mbar_init(&bars->dq_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int issued = 0;
+  uint64_t *last_commit = nullptr;
+  uint32_t last_parity = 0;
+
+  if (warp == 4) {
+    if (lane == 0 && nt > 0) {
+      mbar_arrive_expect_tx(&bars->qdo_full, 2 * Geo<D>::kTile);
+      for (int blk = 0; blk < D / 64; ++blk) {
+        tma_load_4d(q_smem + blk * Geo<D>::kBlk, &maps.q, &bars->qdo_full, blk * 64, q0, h, b);
+        tma_load_4d(do_smem + blk * Geo<D>::kBlk, &maps.o, &bars->qdo_full, blk * 64, q0, h, b);
+      }
+      for (int j = 0; j < nt; ++j) {
+        const int s = j % C::kSlots, r = j / C::kSlots;
+        if (!mbar_wait(&bars->kv_empty[s], (r & 1) ^ 1, abort_flag)) break;
+        uint8_t *dst = kv_smem + 2 * s * Geo<D>::kTile;
+        mbar_arrive_expect_tx(&bars->kv_full[s], 2 * Geo<D>::kTile);
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tma_load_4d(dst + blk * Geo<D>::kBlk, &maps.k, &bars->kv_full[s], blk * 64, j * kT, hk,
+                      b);
+          tma_load_4d(dst + Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.v, &bars->kv_full[s],
+                      blk * 64, j * kT, hk, b);
+        }
+        issued = j + 1;
+      }
+    }
+  } else if (warp == 5) {
+    // S_0, dP_0, S_1; then per tile j: dQ_j, dP_{j+1}, S_{j+2}
+    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
+    const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
+    const uint32_t sq = smem_addr(q_smem), sdo = smem_addr(do_smem);
+    auto k_tile = [&](int j) { return smem_addr(kv_smem + 2 * (j % C::kSlots) * Geo<D>::kTile); };
+    auto v_tile = [&](int j) { return k_tile(j) + Geo<D>::kTile; };
+    auto wait_kv = [&](int j) {
+      return mbar_wait(&bars->kv_full[j % C::kSlots], (j / C::kSlots) & 1, abort_flag);
+    };
+    bool ok = nt == 0 || (mbar_wait(&bars->qdo_full, 0, abort_flag) && wait_kv(0));
+    if (ok && nt > 0) {
+      tc_fence_after();
+      if (lane == 0) {
+        mma_scores<D>(tmem + C::kS, sq, k_tile(0), idesc_s);
+        mma_scores<D>(tmem + C::kDp, sdo, v_tile(0), idesc_s);
+        tc_commit(&bars->sdp_full);
+      }
+      __syncwarp();
+      if (nt > 1 && (ok = wait_kv(1))) {
+        tc_fence_after();
+        if (lane == 0) mma_scores<D>(tmem + C::kS + kT, sq, k_tile(1), idesc_s);
+        __syncwarp();
+      }
+    }
+    for (int j = 0; ok && j < nt; ++j) {
+      if (!(ok = mbar_wait(&bars->ds_full, j & 1, abort_flag))) break;
+      tc_fence_after();
+      const int s = j % C::kSlots;
+      if (lane == 0) {
+        mma_grad<D>(tmem + C::kDq, tmem + C::kDp, k_tile(j), idesc_g, j > 0);
+        tc_commit(&bars->kv_empty[s]);
+        if (j + 1 < nt) {
+          mma_scores<D>(tmem + C::kDp, sdo, v_tile(j + 1), idesc_s);
+          tc_commit(&bars->sdp_full);
+        }
+      }
+      __syncwarp();
+      last_commit = &bars->kv_empty[s];
+      last_parity = (j / C::kSlots) & 1;
+      if (j + 2 < nt) {
+        if (!(ok = wait_kv(j + 2))) break;
+        tc_fence_after();
+        if (lane == 0) mma_scores<D>(tmem + C::kS + (j & 1) * kT, sq, k_tile(j + 2), idesc_s);
+        __syncwarp();
+      }
+    }
+    if (ok && nt > 0 && lane == 0) tc_commit(&bars->dq_done);
+    __syncwarp();
+  } else {
+    const int r = threadIdx.x;
+    const int i = q0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const bool row = i < p.Lq;
+    const size_t ridx = (static_cast<size_t>(b) * p.H + h) * p.Lq + (row ? i : 0);
+    const float lse = row ? a.lse[ridx] : INFINITY;
+    const float dd = row ? a.dsum[ridx] : 0.f;
+    const int jmax = row ? row_limit(p, len, i) : 0;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sdp_full, j & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_t = tmem + lane_base + C::kS + (j & 1) * kT;
+      const uint32_t dp_t = tmem + lane_base + C::kDp;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], pv[32], pk[16];
+        tmem_ld32(s_t + ch * 32, sv);
+        tmem_ld32(dp_t + ch * 32, pv);
+        tmem_wait_ld();
+        const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float w0 = e < lim ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse) : 0.f;
+          const float w1 =
+              e + 1 < lim ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse) : 0.f;
+          pk[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                                   w1 * (__uint_as_float(pv[e + 1]) - dd));
+        }
+        tmem_st16(dp_t + ch * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+    }
+    // the TMEM loads are warp-collective: every thread of the warp takes
+    // them; only rows inside the tensor are stored
+    if (nt > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_done, 0, abort_flag));
+      tc_fence_after();
+    }
+    uint16_t *dst = static_cast<uint16_t *>(a.dq) + (row ? row_at(p.layout, b, h, i, p.H, p.Lq, D) : 0);
+#pragma unroll 1
+    for (int ch = 0; ok && ch < D / 32; ++ch) {
+      if (nt > 0) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kDq + ch * 32, v);
+        tmem_wait_ld();
+        if (row) store_row32(dst + ch * 32, v, a.scale);
+      } else if (row) {
+        store_zero32(dst + ch * 32);
+      }
+    }
+  }
+
+  if (*abort_flag && warp == 4 && lane == 0) {
+    for (int idx = issued - C::kSlots; idx < issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->kv_full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    if (nt > 0) (void)wait_teardown(&bars->qdo_full, 0);
+  }
+  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
+    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================
+// dkdv: per 128 keys of a key/value head, over its query heads' row tiles
+// ============================================================================
+template <int D>
+struct DkdvCfg {
+  static constexpr int kSlots = D == 128 ? 2 : 4;  // ring of (Q tile, dout tile) pairs
+  static constexpr int kStat = 2 * kT * 4;          // lse and D of one query tile
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(2 + 2 * kSlots) * Geo<D>::kTile +
+                                  static_cast<size_t>(kSlots) * kStat + 512;
+  // TMEM: S^T (w^T bf16 over it), dP^T (dS^T bf16 over it), dV, dK
+  static constexpr uint32_t kS = 0, kDp = 128, kDv = 256, kDk = 256 + D;
+};
+struct DkdvBars {
+  uint64_t kv_full;
+  uint64_t qd_full[kMaxSlots], qd_empty[kMaxSlots];
+  uint64_t sdp_full;  // S^T and dP^T in TMEM
+  uint64_t pds_full;  // w^T and dS^T in TMEM (softmax threads)
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// query tiles [t_lo, t_hi) that can read some key of [k0, k0 + 128)
+__device__ __forceinline__ void query_tiles(const Problem &p, int len, int k0, int &t_lo,
+                                            int &t_hi) {
+  const int nqb = (p.Lq + kT - 1) / kT;
+  t_lo = 0;
+  t_hi = nqb;
+  if ((p.mask & kMaskKeyPadding) && k0 >= len) t_hi = 0;
+  if (p.mask & kMaskQueryPadding) t_hi = min(t_hi, (len + kT - 1) / kT);
+  if (p.mask & kMaskCausal) t_lo = max(t_lo, k0 / kT);
+  if (p.mask & kMaskCausalTail) t_lo = max(t_lo, max(k0 - len + p.Lq, 0) / kT);
+  if (t_lo > t_hi) t_lo = t_hi;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *k_smem = smem;                        // K tile
+  uint8_t *v_smem = k_smem + Geo<D>::kTile;      // V tile
+  uint8_t *qd_smem = v_smem + Geo<D>::kTile;     // kSlots x (Q tile, dout tile)
+  float *stat = reinterpret_cast<float *>(qd_smem + 2 * C::kSlots * Geo<D>::kTile);  // lse, D
+  DkdvBars *bars = reinterpret_cast<DkdvBars *>(reinterpret_cast<uint8_t *>(stat) +
+                                                C::kSlots * C::kStat);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BK = p.B * p.Hkv;
+  const int bk = static_cast<int>(blockIdx.x % BK);
+  const int k0 = static_cast<int>(blockIdx.x / BK) * kT;
+  const int b = bk / p.Hkv, hk = bk % p.Hkv;
+  const int group = p.H / p.Hkv;
+  const int len = clamp_len(p, b);
+  int t_lo, t_hi;
+  query_tiles(p, len, k0, t_lo, t_hi);
+  const int per_head = t_hi - t_lo;
+  const int nw = group * per_head;  // work items (query head of the group, query tile)
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bars->qd_full[s], 1);
+      mbar_init(&bars->qd_empty[s], 1);
+    }
+    mbar_init(&bars->sdp_full, 1);
+    mbar_init(&bars->pds_full, kWg);
+    mbar_init(&bars->done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int issued = 0;
+  uint64_t *last_commit = nullptr;
+  uint32_t last_parity = 0;
+
+  if (warp == 4) {
+    if (nw > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * Geo<D>::kTile);
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tma_load_4d(k_smem + blk * Geo<D>::kBlk, &maps.k, &bars->kv_full, blk * 64, k0, hk, b);
+          tma_load_4d(v_smem + blk * Geo<D>::kBlk, &maps.v, &bars->kv_full, blk * 64, k0, hk, b);
+        }
+      }
+      for (int w = 0; w < nw; ++w) {
+        const int s = w % C::kSlots, r = w / C::kSlots;
+        const int h = hk * group + w / per_head, q0 = (t_lo + w % per_head) * kT;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->qd_empty[s], (r & 1) ^ 1, abort_flag)))
+          break;
+        // the tile's lse and D (rows past Lq: weight 0)
+        float *st = stat + s * (C::kStat / 4);
+        const size_t row0 = (static_cast<size_t>(b) * p.H + h) * p.Lq;
+        for (int e = lane; e < kT; e += 32) {
+          const bool in = q0 + e < p.Lq;
+          st[e] = in ? a.lse[row0 + q0 + e] : INFINITY;
+          st[kT + e] = in ? a.dsum[row0 + q0 + e] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          uint8_t *dst = qd_smem + 2 * s * Geo<D>::kTile;
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * Geo<D>::kTile);
+          for (int blk = 0; blk < D / 64; ++blk) {
+            tma_load_4d(dst + blk * Geo<D>::kBlk, &maps.q, &bars->qd_full[s], blk * 64, q0, h, b);
+            tma_load_4d(dst + Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.o, &bars->qd_full[s],
+                        blk * 64, q0, h, b);
+          }
+        }
+        issued = w + 1;
+      }
+    }
+  } else if (warp == 5) {
+    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
+    const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
+    bool ok = nw == 0 || mbar_wait(&bars->kv_full, 0, abort_flag);
+    for (int w = 0; ok && w < nw; ++w) {
+      const int s = w % C::kSlots, r = w / C::kSlots;
+      if (!(ok = mbar_wait(&bars->qd_full[s], r & 1, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t sq = smem_addr(qd_smem + 2 * s * Geo<D>::kTile);
+      const uint32_t sdo = sq + Geo<D>::kTile;
+      if (lane == 0) {
+        mma_scores<D>(tmem + C::kS, smem_addr(k_smem), sq, idesc_s);    // S^T = K Q^T
+        mma_scores<D>(tmem + C::kDp, smem_addr(v_smem), sdo, idesc_s);  // dP^T = V dout^T
+        tc_commit(&bars->sdp_full);
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait(&bars->pds_full, w & 1, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        mma_grad<D>(tmem + C::kDv, tmem + C::kS, sdo, idesc_g, w > 0);  // dV += w^T dout
+        mma_grad<D>(tmem + C::kDk, tmem + C::kDp, sq, idesc_g, w > 0);  // dK += dS^T Q
+        tc_commit(&bars->qd_empty[s]);
+      }
+      __syncwarp();
+      last_commit = &bars->qd_empty[s];
+      last_parity = r & 1;
+    }
+    if (ok && nw > 0 && lane == 0) tc_commit(&bars->done);
+    __syncwarp();
+  } else {
+    const int r = threadIdx.x;
+    const int j = k0 + r;  // this thread's key
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // queries [i_min, i_max) may read key j
+    const bool key_ok = j < p.Lk && !((p.mask & kMaskKeyPadding) && j >= len);
+    int i_min = 0, i_max = p.Lq;
+    if (p.mask & kMaskCausal) i_min = j;
+    if (p.mask & kMaskCausalTail) i_min = max(i_min, j - len + p.Lq);
+    if (p.mask & kMaskQueryPadding) i_max = min(i_max, len);
+    if (!key_ok) i_max = i_min;
+    bool ok = true;
+    for (int w = 0; w < nw; ++w) {
+      const int s = w % C::kSlots;
+      const int q0 = (t_lo + w % per_head) * kT;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sdp_full, w & 1, abort_flag));
+      // the lse and D the producer stored before arriving on qd_full
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars->qd_full[s], (w / C::kSlots) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const float *st = stat + s * (C::kStat / 4);
+      const uint32_t s_t = tmem + lane_base + C::kS, dp_t = tmem + lane_base + C::kDp;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], pv[32], pw[16], pd[16];
+        tmem_ld32(s_t + ch * 32, sv);
+        tmem_ld32(dp_t + ch * 32, pv);
+        tmem_wait_ld();
+        const int c0 = q0 + ch * 32;
+        const int lo = i_min - c0, hi = i_max - c0;  // columns lo <= e < hi are allowed
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(st + ch * 32 + (e & ~3));
+          const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + ch * 32 + (e & ~3));
+          const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
+          const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
+          const bool oka = e >= lo && e < hi, okb = e + 1 >= lo && e + 1 < hi;
+          const float w0 = oka ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - la) : 0.f;
+          const float w1 = okb ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lb) : 0.f;
+          pw[e >> 1] = pack_bf16x2(w0, w1);
+          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
+                                   w1 * (__uint_as_float(pv[e + 1]) - db));
+        }
+        tmem_st16(s_t + ch * 16, pw);
+        tmem_st16(dp_t + ch * 16, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->pds_full);
+    }
+    // warp-collective TMEM loads by every thread; keys inside the tensor stored
+    const bool key = j < p.Lk;
+    if (nw > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->done, 0, abort_flag));
+      tc_fence_after();
+    }
+    uint16_t *dkr = static_cast<uint16_t *>(a.dk) + (key ? row_at(p.layout, b, hk, j, p.Hkv, p.Lk, D) : 0);
+    uint16_t *dvr = static_cast<uint16_t *>(a.dv) + (key ? row_at(p.layout, b, hk, j, p.Hkv, p.Lk, D) : 0);
+#pragma unroll 1
+    for (int ch = 0; ok && ch < D / 32; ++ch) {
+      if (nw > 0) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + C::kDv + ch * 32, v);
+        tmem_wait_ld();
+        if (key) store_row32(dvr + ch * 32, v, 1.f);
+        tmem_ld32(tmem + lane_base + C::kDk + ch * 32, v);
+        tmem_wait_ld();
+        if (key) store_row32(dkr + ch * 32, v, a.scale);
+      } else if (key) {
+        store_zero32(dvr + ch * 32);
+        store_zero32(dkr + ch * 32);
+      }
+    }
+  }
+
+  if (*abort_flag && warp == 4 && lane == 0) {
+    for (int idx = issued - C::kSlots; idx < issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->qd_full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    if (nw > 0) (void)wait_teardown(&bars->kv_full, 0);
+  }
+  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
+    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+template <typename K>
+cudaError_t launch_one(K kernel, size_t smem, long long grid, const LongMaps &maps,
+                       const Problem &p, const BwdArgs &a, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps, p, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_tc_impl(const LongMaps &maps, const Problem &p, const BwdArgs &a,
+                               cudaStream_t stream) {
+  static_assert(StatsCfg<D>::kSmem <= 232448 && DqCfg<D>::kSmem <= 232448 &&
+                    DkdvCfg<D>::kSmem <= 232448,
+                "shared memory budget");
+  const long long nqb = (p.Lq + kT - 1) / kT, nkb = (p.Lk + kT - 1) / kT;
+  const long long q_grid = nqb * p.B * p.H, k_grid = nkb * p.B * p.Hkv;
+  cudaError_t e = launch_one(bwd_stats_tc_kernel<D>, StatsCfg<D>::kSmem, q_grid, maps, p, a, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_one(bwd_dq_tc_kernel<D>, DqCfg<D>::kSmem, q_grid, maps, p, a, stream);
+  if (e != cudaSuccess) return e;
+  return launch_one(bwd_dkdv_tc_kernel<D>, DkdvCfg<D>::kSmem, k_grid, maps, p, a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a,
+                          cudaStream_t stream) {
+  if (p.dk == 128) return launch_bwd_tc_impl<128>(maps, p, a, stream);
+  return launch_bwd_tc_impl<64>(maps, p, a, stream);
+}
+
+}  // namespace mha

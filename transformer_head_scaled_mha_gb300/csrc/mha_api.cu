@@ -380,7 +380,19 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
   a.lse = reinterpret_cast<float *>(ws);
   a.dsum = reinterpret_cast<float *>(ws + nws / 2);
   a.scale = scale;
-  err = launch_bwd_simt(a, p, dtype == MHA_DTYPE_BF16, stream);
+  if (dtype == MHA_DTYPE_BF16) {
+    // tensor cores (d in {64, 128}, enforced by select_path)
+    LongMaps m;
+    std::memset(&m, 0, sizeof m);
+    const bool ok = make_map(&m.q, q, d_k, Lq, H, B, layout, 128, 1) &&
+                    make_map(&m.k, k, d_k, Lk, H_kv, B, layout, 128, 1) &&
+                    make_map(&m.v, v, d_v, Lk, H_kv, B, layout, 128, 1) &&
+                    make_map(&m.o, dout, d_v, Lq, H, B, layout, 128, 1);
+    if (!ok) return MHA_ERR_CUDA;
+    err = launch_bwd_tc(m, p, a, stream);
+  } else {
+    err = launch_bwd_simt(a, p, false, stream);
+  }
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
