@@ -8,7 +8,9 @@ d=64, key + query padding with lengths uniform in [8, 64] (HBM-bound; metric
 GB/s).  ``--workload`` picks another (see gen.WORKLOADS); the long causal one
 reports TFLOP/s.  The ``sublayer_*`` workloads (gen.SUBLAYERS) time the whole
 multi-head sublayer per step (projections with biases, attention, output
-projection; TFLOP/s), with the projection kernel as the roofline kernel.
+projection; TFLOP/s), with the projection kernel as the roofline kernel.  The
+``bwd_*`` workloads time the backward pass (``mha_bwd``: dq, dk, dv of a
+forward workload; TFLOP/s of the five products the chain rule needs).
 
 value  device throughput, inputs resident in HBM; K launches captured in one
        CUDA graph and replayed between CUDA events; consecutive launches read
@@ -47,7 +49,12 @@ import gen  # noqa: E402
 DEFAULT_WORKLOAD = "enc_pad_bf16_b256_h8_l64_d64"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_NAMES = {1: "attn_f32_simt_kernel", 2: "attn_short_tc_kernel", 3: "attn_long_tc_kernel",
-                4: "zero_fill_kernel"}
+                4: "zero_fill_kernel", 5: "attn_decode_tc_kernel"}
+# backward workloads: the gradients of a forward workload (training shapes)
+BWD_WORKLOADS = {"bwd_" + n: n for n in ("enc_pad_bf16_b256_h8_l64_d64",
+                                         "dec_causal_bf16_b128_h8_l128_d64",
+                                         "cross_pad_bf16_b64_h16_lq96_lk128_d64",
+                                         "long_causal_bf16_b4_h16_l8192_d128")}
 
 
 # ---------------------------------------------------------------------------
@@ -309,7 +316,8 @@ def run_ours(args):
     scale = gen.default_scale(spec["dk"])
     mask = spec["mask"]
     B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
-    path = mha.mha_fwd_path(B, H, Lq, Lk, dk, dv, mask, 1 if dt == "bf16" else 0)
+    path = mha.mha_fwd_path_ex(B, H, spec.get("Hkv", H), Lq, Lk, dk, dv, mask,
+                               1 if dt == "bf16" else 0)
     kernel = KERNEL_NAMES.get(path, "?")
 
     def host_tensor(a):
@@ -709,7 +717,8 @@ def run_reference_sublayer(args):
                        "S": spec["S"], "d_model": spec["d_model"], "H": spec["H"],
                        "H_kv": spec["H_kv"], "mask_kind": spec["mask"]},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
-                             "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+                             "cores": min(oracle.max_threads(), len(units)), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -755,6 +764,289 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# backward workloads: the gradients dq, dk, dv of a forward workload
+# ---------------------------------------------------------------------------
+def backward_flops(spec, lens):
+    """Algorithmic flops of the backward pass: per allowed (query, key) pair the
+    scores recomputed (2 d_k), dP = dout v (2 d_v), dV (2 d_v), dK (2 d_k) and
+    dQ (2 d_k) -- 2 (3 d_k + 2 d_v), 2.5 times the forward's 2 (d_k + d_v)."""
+    _, fwd = algorithmic(spec, lens)
+    dk, dv = spec["dk"], spec["dv"]
+    return int(fwd * (3 * dk + 2 * dv) // (dk + dv))
+
+
+def oracle_backward_time(spec, inp, units, rows):
+    """Seconds for the oracle's backward pass over some (batch, key/value head)
+    units and a range of query rows in each, and the share of the whole
+    workload's allowed (query, key) pairs that sample holds."""
+    import oracle
+    q, k, v, lens, dout = inp
+    scale = gen.default_scale(spec["dk"])
+    t0 = time.perf_counter()
+    oracle.mha_bwd(q, k, v, dout, mask_kind=spec["mask"], key_lengths=lens, scale=scale,
+                   layout=spec.get("layout", "bhsd"), units=units, rows=rows)
+    t = time.perf_counter() - t0
+    return t, sample_pair_share(spec, lens, units, rows)
+
+
+def sample_pair_share(spec, lens, units, rows):
+    """Share of all allowed (query, key) pairs that lie in the sampled units and rows."""
+    B, H, Lq, Lk = spec["B"], spec["H"], spec["Lq"], spec["Lk"]
+    Hkv = spec.get("Hkv", H)
+    m = spec["mask"]
+    L = np.full(B, Lk, dtype=np.int64) if lens is None else np.clip(lens.astype(np.int64), 0, Lk)
+    i_lo, i_hi = (0, Lq) if rows is None else rows
+
+    def pairs_of(b, lo, hi):
+        kmax = int(L[b]) if m & gen.MASK_KEY_PADDING else Lk
+        hi = min(hi, int(L[b])) if m & gen.MASK_QUERY_PADDING else hi
+        i = np.arange(lo, max(lo, hi))
+        if m & gen.MASK_CAUSAL:
+            return int(np.minimum(i + 1, kmax).sum())
+        if m & gen.MASK_CAUSAL_TAIL:
+            return int(np.clip(kmax - Lq + i + 1, 0, kmax).sum())
+        return len(i) * kmax
+
+    total = sum(pairs_of(b, 0, Lq) for b in range(B)) * H
+    us = range(B * Hkv) if units is None else units
+    part = sum(pairs_of(u // Hkv, i_lo, i_hi) for u in us) * (H // Hkv)
+    return part / max(total, 1)
+
+
+def backward_sample(spec, inp, budget_s):
+    """Units and a row range whose oracle backward takes about budget_s."""
+    B, Hkv, Lq = spec["B"], spec.get("Hkv", spec["H"]), spec["Lq"]
+    # probe: one unit, a row range sized for a fraction of a second
+    rows = (max(0, Lq - 64), Lq)
+    t, share = oracle_backward_time(spec, inp, [0], rows)
+    rate = share / max(t, 1e-6)  # workload share per second
+    want = rate * budget_s
+    import oracle
+    one_unit = sample_pair_share(spec, inp[3], [0], None)
+    if want >= one_unit:
+        n = max(1, min(B * Hkv, int(want / max(one_unit, 1e-12))))
+        return list(range(n)), None
+    # less than one unit's work: the last rows of as many units as host
+    # threads, so every thread has a unit (the oracle runs one per thread)
+    units = list(range(min(B * Hkv, max(1, oracle.max_threads()))))
+    per = sample_pair_share(spec, inp[3], units, None)
+    n_rows = max(1, min(Lq, int(Lq * want * len(units) / max(per, 1e-12))))
+    return units, (max(0, Lq - n_rows), Lq)
+
+
+def run_backward(args):
+    import torch
+
+    import transformer_head_scaled_mha_gb300 as mha
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    fwd_name = BWD_WORKLOADS[args.workload]
+    spec = gen.WORKLOADS[fwd_name]
+    q, k, v, lens = gen.make_inputs(spec, seed=args.seed)
+    dout = gen.make_dout(spec, seed=args.seed)
+    flops = backward_flops(spec, lens)
+    scale = gen.default_scale(spec["dk"])
+    mask = spec["mask"]
+    layout = spec.get("layout", "bhsd")
+    B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
+    Hkv = spec.get("Hkv", H)
+
+    def host(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+
+    hq, hk, hv, hdo = host(q), host(k), host(v), host(dout)
+    kl = torch.from_numpy(lens).to(dev) if lens is not None else None
+    # the forward output the backward reads, from the forward kernel itself
+    out0 = mha.mha_fwd_ex(hq.to(dev), hk.to(dev), hv.to(dev), layout=layout, mask_kind=mask,
+                          key_lengths=kl, scale=scale)
+    hout = out0.cpu()
+    ins = (hq, hk, hv, hout, hdo)
+    set_bytes = sum(t.numel() * 2 for t in ins) + (hq.numel() + hk.numel() + hv.numel()) * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes))
+    sets = [tuple(t.to(dev) for t in ins) + (torch.empty_like(hq, device=dev),
+                                             torch.empty_like(hk, device=dev),
+                                             torch.empty_like(hv, device=dev))
+            for _ in range(n_sets)]
+    ws = torch.empty(max(1, mha.mha_bwd_workspace_size(B, H, Lq)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        qq, kk, vv, oo, gg, dq, dk_, dv_ = sets[i % n_sets]
+        mha.mha_bwd(qq, kk, vv, oo, gg, layout=layout, mask_kind=mask, key_lengths=kl,
+                    scale=scale, workspace=ws, dq=dq, dk=dk_, dv=dv_, stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(args.steps):
+            step(i, stream)
+
+    def replay():
+        with torch.cuda.stream(stream):
+            graph.replay()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        replay()
+        stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    sampler.mark(t_soak + min(0.2, args.soak / 2), t_wall1)
+    clocks = sampler.stop()
+    per_step = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / args.steps
+    value = flops / per_step / 1e12 * world
+    st = mha.mha_debug_status(stream)
+    if st != mha.MHA_OK:
+        raise RuntimeError("device status after timing: %s" % mha.mha_status_string(st))
+
+    # roofline: the whole backward call (stats, dq and dkdv launches) against
+    # the bf16 tensor peak; the ncu launch list splits its time by kernel
+    peaks, peak_src = read_peaks()
+    achieved = flops / per_step / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": recorded_traffic(args.workload),
+                "kernel": "bwd_stats_tc_kernel + bwd_dq_tc_kernel + bwd_dkdv_tc_kernel "
+                          "(one mha_bwd call, 3 launches)",
+                "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback", "algorithmic_flops": flops}
+
+    # e2e: q, k, v, out, dout (and lengths) in, dq, dk, dv back, every step
+    pins = [t.pin_memory() for t in ins]
+    pl = torch.from_numpy(lens).pin_memory() if lens is not None else None
+    pouts = [torch.empty_like(t).pin_memory() for t in (hq, hk, hv)]
+    dset = sets[0]
+    dl = torch.empty_like(kl) if kl is not None else None
+    h2d = sum(t.numel() * 2 for t in pins) + (pl.numel() * 4 if pl is not None else 0)
+    d2h = sum(t.numel() * 2 for t in pouts)
+
+    def e2e_step():
+        for dst, src in zip(dset[:5], pins):
+            dst.copy_(src, non_blocking=True)
+        if pl is not None:
+            dl.copy_(pl, non_blocking=True)
+        mha.mha_bwd(*dset[:5], layout=layout, mask_kind=mask, key_lengths=dl, scale=scale,
+                    workspace=ws, dq=dset[5], dk=dset[6], dv=dset[7], stream=stream)
+        for dst, src in zip(pouts, dset[5:]):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / e2e_steps
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        inp = (q, k, v, lens, dout)
+        units, rows = backward_sample(spec, inp, args.cpu_budget)
+        t, share = oracle_backward_time(spec, inp, units, rows)
+        cpu = {"value": flops * share / t / 1e12, "unit": "TFLOP/s",
+               "cores": min(oracle.max_threads(), len(units)), "kind": "oracle",
+               "sample": "%d of %d (batch, key/value head) units, query rows %s; %.4g%% of the "
+                         "allowed (query, key) pairs, %.1f s; work scaled by that share" % (
+                             len(units), B * Hkv, "all" if rows is None else "%d..%d" % (
+                                 rows[0], rows[1] - 1), 100 * share, t)}
+    if rank == 0:
+        line = {
+            "metric": "attention bwd TFLOP/s", "value": round(value, 3), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)%s q, k, v and dout; out from the forward "
+                    "kernel; seed %d)" % ("*%g" % spec["amp"] if spec["amp"] != 1.0 else "",
+                                          args.seed),
+            "config": {"workload": args.workload, "forward": fwd_name, "B": B, "H": H,
+                       "H_kv": Hkv, "layout": layout, "Lq": Lq, "Lk": Lk, "d_k": dk,
+                       "d_v": dv, "mask_kind": mask, "len_range": spec["len_range"],
+                       "scale": scale,
+                       "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
+                             % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+                       "timing": "CUDA graph of %d calls (3 launches each), CUDA events"
+                                 % args.steps,
+                       "parallelism": "weak: same workload per rank, no collective"
+                       if world > 1 else "1 GPU"},
+            "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": 3 * args.steps,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference_backward(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    spec = gen.WORKLOADS[BWD_WORKLOADS[args.workload]]
+    q, k, v, lens = gen.make_inputs(spec, seed=args.seed)
+    dout = gen.make_dout(spec, seed=args.seed)
+    flops = backward_flops(spec, lens)
+    import oracle
+    oracle.build()
+    inp = (q, k, v, lens, dout)
+    units, rows = backward_sample(spec, inp, args.ref_step_budget)
+    for _ in range(args.warmup):
+        oracle_backward_time(spec, inp, units, rows)
+    runs = [oracle_backward_time(spec, inp, units, rows) for _ in range(args.steps)]
+    t = sum(r[0] for r in runs)
+    share = runs[0][1]
+    value = flops * share * args.steps / t / 1e12
+    B, Hkv = spec["B"], spec.get("Hkv", spec["H"])
+    sample = ("each step: %d of %d (batch, key/value head) units, query rows %s (%.4g%% of the "
+              "allowed pairs), scaled by that share" % (
+                  len(units), B * Hkv, "all" if rows is None else "%d..%d" % (rows[0], rows[1] - 1),
+                  100 * share))
+    line = {"impl": "reference", "metric": "attention bwd TFLOP/s", "value": round(value, 6),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, seed %d)" % args.seed,
+            "config": {"workload": args.workload, "forward": BWD_WORKLOADS[args.workload],
+                       "B": B, "H": spec["H"], "Lq": spec["Lq"], "Lk": spec["Lk"],
+                       "d_k": spec["dk"], "d_v": spec["dv"], "mask_kind": spec["mask"]},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                             "cores": min(oracle.max_threads(), len(units)), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -762,7 +1054,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(gen.WORKLOADS) + sorted(gen.SUBLAYERS))
+                    choices=sorted(gen.WORKLOADS) + sorted(gen.SUBLAYERS) +
+                    sorted(BWD_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a graph")
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing, s")
@@ -778,6 +1071,9 @@ def main(argv=None):
         if not (world == 1 and args.gpus == 1):
             print("warning: --gpus %d but WORLD_SIZE %d; using WORLD_SIZE" % (args.gpus, world),
                   file=sys.stderr)
+    if args.workload in BWD_WORKLOADS:
+        (run_reference_backward if args.impl == "reference" else run_backward)(args)
+        return
     sub = args.workload in gen.SUBLAYERS
     if args.impl == "reference":
         (run_reference_sublayer if sub else run_reference)(args)

@@ -119,6 +119,10 @@ CASES = [
     spec(2, 2, 200, 333, 64, mask=KP, len_range=(0, 333)),
     spec(1, 4, 257, 257, 128, mask=C | KP, len_range=(100, 257), Hkv=1, layout="bshd"),
     spec(3, 2, 1, 500, 64, mask=TAIL | KP, len_range=(1, 500)),
+    # several query and key tiles with shared key/value heads
+    spec(2, 4, 640, 640, 128, mask=C, amp=0.5, Hkv=2, layout="bshd"),
+    spec(2, 6, 333, 555, 64, mask=KP, len_range=(100, 555), Hkv=3),
+    spec(2, 4, 260, 700, 64, mask=TAIL | KP, len_range=(300, 700), Hkv=1, layout="bshd"),
 ]
 
 
@@ -172,3 +176,37 @@ def test_backward_rejects_small_workspace():
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(mha.MhaError):
         mha.mha_bwd(q, q, q, q.clone(), q.clone(), workspace=ws)
+
+
+def test_backward_long_causal_full_size_sampled():
+    # the long causal workload at full size; rows [L-128, L) of a head give
+    # its dq exactly and, under the causal mask, the whole dk and dv of keys
+    # [L-128, L); rows [0, 128) give their dq exactly
+    import torch
+    import transformer_head_scaled_mha_gb300 as mha
+    s = gen.WORKLOADS["long_causal_bf16_b4_h16_l8192_d128"]
+    L, B, H = s["Lq"], s["B"], s["H"]
+    q, k, v, _ = gen.make_inputs(s, seed=45)
+    dout = gen.make_dout(s, seed=45)
+    scale = gen.default_scale(s["dk"])
+    Q, K, V, DO = (to_device(a, "bf16") for a in (q, k, v, dout))
+    out = mha.mha_fwd(Q, K, V, mask_kind=C, scale=scale)
+    dq, dk, dv = mha.mha_bwd(Q, K, V, out, DO, mask_kind=C, scale=scale)
+    torch.cuda.synchronize()
+    assert mha.mha_debug_status() == mha.MHA_OK
+    got = [gen.as_f64(from_device(t), "bf16") for t in (dq, dk, dv)]
+    del Q, K, V, DO, out, dq, dk, dv
+    units = [0, 17, 38, 63]
+    ref_hi = oracle.mha_bwd(q, k, v, dout, mask_kind=C, scale=scale, units=units,
+                            rows=(L - 128, L))
+    ref_lo = oracle.mha_bwd(q, k, v, dout, mask_kind=C, scale=scale, units=units, rows=(0, 128))
+    for u in units:
+        b, h = divmod(u, H)
+        pieces = [(got[0][b, h, L - 128:], ref_hi[0][b, h, L - 128:], "dq last rows"),
+                  (got[0][b, h, :128], ref_lo[0][b, h, :128], "dq first rows"),
+                  (got[1][b, h, L - 128:], ref_hi[1][b, h, L - 128:], "dk last keys"),
+                  (got[2][b, h, L - 128:], ref_hi[2][b, h, L - 128:], "dv last keys")]
+        for g, r, name in pieces:
+            mag = float(np.abs(r).max())
+            err = np.abs(g - r)
+            assert err.max() <= 2e-2 * mag and err.mean() <= 2e-3 * mag, (u, name, err.max(), mag)
