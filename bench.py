@@ -122,10 +122,23 @@ def read_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest():
+# the source file of each profiled kernel (the digest also covers the shared
+# headers and the dispatcher, which set its launch parameters)
+KERNEL_FILES = {"attn_short_tc_kernel": "attn_short_tc.cu", "attn_long_tc_kernel": "attn_long_tc.cu",
+                "attn_decode_tc_kernel": "attn_decode_tc.cu", "linear_tc_kernel": "linear_tc.cu",
+                "attn_f32_simt_kernel": "attn_f32_simt.cu", "bwd_tc": "attn_bwd_tc.cu"}
+SHARED_FILES = ("common.cuh", "ptx.cuh", "mha_api.cu")
+
+
+def kernel_source_digest(kernel=None):
+    """Digest of the sources a kernel is built from (all of csrc/ when
+    `kernel` is None or unknown)."""
     csrc = os.path.join(ROOT, "transformer_head_scaled_mha_gb300", "csrc")
+    names = sorted(os.listdir(csrc))
+    if kernel in KERNEL_FILES:
+        names = sorted(SHARED_FILES + (KERNEL_FILES[kernel],))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -141,7 +154,7 @@ def recorded_traffic(workload):
             rec = json.load(f).get(workload)
     except Exception:
         return None
-    if not rec or rec.get("source_digest") != kernel_source_digest():
+    if not rec or rec.get("source_digest") != kernel_source_digest(rec.get("kernel")):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -926,6 +939,7 @@ def run_backward(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": recorded_traffic(args.workload),
+                "traffic_kernel": "bwd_dkdv_tc_kernel (the largest share of the call)",
                 "kernel": "bwd_stats_tc_kernel + bwd_dq_tc_kernel + bwd_dkdv_tc_kernel "
                           "(one mha_bwd call, 3 launches)",
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
