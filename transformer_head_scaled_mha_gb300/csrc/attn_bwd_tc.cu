@@ -137,9 +137,11 @@ __device__ __forceinline__ void mma_grad(uint32_t d_tmem, uint32_t a_tmem, uint3
 // ============================================================================
 // stats: lse and D per query row
 // ============================================================================
+// two CTAs per SM (256 TMEM columns and under half the shared memory each):
+// one CTA's softmax runs while the tensor core serves the other
 template <int D>
 struct StatsCfg {
-  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kSlots = D == 128 ? 2 : 4;
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(1 + kSlots) * Geo<D>::kTile + 512;
 };
 struct StatsBars {
@@ -151,7 +153,7 @@ struct StatsBars {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     bwd_stats_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
   using C = StatsCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -743,6 +745,335 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
+// ============================================================================
+// short: query and key lengths of one tile (<= 128), d = 64 -- the whole
+// backward of a (batch, key/value head) pair in one persistent CTA
+// ============================================================================
+// Per query head of the pair's group, two phases over the same tiles:
+//   A  S = Q K^T, dP = dout V^T (rows on the lanes): the row's exact softmax
+//      over its one key tile gives lse, dS = w (dP - D) goes over dP in TMEM,
+//      dQ = dS K
+//   B  S^T = K Q^T, dP^T = V dout^T (keys on the lanes): w^T and dS^T from the
+//      lse and D of phase A, dV += w^T dout, dK += dS^T Q over the group
+// K and V of the next pair, and Q and dout of the next head, load while the
+// current one computes.  TMEM: S | dP | dQ | dV | dK (448 columns).
+struct ShortBwdBars {
+  uint64_t kv_full[2], kv_empty[2];  // K, V of a pair (by pair parity)
+  uint64_t qd_full[2], qd_empty[2];  // Q, dout of a head (by iteration parity)
+  uint64_t a_full;    // S, dP in TMEM
+  uint64_t ds_ready;  // dS in TMEM, lse and D in smem (softmax threads)
+  uint64_t dq_full;   // dQ in TMEM
+  uint64_t dq_free;   // dQ read (softmax threads)
+  uint64_t b_full;    // S^T, dP^T in TMEM
+  uint64_t pds_ready; // w^T, dS^T in TMEM (softmax threads)
+  uint64_t dkv_full;  // dV, dK of a pair complete
+  uint64_t dkv_free;  // dV, dK read (softmax threads)
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr int kSbTile = 128 * 128;  // one [128 x 64] bf16 tile
+constexpr size_t kSbSmem = 1024 + 8 * static_cast<size_t>(kSbTile) + 2 * 2 * kT * 4 + 512;
+constexpr uint32_t kSbS = 0, kSbDp = 128, kSbDq = 256, kSbDv = 320, kSbDk = 384;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_short_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *kv_smem = smem;                   // 2 x (K, V)
+  uint8_t *qd_smem = kv_smem + 4 * kSbTile;  // 2 x (Q, dout)
+  float *stat = reinterpret_cast<float *>(qd_smem + 4 * kSbTile);  // 2 x (lse[128], D[128])
+  ShortBwdBars *bars = reinterpret_cast<ShortBwdBars *>(reinterpret_cast<uint8_t *>(stat) +
+                                                        2 * 2 * kT * 4);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int group = p.H / p.Hkv;
+  const int units = p.B * p.Hkv;
+  const int n_local = static_cast<int>(blockIdx.x) < units
+                          ? (units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                          : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->qd_full[i], 1);
+      mbar_init(&bars->qd_empty[i], 1);
+    }
+    mbar_init(&bars->a_full, 1);
+    mbar_init(&bars->ds_ready, kWg);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, kWg);
+    mbar_init(&bars->b_full, 1);
+    mbar_init(&bars->pds_ready, kWg);
+    mbar_init(&bars->dkv_full, 1);
+    mbar_init(&bars->dkv_free, kWg);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  int kv_issued = 0, qd_issued = 0;
+  uint64_t *last_commit = nullptr;
+  uint32_t last_parity = 0;
+
+  if (warp == 4) {
+    // ---- producer: per pair K and V, then Q and dout of each query head ----
+    int it = 0;
+    for (int ul = 0; ul < n_local; ++ul) {
+      const int u = static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x);
+      const int b = u / p.Hkv, hk = u % p.Hkv;
+      const int kb = ul & 1;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bars->kv_empty[kb], ((ul >> 1) & 1) ^ 1, abort_flag)))
+        break;
+      if (lane == 0) {
+        uint8_t *dst = kv_smem + 2 * kb * kSbTile;
+        mbar_arrive_expect_tx(&bars->kv_full[kb], 2 * kSbTile);
+        tma_load_4d(dst, &maps.k, &bars->kv_full[kb], 0, 0, hk, b);
+        tma_load_4d(dst + kSbTile, &maps.v, &bars->kv_full[kb], 0, 0, hk, b);
+      }
+      kv_issued = ul + 1;
+      bool ok = true;
+      for (int hl = 0; hl < group; ++hl, ++it) {
+        const int st = it & 1;
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->qd_empty[st], ((it >> 1) & 1) ^ 1, abort_flag))))
+          break;
+        if (lane == 0) {
+          uint8_t *dst = qd_smem + 2 * st * kSbTile;
+          mbar_arrive_expect_tx(&bars->qd_full[st], 2 * kSbTile);
+          tma_load_4d(dst, &maps.q, &bars->qd_full[st], 0, 0, hk * group + hl, b);
+          tma_load_4d(dst + kSbTile, &maps.o, &bars->qd_full[st], 0, 0, hk * group + hl, b);
+        }
+        qd_issued = it + 1;
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 5) {
+    // ---- MMA issuer: per head A1 (S, dP), A2 (dQ), B1 (S^T, dP^T), B2 (dV, dK)
+    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
+    const uint32_t idesc_g = idesc_bf16_f32(128, 64, 1);
+    bool ok = true;
+    int it = 0;
+    for (int ul = 0; ok && ul < n_local; ++ul) {
+      const int kb = ul & 1;
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->kv_full[kb], (ul >> 1) & 1, abort_flag))))
+        break;
+      const uint32_t sk = smem_addr(kv_smem + 2 * kb * kSbTile), sv = sk + kSbTile;
+      for (int hl = 0; hl < group; ++hl, ++it) {
+        const int st = it & 1;
+        const uint32_t sq = smem_addr(qd_smem + 2 * st * kSbTile), sdo = sq + kSbTile;
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->qd_full[st], (it >> 1) & 1, abort_flag))))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          mma_scores<64>(tmem + kSbS, sq, sk, idesc_s);     // S = Q K^T
+          mma_scores<64>(tmem + kSbDp, sdo, sv, idesc_s);   // dP = dout V^T
+          tc_commit(&bars->a_full);
+        }
+        __syncwarp();
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, it & 1, abort_flag));
+        // dQ of the previous head has been read
+        if (ok && it >= 1)
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          mma_grad<64>(tmem + kSbDq, tmem + kSbDp, sk, idesc_g, false);  // dQ = dS K
+          tc_commit(&bars->dq_full);
+          mma_scores<64>(tmem + kSbS, sk, sq, idesc_s);    // S^T = K Q^T
+          mma_scores<64>(tmem + kSbDp, sv, sdo, idesc_s);  // dP^T = V dout^T
+          tc_commit(&bars->b_full);
+          if (hl == group - 1) tc_commit(&bars->kv_empty[kb]);
+        }
+        __syncwarp();
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_ready, it & 1, abort_flag));
+        // the pair's first head overwrites dV, dK: the previous pair's were read
+        if (ok && hl == 0 && ul >= 1)
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_free, (ul - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          mma_grad<64>(tmem + kSbDv, tmem + kSbS, sdo, idesc_g, hl > 0);  // dV += w^T dout
+          mma_grad<64>(tmem + kSbDk, tmem + kSbDp, sq, idesc_g, hl > 0);  // dK += dS^T Q
+          tc_commit(&bars->qd_empty[st]);
+          if (hl == group - 1) tc_commit(&bars->dkv_full);
+        }
+        __syncwarp();
+        last_commit = &bars->qd_empty[st];
+        last_parity = (it >> 1) & 1;
+      }
+    }
+  } else {
+    // ---- softmax: phase A thread r = query row r, phase B thread r = key r ---
+    const int r = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    int it = 0;
+    for (int ul = 0; ok && ul < n_local; ++ul) {
+      const int u = static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x);
+      const int b = u / p.Hkv, hk = u % p.Hkv;
+      const int len = clamp_len(p, b);
+      const int jmax = r < p.Lq ? row_limit(p, len, r) : 0;  // phase A: keys j < jmax
+      // phase B: queries [i_min, i_max) may read key r
+      const bool key_ok = r < p.Lk && !((p.mask & kMaskKeyPadding) && r >= len);
+      int i_min = 0, i_max = p.Lq;
+      if (p.mask & kMaskCausal) i_min = r;
+      if (p.mask & kMaskCausalTail) i_min = max(i_min, r - len + p.Lq);
+      if (p.mask & kMaskQueryPadding) i_max = min(i_max, len);
+      if (!key_ok) i_max = i_min;
+      for (int hl = 0; hl < group; ++hl, ++it) {
+        const int h = hk * group + hl;
+        float *st = stat + (it & 1) * 2 * kT;
+        // D of row r, loaded while the scores are computed
+        float dd = 0.f;
+        if (r < p.Lq) {
+          const size_t ro = row_at(p.layout, b, h, r, p.H, p.Lq, 64);
+          const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.out) + ro);
+          const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + ro);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 ov = o4[c], gv = g4[c];
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              dd = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), dd);
+              dd = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u), dd);
+            }
+          }
+        }
+        // ---- phase A: the row's softmax over its one key tile, dS over dP
+        const bool oka = __all_sync(0xffffffffu, mbar_wait(&bars->a_full, it & 1, abort_flag));
+        if (oka) {
+          tc_fence_after();
+          uint32_t sr[4][32];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
+          tmem_wait_ld();
+          const bool need_mask = __any_sync(0xffffffffu, jmax < kT);
+          const float m = scale_mask_max128(sr, p.scale_log2, need_mask, 0, jmax);
+          const float l = exp2_sum128(sr, m, m != -INFINITY);
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          st[r] = l > 0.f ? m + __log2f(l) : INFINITY;
+          st[kT + r] = dd;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pv[32], pk[16];
+            tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float w0 = __uint_as_float(sr[ch][e]) * inv;
+              const float w1 = __uint_as_float(sr[ch][e + 1]) * inv;
+              pk[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                                       w1 * (__uint_as_float(pv[e + 1]) - dd));
+            }
+            tmem_st16(tmem + lane_base + kSbDp + ch * 16, pk);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        // every row's lse and D are in smem before phase B reads them
+        ok = named_barrier_and(1, kWg, ok && oka);
+        if (!ok) break;
+        mbar_arrive(&bars->ds_ready);
+        // ---- phase B: keys on the lanes, w^T and dS^T over S^T and dP^T
+        const bool okb = __all_sync(0xffffffffu, mbar_wait(&bars->b_full, it & 1, abort_flag));
+        if (okb) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t sv[32], pv[32], pw[16], pd[16];
+            tmem_ld32(tmem + lane_base + kSbS + ch * 32, sv);
+            tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
+            tmem_wait_ld();
+            const int lo = i_min - ch * 32, hi = i_max - ch * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(st + ch * 32 + (e & ~3));
+              const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + ch * 32 + (e & ~3));
+              const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
+              const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
+              const bool oka2 = e >= lo && e < hi, okb2 = e + 1 >= lo && e + 1 < hi;
+              const float w0 = oka2 ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - la) : 0.f;
+              const float w1 = okb2 ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lb) : 0.f;
+              pw[e >> 1] = pack_bf16x2(w0, w1);
+              pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
+                                       w1 * (__uint_as_float(pv[e + 1]) - db));
+            }
+            tmem_st16(tmem + lane_base + kSbS + ch * 16, pw);
+            tmem_st16(tmem + lane_base + kSbDp + ch * 16, pd);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->pds_ready);
+        // ---- dQ of this head (thread r = row r)
+        const bool okq = okb && __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag));
+        if (okq) {
+          tc_fence_after();
+          uint16_t *dst = static_cast<uint16_t *>(a.dq) +
+                          (r < p.Lq ? row_at(p.layout, b, h, r, p.H, p.Lq, 64) : 0);
+#pragma unroll 1
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kSbDq + ch * 32, v);
+            tmem_wait_ld();
+            if (r < p.Lq) store_row32(dst + ch * 32, v, a.scale);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free);
+        ok = okq;
+      }
+      // ---- dV and dK of the pair (thread r = key r)
+      const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(&bars->dkv_full, ul & 1, abort_flag));
+      ok = named_barrier_and(1, kWg, okd);
+      if (!ok) break;
+      tc_fence_after();
+      const size_t ko = r < p.Lk ? row_at(p.layout, b, hk, r, p.Hkv, p.Lk, 64) : 0;
+      uint16_t *dvr = static_cast<uint16_t *>(a.dv) + ko;
+      uint16_t *dkr = static_cast<uint16_t *>(a.dk) + ko;
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kSbDv + ch * 32, v);
+        tmem_wait_ld();
+        if (r < p.Lk) store_row32(dvr + ch * 32, v, 1.f);
+        tmem_ld32(tmem + lane_base + kSbDk + ch * 32, v);
+        tmem_wait_ld();
+        if (r < p.Lk) store_row32(dkr + ch * 32, v, a.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dkv_free);
+    }
+  }
+
+  if (*abort_flag && warp == 4 && lane == 0) {
+    for (int i = kv_issued - 2; i < kv_issued; ++i)
+      if (i >= 0) (void)wait_teardown(&bars->kv_full[i & 1], (i >> 1) & 1);
+    for (int i = qd_issued - 2; i < qd_issued; ++i)
+      if (i >= 0) (void)wait_teardown(&bars->qd_full[i & 1], (i >> 1) & 1);
+  }
+  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
+    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
 template <typename K>
 cudaError_t launch_one(K kernel, size_t smem, long long grid, const LongMaps &maps,
                        const Problem &p, const BwdArgs &a, cudaStream_t stream) {
@@ -772,9 +1103,15 @@ cudaError_t launch_bwd_tc_impl(const LongMaps &maps, const Problem &p, const Bwd
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a,
+cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a, int num_sms,
                           cudaStream_t stream) {
   if (p.dk == 128) return launch_bwd_tc_impl<128>(maps, p, a, stream);
+  if (p.Lq <= kT && p.Lk <= kT) {
+    // one tile each way: the fused persistent kernel (no statistics pass)
+    const long long units = static_cast<long long>(p.B) * p.Hkv;
+    return launch_one(bwd_short_tc_kernel, kSbSmem, units < num_sms ? units : num_sms, maps, p,
+                      a, stream);
+  }
   return launch_bwd_tc_impl<64>(maps, p, a, stream);
 }
 

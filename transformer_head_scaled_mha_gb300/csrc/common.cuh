@@ -87,7 +87,7 @@ struct BwdArgs {
 cudaError_t launch_bwd_simt(const BwdArgs &a, const Problem &p, bool bf16, cudaStream_t stream);
 // bf16, d in {64, 128}: maps q, k, v and (in the `o` slot) dout, box
 // (64, 128, 1, 1)
-cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a,
+cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a, int num_sms,
                           cudaStream_t stream);
 
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);

@@ -389,7 +389,9 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
                     make_map(&m.v, v, d_v, Lk, H_kv, B, layout, 128, 1) &&
                     make_map(&m.o, dout, d_v, Lq, H, B, layout, 128, 1);
     if (!ok) return MHA_ERR_CUDA;
-    err = launch_bwd_tc(m, p, a, stream);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return MHA_ERR_CUDA;
+    err = launch_bwd_tc(m, p, a, sms, stream);
   } else {
     err = launch_bwd_simt(a, p, false, stream);
   }
