@@ -939,9 +939,11 @@ def run_backward(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": recorded_traffic(args.workload),
-                "traffic_kernel": "bwd_dkdv_tc_kernel (the largest share of the call)",
-                "kernel": "bwd_stats_tc_kernel + bwd_dq_tc_kernel + bwd_dkdv_tc_kernel "
-                          "(one mha_bwd call, 3 launches)",
+                "traffic_kernel": "bwd_short_tc_kernel" if spec["dk"] == 64 and Lq <= 128 and
+                                  Lk <= 128 else "bwd_dkdv_tc_kernel (the largest share of the call)",
+                "kernel": "bwd_short_tc_kernel (one launch)" if spec["dk"] == 64 and Lq <= 128
+                          and Lk <= 128 else "bwd_stats_tc_kernel + bwd_dq_tc_kernel + "
+                          "bwd_dkdv_tc_kernel (one mha_bwd call, 3 launches)",
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback", "algorithmic_flops": flops}
 
@@ -1005,13 +1007,12 @@ def run_backward(args):
                        "scale": scale,
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
                              % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graph of %d calls (3 launches each), CUDA events"
-                                 % args.steps,
+                       "timing": "CUDA graph of %d mha_bwd calls, CUDA events" % args.steps,
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (1 if spec["dk"] == 64 and Lq <= 128 and Lk <= 128 else 3) * args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "clocks": clocks,
