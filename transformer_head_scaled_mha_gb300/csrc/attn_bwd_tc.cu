@@ -21,9 +21,11 @@
 //          and dQ += dS K_j reads it from TMEM as the A operand.  S is
 //          double-buffered, so S_{j+1} overlaps the softmax of tile j
 //   dkdv   per 128 keys of a key/value head, over the query tiles of every
-//          query head of the group: S^T = K Q^T and dP^T = V dout^T (keys on
-//          the lanes), then thread = key forms w^T and dS^T (bf16) over them
-//          in TMEM, and dV += w^T dout, dK += dS^T Q read them as A operands
+//          query head of the group, 64 queries at a time: S^T = K Q^T and
+//          dP^T = V dout^T (keys on the lanes), then thread = key forms w^T
+//          and dS^T (bf16) over them in TMEM, and dV += w^T dout,
+//          dK += dS^T Q read them as A operands; two score buffers let one
+//          half's softmax overlap the other half's products
 //
 // Warp roles (192 threads): warps 0-3 softmax (thread r = TMEM lane r),
 // warp 4 TMA producer, warp 5 TMEM owner and MMA issuer.  Operand tiles are
@@ -513,18 +515,42 @@ struct DkdvCfg {
   static constexpr int kStat = 2 * kT * 4;          // lse and D of one query tile
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(2 + 2 * kSlots) * Geo<D>::kTile +
                                   static_cast<size_t>(kSlots) * kStat + 512;
-  // TMEM: S^T (w^T bf16 over it), dP^T (dS^T bf16 over it), dV, dK
+  // TMEM, per 64-query half h of a query tile: S^T_h at 64 h (w^T bf16 over
+  // it), dP^T_h at 128 + 64 h (dS^T bf16 over it); then dV, dK
   static constexpr uint32_t kS = 0, kDp = 128, kDv = 256, kDk = 256 + D;
 };
 struct DkdvBars {
   uint64_t kv_full;
   uint64_t qd_full[kMaxSlots], qd_empty[kMaxSlots];
-  uint64_t sdp_full;  // S^T and dP^T in TMEM
-  uint64_t pds_full;  // w^T and dS^T in TMEM (softmax threads)
+  uint64_t sdp_full[2];  // S^T_h and dP^T_h in TMEM
+  uint64_t pds_full[2];  // w^T_h and dS^T_h in TMEM (softmax threads)
+  uint64_t pd_free[2];   // dV, dK products of half h done reading them
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
 };
+constexpr int kDkdvThreads = 224;
+
+// w^T and dS^T over 32 query columns for the calling thread's key: sv, pv the
+// thread's S^T and dP^T row, st the columns' lse (D kT floats further on),
+// columns lo <= e < hi allowed (others weight 0)
+__device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32],
+                                           const float *st, int lo, int hi, float scale_log2,
+                                           uint32_t (&pw)[16], uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float4 l4 = *reinterpret_cast<const float4 *>(st + (e & ~3));
+    const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + (e & ~3));
+    const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
+    const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
+    const bool oka = e >= lo && e < hi, okb = e + 1 >= lo && e + 1 < hi;
+    const float w0 = oka ? ex2_approx(__uint_as_float(sv[e]) * scale_log2 - la) : 0.f;
+    const float w1 = okb ? ex2_approx(__uint_as_float(sv[e + 1]) * scale_log2 - lb) : 0.f;
+    pw[e >> 1] = pack_bf16x2(w0, w1);
+    pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
+                             w1 * (__uint_as_float(pv[e + 1]) - db));
+  }
+}
 
 // query tiles [t_lo, t_hi) that can read some key of [k0, k0 + 128)
 __device__ __forceinline__ void query_tiles(const Problem &p, int len, int k0, int &t_lo,
@@ -539,8 +565,15 @@ __device__ __forceinline__ void query_tiles(const Problem &p, int len, int k0, i
   if (t_lo > t_hi) t_lo = t_hi;
 }
 
+// Each query tile is taken as two 64-query halves (N = 64 score products), so
+// that with dV and dK holding 2 x D TMEM columns two score buffers still fit:
+// the softmax of one half runs while the tensor core computes the other
+// half's scores or the previous half's gradients.  Two warps issue -- the
+// score products S^T_h = K Q_h^T, dP^T_h = V dout_h^T (warp 5) and the
+// gradient products dV += w^T_h dout_h, dK += dS^T_h Q_h (warp 6) -- so that
+// the smaller products do not serialise on one issuing thread.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -572,8 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qd_full[s], 1);
       mbar_init(&bars->qd_empty[s], 1);
     }
-    mbar_init(&bars->sdp_full, 1);
-    mbar_init(&bars->pds_full, kWg);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bars->sdp_full[h], 1);
+      mbar_init(&bars->pds_full[h], kWg);
+      mbar_init(&bars->pd_free[h], 1);
+    }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -602,15 +638,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < nw; ++w) {
         const int s = w % C::kSlots, r = w / C::kSlots;
         const int h = hk * group + w / per_head, q0 = (t_lo + w % per_head) * kT;
+        // the tile's lse and D (rows past Lq: weight 0), all in flight at once
+        // and before the slot is free, so that their latency hides in the wait
+        const size_t row0 = (static_cast<size_t>(b) * p.H + h) * p.Lq;
+        float lse_r[kT / 32], dsum_r[kT / 32];
+#pragma unroll
+        for (int i = 0; i < kT / 32; ++i) {
+          const int e = lane + 32 * i;
+          const bool in = q0 + e < p.Lq;
+          lse_r[i] = in ? a.lse[row0 + q0 + e] : INFINITY;
+          dsum_r[i] = in ? a.dsum[row0 + q0 + e] : 0.f;
+        }
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->qd_empty[s], (r & 1) ^ 1, abort_flag)))
           break;
-        // the tile's lse and D (rows past Lq: weight 0)
         float *st = stat + s * (C::kStat / 4);
-        const size_t row0 = (static_cast<size_t>(b) * p.H + h) * p.Lq;
-        for (int e = lane; e < kT; e += 32) {
-          const bool in = q0 + e < p.Lq;
-          st[e] = in ? a.lse[row0 + q0 + e] : INFINITY;
-          st[kT + e] = in ? a.dsum[row0 + q0 + e] : 0.f;
+#pragma unroll
+        for (int i = 0; i < kT / 32; ++i) {
+          st[lane + 32 * i] = lse_r[i];
+          st[kT + lane + 32 * i] = dsum_r[i];
         }
         __syncwarp();
         if (lane == 0) {
@@ -626,31 +671,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 5) {
-    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
-    const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
-    bool ok = nw == 0 || mbar_wait(&bars->kv_full, 0, abort_flag);
+    // ---- score products of each half: S^T_h = K Q_h^T, dP^T_h = V dout_h^T --
+    const uint32_t idesc_s = idesc_bf16_f32(128, 64, 0);
+    bool ok = nw == 0 || __all_sync(0xffffffffu, mbar_wait(&bars->kv_full, 0, abort_flag));
     for (int w = 0; ok && w < nw; ++w) {
       const int s = w % C::kSlots, r = w / C::kSlots;
-      if (!(ok = mbar_wait(&bars->qd_full[s], r & 1, abort_flag))) break;
-      tc_fence_after();
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->qd_full[s], r & 1, abort_flag)))) break;
       const uint32_t sq = smem_addr(qd_smem + 2 * s * Geo<D>::kTile);
       const uint32_t sdo = sq + Geo<D>::kTile;
-      if (lane == 0) {
-        mma_scores<D>(tmem + C::kS, smem_addr(k_smem), sq, idesc_s);    // S^T = K Q^T
-        mma_scores<D>(tmem + C::kDp, smem_addr(v_smem), sdo, idesc_s);  // dP^T = V dout^T
-        tc_commit(&bars->sdp_full);
+      for (int h = 0; h < 2; ++h) {
+        // half h's buffers: the gradient products of the previous tile's half h are done
+        if (w >= 1 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(&bars->pd_free[h], (w - 1) & 1, abort_flag))))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          // rows 64 h .. 64 h + 63 of each [128 x 64] block of Q and dout
+          mma_scores<D>(tmem + C::kS + 64 * h, smem_addr(k_smem), sq + h * 64 * 128, idesc_s);
+          mma_scores<D>(tmem + C::kDp + 64 * h, smem_addr(v_smem), sdo + h * 64 * 128, idesc_s);
+          tc_commit(&bars->sdp_full[h]);
+        }
+        __syncwarp();
+        last_commit = &bars->sdp_full[h];
+        last_parity = w & 1;
       }
-      __syncwarp();
-      if (!(ok = mbar_wait(&bars->pds_full, w & 1, abort_flag))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        mma_grad<D>(tmem + C::kDv, tmem + C::kS, sdo, idesc_g, w > 0);  // dV += w^T dout
-        mma_grad<D>(tmem + C::kDk, tmem + C::kDp, sq, idesc_g, w > 0);  // dK += dS^T Q
-        tc_commit(&bars->qd_empty[s]);
+    }
+  } else if (warp == 6) {
+    // ---- gradient products: dV += w^T_h dout_h, dK += dS^T_h Q_h ----------
+    const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
+    bool ok = true;
+    for (int w = 0; ok && w < nw; ++w) {
+      const int s = w % C::kSlots;
+      const uint32_t sq = smem_addr(qd_smem + 2 * s * Geo<D>::kTile);
+      const uint32_t sdo = sq + Geo<D>::kTile;
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_full[h], w & 1, abort_flag))))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 16 queries = 8 packed columns; B: 16 query rows (MN-major)
+            const uint32_t rows = (h * 64 + kk * 16) * 128;
+            const uint32_t acc = (w > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_ts(tmem + C::kDv, tmem + C::kS + 64 * h + kk * 8,
+                      smem_desc_sw128(sdo + rows, Geo<D>::kBlk, 1024), idesc_g, acc);
+            tc_mma_ts(tmem + C::kDk, tmem + C::kDp + 64 * h + kk * 8,
+                      smem_desc_sw128(sq + rows, Geo<D>::kBlk, 1024), idesc_g, acc);
+          }
+          tc_commit(&bars->pd_free[h]);
+          if (h == 1) tc_commit(&bars->qd_empty[s]);
+        }
+        __syncwarp();
+        last_commit = &bars->pd_free[h];
+        last_parity = w & 1;
       }
-      __syncwarp();
-      last_commit = &bars->qd_empty[s];
-      last_parity = r & 1;
     }
     if (ok && nw > 0 && lane == 0) tc_commit(&bars->done);
     __syncwarp();
@@ -666,45 +741,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.mask & kMaskQueryPadding) i_max = min(i_max, len);
     if (!key_ok) i_max = i_min;
     bool ok = true;
-    for (int w = 0; w < nw; ++w) {
+    for (int w = 0; ok && w < nw; ++w) {
       const int s = w % C::kSlots;
       const int q0 = (t_lo + w % per_head) * kT;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sdp_full, w & 1, abort_flag));
-      // the lse and D the producer stored before arriving on qd_full
-      if (ok)
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&bars->qd_full[s], (w / C::kSlots) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
       const float *st = stat + s * (C::kStat / 4);
-      const uint32_t s_t = tmem + lane_base + C::kS, dp_t = tmem + lane_base + C::kDp;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[32], pv[32], pw[16], pd[16];
-        tmem_ld32(s_t + ch * 32, sv);
-        tmem_ld32(dp_t + ch * 32, pv);
+      for (int h = 0; h < 2; ++h) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sdp_full[h], w & 1, abort_flag));
+        // the lse and D the producer stored before arriving on qd_full
+        if (ok && h == 0)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(&bars->qd_full[s], (w / C::kSlots) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_t = tmem + lane_base + C::kS + 64 * h;
+        const uint32_t dp_t = tmem + lane_base + C::kDp + 64 * h;
+        // the second chunk loads from TMEM while the first computes; the packed
+        // stores of the first land on columns the load in flight does not read
+        uint32_t sv[2][32], pv[2][32];
+        tmem_ld32(s_t, sv[0]);
+        tmem_ld32(dp_t, pv[0]);
         tmem_wait_ld();
-        const int c0 = q0 + ch * 32;
-        const int lo = i_min - c0, hi = i_max - c0;  // columns lo <= e < hi are allowed
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(st + ch * 32 + (e & ~3));
-          const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + ch * 32 + (e & ~3));
-          const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
-          const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
-          const bool oka = e >= lo && e < hi, okb = e + 1 >= lo && e + 1 < hi;
-          const float w0 = oka ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - la) : 0.f;
-          const float w1 = okb ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lb) : 0.f;
-          pw[e >> 1] = pack_bf16x2(w0, w1);
-          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
-                                   w1 * (__uint_as_float(pv[e + 1]) - db));
+        for (int ch = 0; ch < 2; ++ch) {
+          if (ch == 0) {
+            tmem_ld32(s_t + 32, sv[1]);
+            tmem_ld32(dp_t + 32, pv[1]);
+          }
+          uint32_t pw[16], pd[16];
+          const int c0 = q0 + h * 64 + ch * 32;  // first query of the chunk
+          dkdv_chunk(sv[ch], pv[ch], st + h * 64 + ch * 32, i_min - c0, i_max - c0,
+                     p.scale_log2, pw, pd);
+          tmem_st16(s_t + ch * 16, pw);
+          tmem_st16(dp_t + ch * 16, pd);
+          if (ch == 0) tmem_wait_ld();
         }
-        tmem_st16(s_t + ch * 16, pw);
-        tmem_st16(dp_t + ch * 16, pd);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->pds_full[h]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->pds_full);
     }
     // warp-collective TMEM loads by every thread; keys inside the tensor stored
     const bool key = j < p.Lk;
@@ -736,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx >= 0) (void)wait_teardown(&bars->qd_full[idx % C::kSlots], (idx / C::kSlots) & 1);
     if (nw > 0) (void)wait_teardown(&bars->kv_full, 0);
   }
-  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
+  if (*abort_flag && (warp == 5 || warp == 6) && lane == 0 && last_commit != nullptr)
     (void)wait_teardown(last_commit, last_parity);
   if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
   tc_fence_before();
@@ -1076,13 +1150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename K>
 cudaError_t launch_one(K kernel, size_t smem, long long grid, const LongMaps &maps,
-                       const Problem &p, const BwdArgs &a, cudaStream_t stream) {
+                       const Problem &p, const BwdArgs &a, cudaStream_t stream,
+                       int threads = kThreads) {
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(maps, p, a);
+  kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(maps, p, a);
   return cudaGetLastError();
 }
 
@@ -1098,7 +1173,8 @@ cudaError_t launch_bwd_tc_impl(const LongMaps &maps, const Problem &p, const Bwd
   if (e != cudaSuccess) return e;
   e = launch_one(bwd_dq_tc_kernel<D>, DqCfg<D>::kSmem, q_grid, maps, p, a, stream);
   if (e != cudaSuccess) return e;
-  return launch_one(bwd_dkdv_tc_kernel<D>, DkdvCfg<D>::kSmem, k_grid, maps, p, a, stream);
+  return launch_one(bwd_dkdv_tc_kernel<D>, DkdvCfg<D>::kSmem, k_grid, maps, p, a, stream,
+                    kDkdvThreads);
 }
 
 }  // namespace
