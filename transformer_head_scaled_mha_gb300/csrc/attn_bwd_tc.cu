@@ -297,6 +297,37 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 5) tmem_dealloc(tmem, 256);
 }
 
+// dS = w (dP - D) over 32 key columns for the calling thread's row: sv, pv the
+// row's S and dP, columns c < lim allowed (others weight 0), lse and D the
+// row's.  A chunk the whole warp may read takes packed fp32 pairs, no mask.
+__device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32],
+                                         int lim, float scale_log2, float lse, float dd,
+                                         uint32_t (&pk)[16]) {
+  if (__all_sync(0xffffffffu, lim >= 32)) {
+    const uint64_t sc = f2_pack(scale_log2, scale_log2), nl = f2_pack(-lse, -lse);
+    const uint64_t d2 = f2_pack(dd, dd);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float x0, x1, g0, g1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc, nl),
+                x0, x1);
+      const float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
+      f2_unpack(f2_mul(f2_pack(w0, w1),
+                       f2_sub(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), d2)),
+                g0, g1);
+      pk[e >> 1] = pack_bf16x2(g0, g1);
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float w0 = e < lim ? ex2_approx(__uint_as_float(sv[e]) * scale_log2 - lse) : 0.f;
+    const float w1 = e + 1 < lim ? ex2_approx(__uint_as_float(sv[e + 1]) * scale_log2 - lse) : 0.f;
+    pk[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                             w1 * (__uint_as_float(pv[e + 1]) - dd));
+  }
+}
+
 // ============================================================================
 // dq: per 128 query rows, over the key tiles
 // ============================================================================
@@ -451,22 +482,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t s_t = tmem + lane_base + C::kS + (j & 1) * kT;
       const uint32_t dp_t = tmem + lane_base + C::kDp;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[32], pv[32], pk[16];
-        tmem_ld32(s_t + ch * 32, sv);
-        tmem_ld32(dp_t + ch * 32, pv);
-        tmem_wait_ld();
-        const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
+      // chunk ch + 1 loads from TMEM while chunk ch computes; the packed dS of
+      // chunk ch lands on dP columns no load in flight reads
+      uint32_t sv[2][32], pv[2][32];
+      tmem_ld32(s_t, sv[0]);
+      tmem_ld32(dp_t, pv[0]);
+      tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float w0 = e < lim ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse) : 0.f;
-          const float w1 =
-              e + 1 < lim ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse) : 0.f;
-          pk[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
-                                   w1 * (__uint_as_float(pv[e + 1]) - dd));
+      for (int ch = 0; ch < 4; ++ch) {
+        if (ch < 3) {
+          tmem_ld32(s_t + (ch + 1) * 32, sv[(ch + 1) & 1]);
+          tmem_ld32(dp_t + (ch + 1) * 32, pv[(ch + 1) & 1]);
         }
+        uint32_t pk[16];
+        const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
+        dq_chunk(sv[ch & 1], pv[ch & 1], lim, p.scale_log2, lse, dd, pk);
         tmem_st16(dp_t + ch * 16, pk);
+        if (ch < 3) tmem_wait_ld();
       }
       tmem_wait_st();
       tc_fence_before();
@@ -512,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 struct DkdvCfg {
   static constexpr int kSlots = D == 128 ? 2 : 4;  // ring of (Q tile, dout tile) pairs
-  static constexpr int kStat = 2 * kT * 4;          // lse and D of one query tile
+  static constexpr int kStat = 2 * kT * 4;          // -lse and D of one query tile
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(2 + 2 * kSlots) * Geo<D>::kTile +
                                   static_cast<size_t>(kSlots) * kStat + 512;
   // TMEM, per 64-query half h of a query tile: S^T_h at 64 h (w^T bf16 over
@@ -532,11 +564,43 @@ struct DkdvBars {
 constexpr int kDkdvThreads = 224;
 
 // w^T and dS^T over 32 query columns for the calling thread's key: sv, pv the
-// thread's S^T and dP^T row, st the columns' lse (D kT floats further on),
-// columns lo <= e < hi allowed (others weight 0)
+// thread's S^T and dP^T row, st the columns' negated lse (their D kT floats
+// further on), columns lo <= e < hi allowed (others weight 0).  A chunk the
+// whole warp may read takes packed fp32 pairs and no mask.
 __device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32],
                                            const float *st, int lo, int hi, float scale_log2,
                                            uint32_t (&pw)[16], uint32_t (&pd)[16]) {
+  if (__all_sync(0xffffffffu, lo <= 0 && hi >= 32)) {
+    const uint64_t sc = f2_pack(scale_log2, scale_log2);
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 l4 = *reinterpret_cast<const float4 *>(st + e);
+      const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + e);
+      float x0, x1, x2, x3;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc,
+                       f2_pack(l4.x, l4.y)),
+                x0, x1);
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), sc,
+                       f2_pack(l4.z, l4.w)),
+                x2, x3);
+      const float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
+      const float w2 = ex2_approx(x2), w3 = ex2_approx(x3);
+      float g0, g1, g2, g3;
+      f2_unpack(f2_mul(f2_pack(w0, w1),
+                       f2_sub(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
+                              f2_pack(d4.x, d4.y))),
+                g0, g1);
+      f2_unpack(f2_mul(f2_pack(w2, w3),
+                       f2_sub(f2_pack(__uint_as_float(pv[e + 2]), __uint_as_float(pv[e + 3])),
+                              f2_pack(d4.z, d4.w))),
+                g2, g3);
+      pw[e >> 1] = pack_bf16x2(w0, w1);
+      pw[(e >> 1) + 1] = pack_bf16x2(w2, w3);
+      pd[e >> 1] = pack_bf16x2(g0, g1);
+      pd[(e >> 1) + 1] = pack_bf16x2(g2, g3);
+    }
+    return;
+  }
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
     const float4 l4 = *reinterpret_cast<const float4 *>(st + (e & ~3));
@@ -544,8 +608,8 @@ __device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint3
     const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
     const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
     const bool oka = e >= lo && e < hi, okb = e + 1 >= lo && e + 1 < hi;
-    const float w0 = oka ? ex2_approx(__uint_as_float(sv[e]) * scale_log2 - la) : 0.f;
-    const float w1 = okb ? ex2_approx(__uint_as_float(sv[e + 1]) * scale_log2 - lb) : 0.f;
+    const float w0 = oka ? ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, la)) : 0.f;
+    const float w1 = okb ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), scale_log2, lb)) : 0.f;
     pw[e >> 1] = pack_bf16x2(w0, w1);
     pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
                              w1 * (__uint_as_float(pv[e + 1]) - db));
@@ -582,7 +646,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   uint8_t *k_smem = smem;                        // K tile
   uint8_t *v_smem = k_smem + Geo<D>::kTile;      // V tile
   uint8_t *qd_smem = v_smem + Geo<D>::kTile;     // kSlots x (Q tile, dout tile)
-  float *stat = reinterpret_cast<float *>(qd_smem + 2 * C::kSlots * Geo<D>::kTile);  // lse, D
+  float *stat = reinterpret_cast<float *>(qd_smem + 2 * C::kSlots * Geo<D>::kTile);  // -lse, D
   DkdvBars *bars = reinterpret_cast<DkdvBars *>(reinterpret_cast<uint8_t *>(stat) +
                                                 C::kSlots * C::kStat);
   volatile int *abort_flag = &bars->abort_flag;
@@ -638,7 +702,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       for (int w = 0; w < nw; ++w) {
         const int s = w % C::kSlots, r = w / C::kSlots;
         const int h = hk * group + w / per_head, q0 = (t_lo + w % per_head) * kT;
-        // the tile's lse and D (rows past Lq: weight 0), all in flight at once
+        // the tile's -lse and D (rows past Lq: weight 0), all in flight at once
         // and before the slot is free, so that their latency hides in the wait
         const size_t row0 = (static_cast<size_t>(b) * p.H + h) * p.Lq;
         float lse_r[kT / 32], dsum_r[kT / 32];
@@ -646,7 +710,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         for (int i = 0; i < kT / 32; ++i) {
           const int e = lane + 32 * i;
           const bool in = q0 + e < p.Lq;
-          lse_r[i] = in ? a.lse[row0 + q0 + e] : INFINITY;
+          lse_r[i] = in ? -a.lse[row0 + q0 + e] : -INFINITY;  // negated
           dsum_r[i] = in ? a.dsum[row0 + q0 + e] : 0.f;
         }
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->qd_empty[s], (r & 1) ^ 1, abort_flag)))
