@@ -168,8 +168,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
+  const int nqb = (p.Lq + kT - 1) / kT;
   const int bh = static_cast<int>(blockIdx.x % BH);
-  const int q0 = static_cast<int>(blockIdx.x / BH) * kT;
+  const int q0 = (nqb - 1 - static_cast<int>(blockIdx.x / BH)) * kT;  // heaviest (causal) first
   const int b = bh / p.H, h = bh % p.H, hk = h / (p.H / p.Hkv);
   const int len = clamp_len(p, b);
   const int nt = key_tiles(p, len, q0);
@@ -333,15 +334,19 @@ __device__ __forceinline__ void dq_chunk(const uint32_t (&sv)[32], const uint32_
 // ============================================================================
 template <int D>
 struct DqCfg {
-  static constexpr int kSlots = D == 128 ? 2 : 4;  // ring of (K, V) tile pairs
+  // separate K and V rings: K_j is read until dQ_j, V_j only until dP_j, so a
+  // third K slot lets K_{j+2} load while dQ_j still holds K_j
+  static constexpr int kKSlots = D == 128 ? 3 : 4;
+  static constexpr int kVSlots = D == 128 ? 2 : 4;
   static constexpr size_t kSmem =
-      1024 + static_cast<size_t>(2 + 2 * kSlots) * Geo<D>::kTile + 512;
+      1024 + static_cast<size_t>(2 + kKSlots + kVSlots) * Geo<D>::kTile + 512;
   // TMEM: S0, S1, dP (dS bf16 over its first 64 columns), dQ
   static constexpr uint32_t kS = 0, kDp = 256, kDq = 384;
 };
 struct DqBars {
   uint64_t qdo_full;
-  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
+  uint64_t k_full[kMaxSlots], k_empty[kMaxSlots];
+  uint64_t v_full[kMaxSlots], v_empty[kMaxSlots];
   uint64_t sdp_full;  // S_j and dP_j in TMEM
   uint64_t ds_full;   // dS_j in TMEM (softmax threads)
   uint64_t dq_done;
@@ -358,8 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *q_smem = smem;                           // Q tile
   uint8_t *do_smem = q_smem + Geo<D>::kTile;        // dout tile
-  uint8_t *kv_smem = do_smem + Geo<D>::kTile;       // kSlots x (K tile, V tile)
-  DqBars *bars = reinterpret_cast<DqBars *>(kv_smem + 2 * C::kSlots * Geo<D>::kTile);
+  uint8_t *k_smem = do_smem + Geo<D>::kTile;        // kKSlots K tiles
+  uint8_t *v_smem = k_smem + C::kKSlots * Geo<D>::kTile;  // kVSlots V tiles
+  DqBars *bars = reinterpret_cast<DqBars *>(v_smem + C::kVSlots * Geo<D>::kTile);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -374,9 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->qdo_full, 1);
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < C::kKSlots; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->sdp_full, 1);
     mbar_init(&bars->ds_full, kWg);
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  int issued = 0;
+  int k_issued = 0, v_issued = 0;
   uint64_t *last_commit = nullptr;
   uint32_t last_parity = 0;
 
@@ -404,17 +414,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(do_smem + blk * Geo<D>::kBlk, &maps.o, &bars->qdo_full, blk * 64, q0, h, b);
       }
       for (int j = 0; j < nt; ++j) {
-        const int s = j % C::kSlots, r = j / C::kSlots;
-        if (!mbar_wait(&bars->kv_empty[s], (r & 1) ^ 1, abort_flag)) break;
-        uint8_t *dst = kv_smem + 2 * s * Geo<D>::kTile;
-        mbar_arrive_expect_tx(&bars->kv_full[s], 2 * Geo<D>::kTile);
-        for (int blk = 0; blk < D / 64; ++blk) {
-          tma_load_4d(dst + blk * Geo<D>::kBlk, &maps.k, &bars->kv_full[s], blk * 64, j * kT, hk,
-                      b);
-          tma_load_4d(dst + Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.v, &bars->kv_full[s],
+        const int sk = j % C::kKSlots, rk = j / C::kKSlots;
+        const int sv = j % C::kVSlots, rv = j / C::kVSlots;
+        if (!mbar_wait(&bars->k_empty[sk], (rk & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars->k_full[sk], Geo<D>::kTile);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(k_smem + sk * Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.k, &bars->k_full[sk],
                       blk * 64, j * kT, hk, b);
-        }
-        issued = j + 1;
+        k_issued = j + 1;
+        if (!mbar_wait(&bars->v_empty[sv], (rv & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars->v_full[sv], Geo<D>::kTile);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(v_smem + sv * Geo<D>::kTile + blk * Geo<D>::kBlk, &maps.v, &bars->v_full[sv],
+                      blk * 64, j * kT, hk, b);
+        v_issued = j + 1;
       }
     }
   } else if (warp == 5) {
@@ -422,21 +435,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
     const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
     const uint32_t sq = smem_addr(q_smem), sdo = smem_addr(do_smem);
-    auto k_tile = [&](int j) { return smem_addr(kv_smem + 2 * (j % C::kSlots) * Geo<D>::kTile); };
-    auto v_tile = [&](int j) { return k_tile(j) + Geo<D>::kTile; };
-    auto wait_kv = [&](int j) {
-      return mbar_wait(&bars->kv_full[j % C::kSlots], (j / C::kSlots) & 1, abort_flag);
+    auto k_tile = [&](int j) { return smem_addr(k_smem + (j % C::kKSlots) * Geo<D>::kTile); };
+    auto v_tile = [&](int j) { return smem_addr(v_smem + (j % C::kVSlots) * Geo<D>::kTile); };
+    auto wait_k = [&](int j) {
+      return mbar_wait(&bars->k_full[j % C::kKSlots], (j / C::kKSlots) & 1, abort_flag);
     };
-    bool ok = nt == 0 || (mbar_wait(&bars->qdo_full, 0, abort_flag) && wait_kv(0));
+    auto wait_v = [&](int j) {
+      return mbar_wait(&bars->v_full[j % C::kVSlots], (j / C::kVSlots) & 1, abort_flag);
+    };
+    bool ok = nt == 0 || (mbar_wait(&bars->qdo_full, 0, abort_flag) && wait_k(0) && wait_v(0));
     if (ok && nt > 0) {
       tc_fence_after();
       if (lane == 0) {
         mma_scores<D>(tmem + C::kS, sq, k_tile(0), idesc_s);
         mma_scores<D>(tmem + C::kDp, sdo, v_tile(0), idesc_s);
         tc_commit(&bars->sdp_full);
+        tc_commit(&bars->v_empty[0]);
       }
       __syncwarp();
-      if (nt > 1 && (ok = wait_kv(1))) {
+      if (nt > 1 && (ok = wait_k(1))) {
         tc_fence_after();
         if (lane == 0) mma_scores<D>(tmem + C::kS + kT, sq, k_tile(1), idesc_s);
         __syncwarp();
@@ -444,21 +461,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; ok && j < nt; ++j) {
       if (!(ok = mbar_wait(&bars->ds_full, j & 1, abort_flag))) break;
+      if (j + 1 < nt && !(ok = wait_v(j + 1))) break;
       tc_fence_after();
-      const int s = j % C::kSlots;
       if (lane == 0) {
         mma_grad<D>(tmem + C::kDq, tmem + C::kDp, k_tile(j), idesc_g, j > 0);
-        tc_commit(&bars->kv_empty[s]);
+        tc_commit(&bars->k_empty[j % C::kKSlots]);
         if (j + 1 < nt) {
           mma_scores<D>(tmem + C::kDp, sdo, v_tile(j + 1), idesc_s);
           tc_commit(&bars->sdp_full);
+          tc_commit(&bars->v_empty[(j + 1) % C::kVSlots]);
         }
       }
       __syncwarp();
-      last_commit = &bars->kv_empty[s];
-      last_parity = (j / C::kSlots) & 1;
+      if (j + 1 < nt) {
+        last_commit = &bars->v_empty[(j + 1) % C::kVSlots];
+        last_parity = ((j + 1) / C::kVSlots) & 1;
+      } else {
+        last_commit = &bars->k_empty[j % C::kKSlots];
+        last_parity = (j / C::kKSlots) & 1;
+      }
       if (j + 2 < nt) {
-        if (!(ok = wait_kv(j + 2))) break;
+        if (!(ok = wait_k(j + 2))) break;
         tc_fence_after();
         if (lane == 0) mma_scores<D>(tmem + C::kS + (j & 1) * kT, sq, k_tile(j + 2), idesc_s);
         __syncwarp();
@@ -525,8 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (*abort_flag && warp == 4 && lane == 0) {
-    for (int idx = issued - C::kSlots; idx < issued; ++idx)
-      if (idx >= 0) (void)wait_teardown(&bars->kv_full[idx % C::kSlots], (idx / C::kSlots) & 1);
+    for (int idx = k_issued - C::kKSlots; idx < k_issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->k_full[idx % C::kKSlots], (idx / C::kKSlots) & 1);
+    for (int idx = v_issued - C::kVSlots; idx < v_issued; ++idx)
+      if (idx >= 0) (void)wait_teardown(&bars->v_full[idx % C::kVSlots], (idx / C::kVSlots) & 1);
     if (nt > 0) (void)wait_teardown(&bars->qdo_full, 0);
   }
   if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
