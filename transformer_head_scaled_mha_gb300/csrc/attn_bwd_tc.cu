@@ -17,15 +17,17 @@
 //          sum (moved lazily, as in the forward), lse; D from out and dout
 //          (+inf lse for a row that attends to nothing: all its weights 0)
 //   dq     per 128 query rows: S = Q K_j^T and dP = dout V_j^T, then the
-//          softmax warpgroup (thread = row) forms dS (bf16) over dP in TMEM,
-//          and dQ += dS K_j reads it from TMEM as the A operand.  S is
-//          double-buffered, so S_{j+1} overlaps the softmax of tile j
+//          softmax warpgroup (thread = row) forms dS (bf16) over S_j in
+//          TMEM, and dQ += dS K_j reads it from TMEM as the A operand.  S is
+//          double-buffered, so S_{j+1} overlaps the softmax of tile j, and
+//          dP_{j+1} goes ahead of dQ_j
 //   dkdv   per 128 keys of a key/value head, over the query tiles of every
 //          query head of the group, 64 queries at a time: S^T = K Q^T and
 //          dP^T = V dout^T (keys on the lanes), then thread = key forms w^T
 //          and dS^T (bf16) over them in TMEM, and dV += w^T dout,
 //          dK += dS^T Q read them as A operands; two score buffers let one
-//          half's softmax overlap the other half's products
+//          half's softmax overlap the other half's products, w^T forms while
+//          dP^T is computed, and dV starts before dS^T is ready
 //
 // Warp roles (192 threads): warps 0-3 softmax (thread r = TMEM lane r),
 // warp 4 TMA producer, warp 5 TMEM owner and MMA issuer.  Operand tiles are
@@ -253,12 +255,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive(&bars->s_free[j & 1]);
       const int lim = min(max(jmax - j * kT, 0), kT);
       const bool need_mask = __any_sync(0xffffffffu, lim < kT);
-      const float mt = scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
+      // positive scale: max over the raw scores, then one FMA per score (the
+      // same rounding as the weights the gradient kernels form)
+      const bool pos = p.scale_log2 > 0.f;
+      const float mt = pos ? mask_max128(sr, need_mask, 0, lim) * p.scale_log2
+                           : scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
       if (mt > m + kRescaleThreshold) {
         if (m != -INFINITY) l *= ex2_approx(m - mt);
         m = mt;
       }
-      l += exp2_sum128(sr, m, m != -INFINITY);
+      l += pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
+               : exp2_sum128(sr, m, m != -INFINITY);
     }
     if (ok && i < p.Lq) {
       const size_t row = (static_cast<size_t>(b) * p.H + h) * p.Lq + i;
@@ -340,7 +347,7 @@ struct DqCfg {
   static constexpr int kVSlots = D == 128 ? 2 : 4;
   static constexpr size_t kSmem =
       1024 + static_cast<size_t>(2 + kKSlots + kVSlots) * Geo<D>::kTile + 512;
-  // TMEM: S0, S1, dP (dS bf16 over its first 64 columns), dQ
+  // TMEM: S0, S1 (dS_j bf16 over the first 64 columns of S_j), dP, dQ
   static constexpr uint32_t kS = 0, kDp = 256, kDq = 384;
 };
 struct DqBars {
@@ -431,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 5) {
-    // S_0, dP_0, S_1; then per tile j: dQ_j, dP_{j+1}, S_{j+2}
+    // S_0, dP_0, S_1; then per tile j, once dS_j is in TMEM: dP_{j+1} (dP_j
+    // is in the softmax's registers), dQ_j, and S_{j+2} over S_j (after dQ_j
+    // read dS_j: the products of one thread run in issue order)
     const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
     const uint32_t idesc_g = idesc_bf16_f32(128, D, 1);
     const uint32_t sq = smem_addr(q_smem), sdo = smem_addr(do_smem);
@@ -464,22 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j + 1 < nt && !(ok = wait_v(j + 1))) break;
       tc_fence_after();
       if (lane == 0) {
-        mma_grad<D>(tmem + C::kDq, tmem + C::kDp, k_tile(j), idesc_g, j > 0);
-        tc_commit(&bars->k_empty[j % C::kKSlots]);
         if (j + 1 < nt) {
           mma_scores<D>(tmem + C::kDp, sdo, v_tile(j + 1), idesc_s);
           tc_commit(&bars->sdp_full);
           tc_commit(&bars->v_empty[(j + 1) % C::kVSlots]);
         }
+        mma_grad<D>(tmem + C::kDq, tmem + C::kS + (j & 1) * kT, k_tile(j), idesc_g, j > 0);
+        tc_commit(&bars->k_empty[j % C::kKSlots]);
       }
       __syncwarp();
-      if (j + 1 < nt) {
-        last_commit = &bars->v_empty[(j + 1) % C::kVSlots];
-        last_parity = ((j + 1) / C::kVSlots) & 1;
-      } else {
-        last_commit = &bars->k_empty[j % C::kKSlots];
-        last_parity = (j / C::kKSlots) & 1;
-      }
+      last_commit = &bars->k_empty[j % C::kKSlots];
+      last_parity = (j / C::kKSlots) & 1;
       if (j + 2 < nt) {
         if (!(ok = wait_k(j + 2))) break;
         tc_fence_after();
@@ -506,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_t = tmem + lane_base + C::kS + (j & 1) * kT;
       const uint32_t dp_t = tmem + lane_base + C::kDp;
       // chunk ch + 1 loads from TMEM while chunk ch computes; the packed dS of
-      // chunk ch lands on dP columns no load in flight reads
+      // chunk ch lands on S columns already in registers that no load in
+      // flight reads
       uint32_t sv[2][32], pv[2][32];
       tmem_ld32(s_t, sv[0]);
       tmem_ld32(dp_t, pv[0]);
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
         const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
         dq_chunk(sv[ch & 1], pv[ch & 1], lim, p.scale_log2, lse, dd, pk);
-        tmem_st16(dp_t + ch * 16, pk);
+        tmem_st16(s_t + ch * 16, pk);
         if (ch < 3) tmem_wait_ld();
       }
       tmem_wait_st();
@@ -579,8 +584,10 @@ struct DkdvCfg {
 struct DkdvBars {
   uint64_t kv_full;
   uint64_t qd_full[kMaxSlots], qd_empty[kMaxSlots];
-  uint64_t sdp_full[2];  // S^T_h and dP^T_h in TMEM
-  uint64_t pds_full[2];  // w^T_h and dS^T_h in TMEM (softmax threads)
+  uint64_t s_full[2];    // S^T_h in TMEM
+  uint64_t dp_full[2];   // dP^T_h in TMEM
+  uint64_t w_full[2];    // w^T_h in TMEM (softmax threads)
+  uint64_t ds_full[2];   // dS^T_h in TMEM (softmax threads)
   uint64_t pd_free[2];   // dV, dK products of half h done reading them
   uint64_t done;
   uint32_t tmem_base;
@@ -588,19 +595,18 @@ struct DkdvBars {
 };
 constexpr int kDkdvThreads = 224;
 
-// w^T and dS^T over 32 query columns for the calling thread's key: sv, pv the
-// thread's S^T and dP^T row, st the columns' negated lse (their D kT floats
-// further on), columns lo <= e < hi allowed (others weight 0).  A chunk the
-// whole warp may read takes packed fp32 pairs and no mask.
-__device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32],
-                                           const float *st, int lo, int hi, float scale_log2,
-                                           uint32_t (&pw)[16], uint32_t (&pd)[16]) {
+// w^T over 32 query columns for the calling thread's key: sv its S^T row,
+// st the columns' negated lse, columns lo <= e < hi allowed (others weight
+// 0); w in fp32 (for dS) and packed bf16 pairs (the dV operand).  A chunk
+// the whole warp may read takes packed fp32 pairs and no mask.
+__device__ __forceinline__ void dkdv_w32(const uint32_t (&sv)[32], const float *st, int lo,
+                                         int hi, float scale_log2, float (&w)[32],
+                                         uint32_t (&pw)[16]) {
   if (__all_sync(0xffffffffu, lo <= 0 && hi >= 32)) {
     const uint64_t sc = f2_pack(scale_log2, scale_log2);
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
       const float4 l4 = *reinterpret_cast<const float4 *>(st + e);
-      const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + e);
       float x0, x1, x2, x3;
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc,
                        f2_pack(l4.x, l4.y)),
@@ -608,36 +614,45 @@ __device__ __forceinline__ void dkdv_chunk(const uint32_t (&sv)[32], const uint3
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), sc,
                        f2_pack(l4.z, l4.w)),
                 x2, x3);
-      const float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
-      const float w2 = ex2_approx(x2), w3 = ex2_approx(x3);
-      float g0, g1, g2, g3;
-      f2_unpack(f2_mul(f2_pack(w0, w1),
-                       f2_sub(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
-                              f2_pack(d4.x, d4.y))),
-                g0, g1);
-      f2_unpack(f2_mul(f2_pack(w2, w3),
-                       f2_sub(f2_pack(__uint_as_float(pv[e + 2]), __uint_as_float(pv[e + 3])),
-                              f2_pack(d4.z, d4.w))),
-                g2, g3);
-      pw[e >> 1] = pack_bf16x2(w0, w1);
-      pw[(e >> 1) + 1] = pack_bf16x2(w2, w3);
-      pd[e >> 1] = pack_bf16x2(g0, g1);
-      pd[(e >> 1) + 1] = pack_bf16x2(g2, g3);
+      w[e] = ex2_approx(x0);
+      w[e + 1] = ex2_approx(x1);
+      w[e + 2] = ex2_approx(x2);
+      w[e + 3] = ex2_approx(x3);
     }
-    return;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 l4 = *reinterpret_cast<const float4 *>(st + e);
+      const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        w[e + t] = e + t >= lo && e + t < hi
+                       ? ex2_approx(fmaf(__uint_as_float(sv[e + t]), scale_log2, l[t]))
+                       : 0.f;
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float4 l4 = *reinterpret_cast<const float4 *>(st + (e & ~3));
-    const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + (e & ~3));
-    const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
-    const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
-    const bool oka = e >= lo && e < hi, okb = e + 1 >= lo && e + 1 < hi;
-    const float w0 = oka ? ex2_approx(fmaf(__uint_as_float(sv[e]), scale_log2, la)) : 0.f;
-    const float w1 = okb ? ex2_approx(fmaf(__uint_as_float(sv[e + 1]), scale_log2, lb)) : 0.f;
-    pw[e >> 1] = pack_bf16x2(w0, w1);
-    pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
-                             w1 * (__uint_as_float(pv[e + 1]) - db));
+  for (int e = 0; e < 32; e += 2) pw[e >> 1] = pack_bf16x2(w[e], w[e + 1]);
+}
+
+// dS^T = w^T (dP^T - D) over the same 32 columns, packed bf16 pairs (the dK
+// operand); st the columns' negated lse, their D kT floats further on
+__device__ __forceinline__ void dkdv_ds32(const float (&w)[32], const uint32_t (&pv)[32],
+                                          const float *st, uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + e);
+    float g0, g1, g2, g3;
+    f2_unpack(f2_mul(f2_pack(w[e], w[e + 1]),
+                     f2_sub(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
+                            f2_pack(d4.x, d4.y))),
+              g0, g1);
+    f2_unpack(f2_mul(f2_pack(w[e + 2], w[e + 3]),
+                     f2_sub(f2_pack(__uint_as_float(pv[e + 2]), __uint_as_float(pv[e + 3])),
+                            f2_pack(d4.z, d4.w))),
+              g2, g3);
+    pd[e >> 1] = pack_bf16x2(g0, g1);
+    pd[(e >> 1) + 1] = pack_bf16x2(g2, g3);
   }
 }
 
@@ -695,8 +710,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_init(&bars->qd_empty[s], 1);
     }
     for (int h = 0; h < 2; ++h) {
-      mbar_init(&bars->sdp_full[h], 1);
-      mbar_init(&bars->pds_full[h], kWg);
+      mbar_init(&bars->s_full[h], 1);
+      mbar_init(&bars->dp_full[h], 1);
+      mbar_init(&bars->w_full[h], kWg);
+      mbar_init(&bars->ds_full[h], kWg);
       mbar_init(&bars->pd_free[h], 1);
     }
     mbar_init(&bars->done, 1);
@@ -777,11 +794,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (lane == 0) {
           // rows 64 h .. 64 h + 63 of each [128 x 64] block of Q and dout
           mma_scores<D>(tmem + C::kS + 64 * h, smem_addr(k_smem), sq + h * 64 * 128, idesc_s);
+          tc_commit(&bars->s_full[h]);
           mma_scores<D>(tmem + C::kDp + 64 * h, smem_addr(v_smem), sdo + h * 64 * 128, idesc_s);
-          tc_commit(&bars->sdp_full[h]);
+          tc_commit(&bars->dp_full[h]);
         }
         __syncwarp();
-        last_commit = &bars->sdp_full[h];
+        last_commit = &bars->dp_full[h];
         last_parity = w & 1;
       }
     }
@@ -794,17 +812,29 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const uint32_t sq = smem_addr(qd_smem + 2 * s * Geo<D>::kTile);
       const uint32_t sdo = sq + Geo<D>::kTile;
       for (int h = 0; h < 2; ++h) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_full[h], w & 1, abort_flag))))
+        // A: 16 queries = 8 packed columns; B: 16 query rows (MN-major).  dV
+        // goes as soon as w^T_h is in TMEM, dK once dS^T_h is
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->w_full[h], w & 1, abort_flag))))
           break;
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // A: 16 queries = 8 packed columns; B: 16 query rows (MN-major)
             const uint32_t rows = (h * 64 + kk * 16) * 128;
             const uint32_t acc = (w > 0 || h > 0 || kk > 0) ? 1u : 0u;
             tc_mma_ts(tmem + C::kDv, tmem + C::kS + 64 * h + kk * 8,
                       smem_desc_sw128(sdo + rows, Geo<D>::kBlk, 1024), idesc_g, acc);
+          }
+        }
+        __syncwarp();
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars->ds_full[h], w & 1, abort_flag))))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t rows = (h * 64 + kk * 16) * 128;
+            const uint32_t acc = (w > 0 || h > 0 || kk > 0) ? 1u : 0u;
             tc_mma_ts(tmem + C::kDk, tmem + C::kDp + 64 * h + kk * 8,
                       smem_desc_sw128(sq + rows, Geo<D>::kBlk, 1024), idesc_g, acc);
           }
@@ -835,7 +865,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int q0 = (t_lo + w % per_head) * kT;
       const float *st = stat + s * (C::kStat / 4);
       for (int h = 0; h < 2; ++h) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sdp_full[h], w & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[h], w & 1, abort_flag));
         // the lse and D the producer stored before arriving on qd_full
         if (ok && h == 0)
           ok = __all_sync(0xffffffffu,
@@ -844,29 +874,49 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         tc_fence_after();
         const uint32_t s_t = tmem + lane_base + C::kS + 64 * h;
         const uint32_t dp_t = tmem + lane_base + C::kDp + 64 * h;
-        // the second chunk loads from TMEM while the first computes; the packed
-        // stores of the first land on columns the load in flight does not read
-        uint32_t sv[2][32], pv[2][32];
-        tmem_ld32(s_t, sv[0]);
-        tmem_ld32(dp_t, pv[0]);
-        tmem_wait_ld();
+        const float *sth = st + h * 64;
+        const int c0 = q0 + h * 64;  // first query of the half
+        // w^T while dP^T_h is still being computed: the second 32 columns
+        // load from TMEM while the first compute, and the packed w of the
+        // first land on columns the load in flight does not read
+        float wv[2][32];
+        {
+          uint32_t sv[2][32];
+          tmem_ld32(s_t, sv[0]);
+          tmem_wait_ld();
+          tmem_ld32(s_t + 32, sv[1]);
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          if (ch == 0) {
-            tmem_ld32(s_t + 32, sv[1]);
-            tmem_ld32(dp_t + 32, pv[1]);
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t pw[16];
+            dkdv_w32(sv[ch], sth + ch * 32, i_min - (c0 + ch * 32), i_max - (c0 + ch * 32),
+                     p.scale_log2, wv[ch], pw);
+            tmem_st16(s_t + ch * 16, pw);
+            if (ch == 0) tmem_wait_ld();
           }
-          uint32_t pw[16], pd[16];
-          const int c0 = q0 + h * 64 + ch * 32;  // first query of the chunk
-          dkdv_chunk(sv[ch], pv[ch], st + h * 64 + ch * 32, i_min - c0, i_max - c0,
-                     p.scale_log2, pw, pd);
-          tmem_st16(s_t + ch * 16, pw);
-          tmem_st16(dp_t + ch * 16, pd);
-          if (ch == 0) tmem_wait_ld();
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->pds_full[h]);
+        mbar_arrive(&bars->w_full[h]);
+        // dS^T = w^T (dP^T - D)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->dp_full[h], w & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t pv[2][32];
+          tmem_ld32(dp_t, pv[0]);
+          tmem_wait_ld();
+          tmem_ld32(dp_t + 32, pv[1]);
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t pd[16];
+            dkdv_ds32(wv[ch], pv[ch], sth + ch * 32, pd);
+            tmem_st16(dp_t + ch * 16, pd);
+            if (ch == 0) tmem_wait_ld();
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->ds_full[h]);
       }
     }
     // warp-collective TMEM loads by every thread; keys inside the tensor stored
@@ -1124,8 +1174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
           tmem_wait_ld();
           const bool need_mask = __any_sync(0xffffffffu, jmax < kT);
-          const float m = scale_mask_max128(sr, p.scale_log2, need_mask, 0, jmax);
-          const float l = exp2_sum128(sr, m, m != -INFINITY);
+          const bool pos = p.scale_log2 > 0.f;
+          const float m = pos ? mask_max128(sr, need_mask, 0, jmax) * p.scale_log2
+                              : scale_mask_max128(sr, p.scale_log2, need_mask, 0, jmax);
+          const float l = pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
+                              : exp2_sum128(sr, m, m != -INFINITY);
           const float inv = l > 0.f ? 1.f / l : 0.f;
           st[r] = l > 0.f ? m + __log2f(l) : INFINITY;
           st[kT + r] = dd;
