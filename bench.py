@@ -18,7 +18,9 @@ value  device throughput, inputs resident in HBM; K launches captured in one
        finds its inputs in L2.
 e2e    the same metric through the public call with host buffers: pinned
        host -> device copies of Q, K, V (and lengths), mha_fwd, device -> host
-       copy of the output, every step, inside the timed region.
+       copy of the output, every step, inside the timed region; two device
+       buffer slots and separate copy streams let step i+1's inputs arrive and
+       step i-1's output leave while step i computes.
 --impl reference   times the fp64 CPU oracle (the only other implementation
        of this path) on the host cores, on a bounded sample of the workload.
 
@@ -255,6 +257,66 @@ def barrier(world: int):
 
 
 # ---------------------------------------------------------------------------
+# end to end: host buffers in, result back, every step
+# ---------------------------------------------------------------------------
+E2E_PIPELINE = ("two device buffer slots, three streams: the host->device copies of step i+1 "
+                "and the device->host copy of step i-1 run while step i computes")
+
+
+def e2e_seconds_per_step(slots_in, launch, slots_out, steps, stream, world):
+    """Seconds per step of a pipelined host -> call -> host loop.
+
+    slots_in[s]  (device dst, pinned host src) pairs copied in for a step on slot s
+    launch(s, stream)  enqueues the call that reads slot s's inputs and writes
+                 its outputs
+    slots_out[s] (pinned host dst, device src) pairs copied back after the call
+    Step i uses slot i % 2.  Its input copies wait until the call of step i - 2
+    (the slot's previous user) has read the slot; its call waits for its input
+    copies and for the read-back of step i - 2 (which frees the slot's
+    outputs); its read-back waits for its call.  Every step's copies and call
+    lie between the two timing events."""
+    import torch
+    dev = stream.device
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        s = i % 2
+        if i >= 2:
+            s_in.wait_event(done[s])
+        with torch.cuda.stream(s_in):
+            for dst, src in slots_in[s]:
+                dst.copy_(src, non_blocking=True)
+        in_ready[s].record(s_in)
+        stream.wait_event(in_ready[s])
+        if i >= 2:
+            stream.wait_event(out_read[s])
+        launch(s, stream)
+        done[s].record(stream)
+        s_out.wait_event(done[s])
+        with torch.cuda.stream(s_out):
+            for dst, src in slots_out[s]:
+                dst.copy_(src, non_blocking=True)
+        out_read[s].record(s_out)
+
+    for i in range(2):  # warm-up: both slots once
+        step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(steps):
+        step(i)
+    s_out.wait_stream(stream)
+    s_out.wait_stream(s_in)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle timing (baseline / reference arm)
 # ---------------------------------------------------------------------------
 def oracle_sample_rows(spec, lens, target_flops, seed=0):
@@ -418,34 +480,24 @@ def run_ours(args):
     pq, pk, pv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
     pout = torch.empty(out_shape, dtype=hq.dtype).pin_memory()
     plen = torch.from_numpy(lens).pin_memory() if lens is not None else None
-    dq, dk_, dv_, do = sets[0]
-    dl = torch.empty_like(kl) if kl is not None else None
     h2d = sum(t.numel() * t.element_size() for t in (pq, pk, pv))
     h2d += plen.numel() * 4 if plen is not None else 0
     d2h = pout.numel() * pout.element_size()
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    # slot 0 reuses the first timed input set; slot 1 gets its own buffers
+    e2e_dev = [list(sets[0]) + [torch.empty_like(kl) if kl is not None else None]]
+    e2e_dev.append([torch.empty_like(t) if t is not None else None for t in e2e_dev[0]])
+    srcs = (pq, pk, pv)
+    slots_in = [[(d[j], srcs[j]) for j in range(3)] + ([(d[4], plen)] if plen is not None else [])
+                for d in e2e_dev]
+    slots_out = [[(pout, d[3])] for d in e2e_dev]
 
-    def e2e_step():
-        dq.copy_(pq, non_blocking=True)
-        dk_.copy_(pk, non_blocking=True)
-        dv_.copy_(pv, non_blocking=True)
-        if plen is not None:
-            dl.copy_(plen, non_blocking=True)
-        call(dq, dk_, dv_, do, dl, stream)
-        pout.copy_(do, non_blocking=True)
+    def e2e_launch(s, st):
+        d = e2e_dev[s]
+        call(d[0], d[1], d[2], d[3], d[4], st)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / e2e_steps
+    e2e_t = max_over_ranks(e2e_seconds_per_step(slots_in, e2e_launch, slots_out, e2e_steps,
+                                                stream, world), world, dev)
     e2e_value = weak_scaling_value(spec, nbytes, flops, e2e_t, world)
 
     peaks, peak_src = read_peaks()
@@ -481,7 +533,7 @@ def run_ours(args):
                        "parallelism": "weak: same workload per rank, no collective" if world > 1
                        else "1 GPU"},
             "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h)},
+                    "d2h_bytes_per_step": int(d2h), "pipeline": E2E_PIPELINE},
             "gpu_launches": args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -638,34 +690,25 @@ def run_sublayer(args):
     pm = hm.pin_memory() if hm is not None else None
     pl = torch.from_numpy(lens).pin_memory() if lens is not None else None
     pout = torch.empty((B, T, d), dtype=torch.bfloat16).pin_memory()
-    dx, dm, do = sets[0]
-    dl = torch.empty_like(kl) if kl is not None else None
     h2d = px.numel() * 2 + (pm.numel() * 2 if pm is not None else 0) + (
         pl.numel() * 4 if pl is not None else 0)
     d2h = pout.numel() * 2
+    # per slot: x, mem, out, lengths, workspace (slot 0 reuses the first set)
+    dx, dm, do = sets[0]
+    e2e_dev = [[dx, dm, do, torch.empty_like(kl) if kl is not None else None, ws]]
+    e2e_dev.append([torch.empty_like(t) if t is not None else None for t in e2e_dev[0]])
+    slots_in = [[(e[0], px)] + ([(e[1], pm)] if pm is not None else []) +
+                ([(e[3], pl)] if pl is not None else []) for e in e2e_dev]
+    slots_out = [[(pout, e[2])] for e in e2e_dev]
 
-    def e2e_step():
-        dx.copy_(px, non_blocking=True)
-        if pm is not None:
-            dm.copy_(pm, non_blocking=True)
-        if pl is not None:
-            dl.copy_(pl, non_blocking=True)
-        mha.mha_sublayer_fwd(dx, *w, *bias, mem=dm, H=H, H_kv=Hkv, mask_kind=mask,
-                             key_lengths=dl, scale=scale, workspace=ws, out=do, stream=stream)
-        pout.copy_(do, non_blocking=True)
+    def e2e_launch(s, st):
+        e = e2e_dev[s]
+        mha.mha_sublayer_fwd(e[0], *w, *bias, mem=e[1], H=H, H_kv=Hkv, mask_kind=mask,
+                             key_lengths=e[3], scale=scale, workspace=e[4], out=e[2], stream=st)
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, dev)
+    e2e_t = max_over_ranks(e2e_seconds_per_step(slots_in, e2e_launch, slots_out, e2e_steps,
+                                                stream, world), world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -689,7 +732,7 @@ def run_sublayer(args):
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "note": "weights resident on the device"},
+                    "note": "weights resident on the device", "pipeline": E2E_PIPELINE},
             "gpu_launches": 5 * args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -951,33 +994,24 @@ def run_backward(args):
     pins = [t.pin_memory() for t in ins]
     pl = torch.from_numpy(lens).pin_memory() if lens is not None else None
     pouts = [torch.empty_like(t).pin_memory() for t in (hq, hk, hv)]
-    dset = sets[0]
-    dl = torch.empty_like(kl) if kl is not None else None
     h2d = sum(t.numel() * 2 for t in pins) + (pl.numel() * 4 if pl is not None else 0)
     d2h = sum(t.numel() * 2 for t in pouts)
+    # per slot: q, k, v, out, dout, dq, dk, dv, lengths, workspace (slot 0
+    # reuses the first set)
+    e2e_dev = [list(sets[0][:8]) + [torch.empty_like(kl) if kl is not None else None, ws]]
+    e2e_dev.append([torch.empty_like(t) if t is not None else None for t in e2e_dev[0]])
+    slots_in = [list(zip(e[:5], pins)) + ([(e[8], pl)] if pl is not None else [])
+                for e in e2e_dev]
+    slots_out = [list(zip(pouts, e[5:8])) for e in e2e_dev]
 
-    def e2e_step():
-        for dst, src in zip(dset[:5], pins):
-            dst.copy_(src, non_blocking=True)
-        if pl is not None:
-            dl.copy_(pl, non_blocking=True)
-        mha.mha_bwd(*dset[:5], layout=layout, mask_kind=mask, key_lengths=dl, scale=scale,
-                    workspace=ws, dq=dset[5], dk=dset[6], dv=dset[7], stream=stream)
-        for dst, src in zip(pouts, dset[5:]):
-            dst.copy_(src, non_blocking=True)
+    def e2e_launch(s, st):
+        e = e2e_dev[s]
+        mha.mha_bwd(*e[:5], layout=layout, mask_kind=mask, key_lengths=e[8], scale=scale,
+                    workspace=e[9], dq=e[5], dk=e[6], dv=e[7], stream=st)
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / e2e_steps
+    e2e_t = max_over_ranks(e2e_seconds_per_step(slots_in, e2e_launch, slots_out, e2e_steps,
+                                                stream, world), world, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1011,7 +1045,8 @@ def run_backward(args):
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "pipeline": E2E_PIPELINE},
             "gpu_launches": (1 if spec["dk"] == 64 and Lq <= 128 and Lk <= 128 else 3) * args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
