@@ -226,3 +226,45 @@ def test_static_sublayer_rejects_shapes_beyond_its_scratch(mha):
     assert call(257) == mha.MHA_ERR_UNSUPPORTED
     assert call(-1) == mha.MHA_ERR_INVALID_ARGUMENT
     assert call(0) == mha.MHA_OK
+
+
+def test_bwd_workspace_size(mha):
+    # two fp32 values per query row, each part rounded up to 256 bytes
+    assert mha.mha_bwd_workspace_size(2, 4, 64) == 2 * (2 * 4 * 64 * 4)
+    assert mha.mha_bwd_workspace_size(1, 1, 3) == 2 * 256
+    assert mha.mha_bwd_workspace_size(0, 4, 64) == 0
+    assert mha.mha_bwd_workspace_size(2, 4, -1) == 0
+
+
+def test_bwd_rejects_before_launch(mha):
+    E_ARG, E_UNS = mha.MHA_ERR_INVALID_ARGUMENT, mha.MHA_ERR_UNSUPPORTED
+    p = [FAKE + (i << 24) for i in range(10)]
+    ws_n = mha.mha_bwd_workspace_size(2, 4, 64)
+
+    def call(q=p[0], k=p[1], v=p[2], out=p[3], dout=p[4], dq=p[5], dk=p[6], dv=p[7], B=2, H=4,
+             Hkv=2, Lq=64, Lk=64, d=64, layout=0, mask=0, kl=None, scale=0.125, dtype=1,
+             ws=p[8], ws_n=ws_n):
+        return mha.lib.mha_bwd(q, k, v, out, dout, dq, dk, dv, B, H, Hkv, Lq, Lk, d, d, layout,
+                               mask, kl, scale, dtype, ws, ws_n, None)
+    k_bytes = 2 * 2 * 64 * 64 * 2
+    assert call(layout=2) == E_ARG
+    assert call(scale=math.inf) == E_ARG
+    assert call(mask=2) == E_ARG  # key lengths missing
+    assert call(mask=1, Lk=65) == E_ARG  # causal needs Lq == Lk
+    assert call(Hkv=3) == E_ARG  # does not divide H
+    assert call(dtype=3) == E_ARG
+    assert call(d=96) == E_UNS
+    assert call(q=p[0] + 8) == E_ARG  # not 16-byte aligned
+    assert call(dout=None) == E_ARG
+    assert call(dq=None) == E_ARG
+    assert call(dv=p[7] + 8) == E_ARG
+    assert call(ws=None) == E_ARG
+    assert call(ws_n=ws_n - 1) == E_ARG
+    assert call(ws=p[8] + 16) == E_ARG  # workspace is 256-byte aligned
+    assert call(dq=p[0] + 4096) == E_ARG  # dq overlaps q
+    assert call(dk=p[7] - k_bytes + 16) == E_ARG  # dk overlaps dv
+    assert call(dv=p[4] + 64) == E_ARG  # dv overlaps dout
+    assert call(ws=p[3] + 1024) == E_ARG  # workspace overlaps out
+    assert call(mask=2, kl=p[5] + 64) == E_ARG  # lengths inside dq
+    assert call(mask=2, kl=p[8] + 64) == E_ARG  # lengths inside the workspace
+    assert call(B=0) == mha.MHA_OK  # empty: nothing to do
