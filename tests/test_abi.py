@@ -268,3 +268,91 @@ def test_bwd_rejects_before_launch(mha):
     assert call(mask=2, kl=p[5] + 64) == E_ARG  # lengths inside dq
     assert call(mask=2, kl=p[8] + 64) == E_ARG  # lengths inside the workspace
     assert call(B=0) == mha.MHA_OK  # empty: nothing to do
+
+
+class FakeCudaTensor:
+    """Stands in for a CUDA tensor in the bindings' argument checks, which read
+    only these attributes (no GPU needed; nothing is dereferenced)."""
+
+    def __init__(self, shape, dtype="bf16", device="cuda:0", contiguous=True, ptr=FAKE):
+        import torch
+        self.shape = tuple(shape)
+        self.dtype = {"bf16": torch.bfloat16, "f32": torch.float32, "i32": torch.int32,
+                      "u8": torch.uint8}[dtype]
+        self.device = torch.device(device)
+        self.is_cuda = self.device.type == "cuda"
+        self._contiguous, self._ptr = contiguous, ptr
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return self._contiguous
+
+    def data_ptr(self):
+        return self._ptr
+
+    def numel(self):
+        return math.prod(self.shape)
+
+    def element_size(self):
+        return self.dtype.itemsize
+
+
+def test_sublayer_binding_checks_every_tensor_against_the_dimensions(mha):
+    pytest.importorskip("torch")
+    F = FakeCudaTensor
+    B, T, S, d, H, Hkv, dk = 2, 16, 24, 128, 2, 1, 64
+
+    def args(**over):
+        a = dict(x=F((B, T, d)), w_q=F((d, H * dk)), w_k=F((d, Hkv * dk)), w_v=F((d, Hkv * dk)),
+                 w_o=F((H * dk, d)), b_q=F((H * dk,)), b_k=F((Hkv * dk,)), b_v=F((Hkv * dk,)),
+                 b_o=F((d,)), mem=F((B, S, d)), H=H, H_kv=Hkv, key_lengths=F((B,), "i32"),
+                 scale=None, out=F((B, T, d)))
+        a.update(over)
+        return a
+    out, dims, kl, scale, mem_ptr = mha.mha._sublayer_marshal(**args())
+    assert dims == (B, T, S, d, H, Hkv, dk, dk)
+    assert kl == FAKE and mem_ptr == FAKE and scale == pytest.approx(dk ** -0.5)
+    bad = [dict(w_q=F((d + 8, H * dk))), dict(w_k=F((d, H * dk))), dict(w_o=F((H * dk, d + 8))),
+           dict(b_o=F((d + 8,))), dict(b_q=F((dk,))), dict(mem=F((B, S, d + 8))),
+           dict(mem=F((B + 1, S, d))), dict(out=F((B, T, d + 8))), dict(out=F((B, T, d), "f32")),
+           dict(w_v=F((d, Hkv * dk), device="cuda:1")), dict(out=F((B, T, d), device="cuda:1")),
+           dict(key_lengths=F((B,), "i32", device="cuda:1")),
+           dict(key_lengths=F((B,), "i32", contiguous=False)), dict(key_lengths=F((B + 1,), "i32")),
+           dict(x=F((B, T, d), device="cpu")), dict(H=3), dict(H=0)]
+    for over in bad:
+        with pytest.raises(ValueError):
+            mha.mha._sublayer_marshal(**args(**over))
+    # self-attention: no memory tensor, S = T
+    assert mha.mha._sublayer_marshal(**args(mem=None))[1][2] == T
+    assert mha.mha._workspace_bytes(F((100,), "f32"), F((1,)).device) == 400
+    with pytest.raises(ValueError):
+        mha.mha._workspace_bytes(F((100,), "u8", device="cuda:1"), F((1,)).device)
+
+
+def test_attention_binding_checks_devices_and_lengths(mha):
+    pytest.importorskip("torch")
+    F = FakeCudaTensor
+    q, k, v, out = F((2, 4, 8, 64)), F((2, 2, 8, 64)), F((2, 2, 8, 64)), F((2, 4, 8, 64))
+    res = mha.mha._marshal(q, k, v, out, F((2,), "i32"), None, "bhsd")
+    assert res[1] == (2, 4, 2, 8, 8, 64, 64) and res[2] == FAKE
+    for bad in (dict(k=F((2, 2, 8, 64), device="cuda:1")), dict(out=F((2, 4, 8, 64), device="cuda:1")),
+                dict(kl=F((2,), "i32", device="cuda:1")), dict(kl=F((2,), "i32", contiguous=False)),
+                dict(out=F((2, 4, 8, 32)))):
+        a = dict(q=q, k=k, v=v, out=out, kl=F((2,), "i32"))
+        a.update(bad)
+        with pytest.raises(ValueError):
+            mha.mha._marshal(a["q"], a["k"], a["v"], a["out"], a["kl"], None, "bhsd")
+
+
+def test_linear_binding_checks_devices(mha):
+    pytest.importorskip("torch")
+    F = FakeCudaTensor
+    x, w = F((4, 16, 64)), F((64, 32))
+    for kw in (dict(w=F((64, 32), device="cuda:1")), dict(b=F((32,), device="cuda:1")),
+               dict(out=F((4, 16, 32), device="cuda:1")), dict(b=F((16,))), dict(w=F((48, 32)))):
+        a = dict(x=x, w=w)
+        a.update(kw)
+        with pytest.raises(ValueError):
+            mha.mha_linear_fwd(a.pop("x"), a.pop("w"), **a)

@@ -106,6 +106,26 @@ def mha_debug_status(stream=None) -> int:
     return int(lib.mha_debug_status(_stream_handle(stream)))
 
 
+def _lengths_ptr(key_lengths, B, device):
+    """Device address of the per-sequence lengths (None when not given)."""
+    import torch
+    if key_lengths is None:
+        return None
+    if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or \
+            key_lengths.numel() != B or not key_lengths.is_contiguous() or \
+            key_lengths.device != device:
+        raise ValueError("key_lengths must be a contiguous int32 CUDA tensor of shape [B] on "
+                         "the inputs' device")
+    return key_lengths.data_ptr()
+
+
+def _workspace_bytes(workspace, device):
+    """Size in bytes of a caller's workspace tensor, after checking where it lives."""
+    if not workspace.is_cuda or not workspace.is_contiguous() or workspace.device != device:
+        raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
+    return workspace.numel() * workspace.element_size()
+
+
 def _marshal(q, k, v, out, key_lengths, scale, layout):
     """Check shapes/dtypes, allocate ``out`` if needed; returns the C arguments."""
     import torch
@@ -133,15 +153,15 @@ def _marshal(q, k, v, out, key_lengths, scale, layout):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("%s must be a contiguous CUDA tensor" % name)
+        if t.device != q.device:
+            raise ValueError("%s must be on q's device" % name)
     if out is None:
         out = torch.empty(oshape, dtype=q.dtype, device=q.device)
-    elif tuple(out.shape) != oshape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous %s tensor of q's dtype" % (oshape,))
-    kl_ptr = None
-    if key_lengths is not None:
-        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
-            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
-        kl_ptr = key_lengths.data_ptr()
+    elif tuple(out.shape) != oshape or out.dtype != q.dtype or not out.is_contiguous() or \
+            out.device != q.device:
+        raise ValueError("out must be a contiguous %s tensor of q's dtype on q's device"
+                         % (oshape,))
+    kl_ptr = _lengths_ptr(key_lengths, B, q.device)
     if scale is None:
         scale = float(dk) ** -0.5
     return out, (B, H, Hkv, Lq, Lk, dk, dv), kl_ptr, float(scale), dtype
@@ -219,12 +239,13 @@ def mha_bwd(q, k, v, out, dout, *, layout: str = "bhsd", mask_kind: int = 0, key
     n = mha_bwd_workspace_size(B, H, Lq)
     if workspace is None:
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = _workspace_bytes(workspace, q.device)
     with torch.cuda.device(q.device):
         st = lib.mha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv,
                          Lq, Lk, dk_, dv_, MHA_LAYOUT_BSHD if layout == "bshd" else MHA_LAYOUT_BHSD,
-                         int(mask_kind), kl_ptr, scale, dtype, workspace.data_ptr(),
-                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
+                         int(mask_kind), kl_ptr, scale, dtype, workspace.data_ptr(), ws_bytes,
+                         _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st, "mha_bwd")
     return dq, dk, dv
@@ -250,6 +271,9 @@ def mha_linear_fwd(x, w, b=None, out=None, *, stream=None):
     K, N = w.shape
     if x.shape[-1] != K or (b is not None and b.shape[0] != N):
         raise ValueError("shape mismatch: x %s w %s" % (tuple(x.shape), tuple(w.shape)))
+    for name, t in (("w", w), ("b", b), ("out", out)):
+        if t is not None and t.device != x.device:
+            raise ValueError("%s must be on x's device" % name)
     M = x.numel() // K if K else 0
     if out is None:
         out = torch.empty(tuple(x.shape[:-1]) + (N,), dtype=x.dtype, device=x.device)
@@ -269,6 +293,51 @@ def mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v) -> int:
     return int(lib.mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v))
 
 
+def _sublayer_marshal(x, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, mem, H, H_kv, key_lengths,
+                      scale, out):
+    """Check the sublayer's tensors against one another (shapes, dtype, device);
+    returns (out, (B, T, S, d_model, H, H_kv, d_k, d_v), lengths pointer, scale,
+    memory pointer).  The library sizes every buffer from these dimensions, so
+    a tensor that disagrees with them is refused here."""
+    import torch
+    H_kv = H if H_kv is None else H_kv
+    _bf16_cuda("x", x, 3)
+    _bf16_cuda("mem", mem, 3)
+    for name, t in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v), ("w_o", w_o)):
+        _bf16_cuda(name, t, 2)
+    for name, t in (("b_q", b_q), ("b_k", b_k), ("b_v", b_v), ("b_o", b_o)):
+        _bf16_cuda(name, t, 1)
+    B, T, d_model = x.shape
+    S = mem.shape[1] if mem is not None else T
+    if H <= 0 or H_kv <= 0 or w_q.shape[1] % H or w_v.shape[1] % H_kv:
+        raise ValueError("the projection widths must be whole multiples of the head counts")
+    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H_kv
+    want = {"w_q": (w_q, (d_model, H * d_k)), "w_k": (w_k, (d_model, H_kv * d_k)),
+            "w_v": (w_v, (d_model, H_kv * d_v)), "w_o": (w_o, (H * d_v, d_model)),
+            "b_q": (b_q, (H * d_k,)), "b_k": (b_k, (H_kv * d_k,)), "b_v": (b_v, (H_kv * d_v,)),
+            "b_o": (b_o, (d_model,)), "mem": (mem, (B, S, d_model))}
+    for name, (t, shape) in want.items():
+        if t is None:
+            continue
+        if tuple(t.shape) != shape:
+            raise ValueError("%s must have shape %s, not %s" % (name, shape, tuple(t.shape)))
+        if t.device != x.device:
+            raise ValueError("%s must be on x's device" % name)
+    if out is None:
+        out = torch.empty((B, T, d_model), dtype=x.dtype, device=x.device)
+    else:
+        _bf16_cuda("out", out, 3)
+        if tuple(out.shape) != (B, T, d_model) or out.device != x.device:
+            raise ValueError("out must have shape %s on x's device" % ((B, T, d_model),))
+    kl_ptr = _lengths_ptr(key_lengths, B, x.device)
+    if scale is None:
+        scale = float(d_k) ** -0.5
+    # an empty memory (S = 0) is never read; pass a non-null stand-in so it is
+    # not taken for self-attention
+    mem_ptr = None if mem is None else (mem.data_ptr() if mem.numel() else x.data_ptr())
+    return out, (B, T, S, d_model, H, H_kv, d_k, d_v), kl_ptr, float(scale), mem_ptr
+
+
 def mha_sublayer_fwd(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=None, *, mem=None,
                      H, H_kv=None, mask_kind: int = 0, key_lengths=None, scale=None,
                      workspace=None, out=None, stream=None):
@@ -280,38 +349,18 @@ def mha_sublayer_fwd(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None, b_o=No
     mha_sublayer_workspace_size(...) bytes (allocated here when None).
     """
     import torch
-    H_kv = H if H_kv is None else H_kv
-    _bf16_cuda("x", x, 3)
-    _bf16_cuda("mem", mem, 3)
-    for name, t in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v), ("w_o", w_o)):
-        _bf16_cuda(name, t, 2)
-    for name, t in (("b_q", b_q), ("b_k", b_k), ("b_v", b_v), ("b_o", b_o)):
-        _bf16_cuda(name, t, 1)
-    B, T, d_model = x.shape
-    S = mem.shape[1] if mem is not None else T
-    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H_kv
-    if out is None:
-        out = torch.empty((B, T, w_o.shape[1]), dtype=x.dtype, device=x.device)
-    need = mha_sublayer_workspace_size(B, T, S, d_model, H, H_kv, d_k, d_v)
+    out, dims, kl_ptr, scale, mem_ptr = _sublayer_marshal(
+        x, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, mem, H, H_kv, key_lengths, scale, out)
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
-    kl_ptr = None
-    if key_lengths is not None:
-        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
-            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
-        kl_ptr = key_lengths.data_ptr()
-    if scale is None:
-        scale = float(d_k) ** -0.5
+        workspace = torch.empty(max(mha_sublayer_workspace_size(*dims), 1), dtype=torch.uint8,
+                                device=x.device)
+    ws_bytes = _workspace_bytes(workspace, x.device)
     ptr = lambda t: t.data_ptr() if t is not None else None
-    # an empty memory (S = 0) is never read; pass a non-null stand-in so it is
-    # not taken for self-attention
-    mem_ptr = None if mem is None else (mem.data_ptr() if mem.numel() else x.data_ptr())
     with torch.cuda.device(x.device):
         st = lib.mha_sublayer_fwd(ptr(x), mem_ptr, ptr(out), ptr(w_q), ptr(w_k), ptr(w_v),
-                                  ptr(w_o), ptr(b_q), ptr(b_k), ptr(b_v), ptr(b_o), B, T, S,
-                                  d_model, H, H_kv, d_k, d_v, int(mask_kind), kl_ptr,
-                                  float(scale), MHA_DTYPE_BF16, workspace.data_ptr(),
-                                  workspace.numel(), _stream_handle(stream))
+                                  ptr(w_o), ptr(b_q), ptr(b_k), ptr(b_v), ptr(b_o), *dims,
+                                  int(mask_kind), kl_ptr, scale, MHA_DTYPE_BF16,
+                                  workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st, "mha_sublayer_fwd")
     return out
@@ -324,33 +373,14 @@ def mha_sublayer_fwd_static(x, w_q, w_k, w_v, w_o, b_q=None, b_k=None, b_v=None,
     nothing allocated per call; calls that overlap in time race on the
     scratch).  Raises MhaError (unsupported) above 64 MiB of intermediates."""
     import torch
-    H_kv = H if H_kv is None else H_kv
-    _bf16_cuda("x", x, 3)
-    _bf16_cuda("mem", mem, 3)
-    for name, t in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v), ("w_o", w_o)):
-        _bf16_cuda(name, t, 2)
-    for name, t in (("b_q", b_q), ("b_k", b_k), ("b_v", b_v), ("b_o", b_o)):
-        _bf16_cuda(name, t, 1)
-    B, T, d_model = x.shape
-    S = mem.shape[1] if mem is not None else T
-    d_k, d_v = w_q.shape[1] // H, w_v.shape[1] // H_kv
-    if out is None:
-        out = torch.empty((B, T, w_o.shape[1]), dtype=x.dtype, device=x.device)
-    kl_ptr = None
-    if key_lengths is not None:
-        if key_lengths.dtype != torch.int32 or not key_lengths.is_cuda or key_lengths.numel() != B:
-            raise ValueError("key_lengths must be an int32 CUDA tensor of shape [B]")
-        kl_ptr = key_lengths.data_ptr()
-    if scale is None:
-        scale = float(d_k) ** -0.5
+    out, dims, kl_ptr, scale, mem_ptr = _sublayer_marshal(
+        x, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, mem, H, H_kv, key_lengths, scale, out)
     ptr = lambda t: t.data_ptr() if t is not None else None
-    mem_ptr = None if mem is None else (mem.data_ptr() if mem.numel() else x.data_ptr())
     with torch.cuda.device(x.device):
         st = lib.mha_sublayer_fwd_static(ptr(x), mem_ptr, ptr(out), ptr(w_q), ptr(w_k),
                                          ptr(w_v), ptr(w_o), ptr(b_q), ptr(b_k), ptr(b_v),
-                                         ptr(b_o), B, T, S, d_model, H, H_kv, d_k, d_v,
-                                         int(mask_kind), kl_ptr, float(scale), MHA_DTYPE_BF16,
-                                         _stream_handle(stream))
+                                         ptr(b_o), *dims, int(mask_kind), kl_ptr, scale,
+                                         MHA_DTYPE_BF16, _stream_handle(stream))
     if st != MHA_OK:
         raise MhaError(st, "mha_sublayer_fwd_static")
     return out
