@@ -356,3 +356,56 @@ def test_linear_binding_checks_devices(mha):
         a.update(kw)
         with pytest.raises(ValueError):
             mha.mha_linear_fwd(a.pop("x"), a.pop("w"), **a)
+
+
+class _RecordingLib:
+    """Takes the place of the loaded library: records each call's arguments."""
+
+    def __init__(self):
+        self.calls = []
+
+    def __getattr__(self, name):
+        def fn(*args):
+            self.calls.append((name, args))
+            return 0
+        return fn
+
+
+def test_bindings_pass_each_entry_point_its_declared_arguments(mha, monkeypatch):
+    torch = pytest.importorskip("torch")
+    import contextlib
+    F = FakeCudaTensor
+    real = mha.mha.lib
+    rec = _RecordingLib()
+    monkeypatch.setattr(mha.mha, "lib", rec)
+    monkeypatch.setattr(torch.cuda, "device", lambda d: contextlib.nullcontext())
+    kl = F((2,), "i32")
+    q, k, v, o = F((2, 4, 8, 64)), F((2, 2, 8, 64)), F((2, 2, 8, 64)), F((2, 4, 8, 64))
+    q4 = F((2, 4, 8, 64))
+    mha.mha.mha_fwd(q, q4, q4, out=o, mask_kind=2, key_lengths=kl, stream=0)
+    mha.mha.mha_fwd_ex(q, k, v, out=o, mask_kind=2, key_lengths=kl, stream=0)
+    mha.mha.mha_bwd(q, k, v, o, F((2, 4, 8, 64)), mask_kind=2, key_lengths=kl, stream=0,
+                    workspace=F((4096,), "u8"), dq=F((2, 4, 8, 64)), dk=F((2, 2, 8, 64)),
+                    dv=F((2, 2, 8, 64)))
+    mha.mha.mha_linear_fwd(F((4, 16, 64)), F((64, 32)), F((32,)), out=F((4, 16, 32)), stream=0)
+    B, T, S, d, H, Hkv, dk = 2, 16, 24, 128, 2, 1, 64
+    sub = dict(mem=F((B, S, d)), H=H, H_kv=Hkv, mask_kind=2, key_lengths=kl, out=F((B, T, d)),
+               stream=0)
+    ws = [F((B, T, d)), F((d, H * dk)), F((d, Hkv * dk)), F((d, Hkv * dk)), F((H * dk, d))]
+    mha.mha.mha_sublayer_fwd(*ws, workspace=F((1 << 20,), "u8"), **sub)
+    mha.mha.mha_sublayer_fwd_static(*ws, **sub)
+    rec.calls = [c for c in rec.calls if not c[0].endswith("_workspace_size")]
+    names = [c[0] for c in rec.calls]
+    assert names == ["mha_fwd", "mha_fwd_ex", "mha_bwd", "mha_linear_fwd", "mha_sublayer_fwd",
+                     "mha_sublayer_fwd_static"]
+    for name, args in rec.calls:
+        assert len(args) == len(getattr(real, name).argtypes), name
+    a = dict(rec.calls)
+    assert a["mha_fwd"][4:11] == (2, 4, 8, 8, 64, 64, 2)  # B, H, Lq, Lk, d_k, d_v, mask
+    assert a["mha_fwd_ex"][4:13] == (2, 4, 2, 8, 8, 64, 64, 0, 2)  # ..., H_kv, ..., layout, mask
+    assert a["mha_bwd"][8:17] == (2, 4, 2, 8, 8, 64, 64, 0, 2)
+    assert a["mha_bwd"][-2] == 4096  # workspace bytes
+    assert a["mha_linear_fwd"][4:8] == (64, 64, 32, 1)  # M, K, N, dtype
+    assert a["mha_sublayer_fwd"][11:19] == (B, T, S, d, H, Hkv, dk, dk)
+    assert a["mha_sublayer_fwd"][-2] == 1 << 20
+    assert a["mha_sublayer_fwd_static"][11:19] == (B, T, S, d, H, Hkv, dk, dk)
