@@ -3,19 +3,26 @@
 
 One step = one ``mha_fwd`` call (the whole path: load, Q K^T, scale + mask,
 softmax, P V, normalise + store) over one batch of the workload.  Default
-workload: Transformer-base encoder self-attention, bf16, B=256, H=8, L=64,
-d=64, key + query padding with lengths uniform in [8, 64] (HBM-bound; metric
-GB/s).  ``--workload`` picks another (see gen.WORKLOADS); the long causal one
-reports TFLOP/s.  The ``sublayer_*`` workloads (gen.SUBLAYERS) time the whole
+(``--workload all``): the headline is the long-context causal configuration
+(bf16, B=4, H=16, L=8192, d=128; TFLOP/s against the bf16 tensor peak), and
+the line's ``configs`` object carries the other four configurations of the
+metric, each timed the same way: the fp32 parity case, the Transformer-base
+padded encoder (B=256, H=8, L=64, lengths uniform in [8, 64]), the causal
+decoder (B=128, H=8, L=128) and the Transformer-big cross-attention (B=64,
+H=16, Lq=96, Lk=128, source lengths uniform in [16, 128]) -- GB/s against
+HBM.  ``--workload NAME`` times one workload of gen.WORKLOADS alone.  The ``sublayer_*`` workloads (gen.SUBLAYERS) time the whole
 multi-head sublayer per step (projections with biases, attention, output
 projection; TFLOP/s), with the projection kernel as the roofline kernel.  The
 ``bwd_*`` workloads time the backward pass (``mha_bwd``: dq, dk, dv of a
 forward workload; TFLOP/s of the five products the chain rule needs).
 
 value  device throughput, inputs resident in HBM; K launches captured in one
-       CUDA graph and replayed between CUDA events; consecutive launches read
-       different input sets whose total exceeds 3x the L2 size, so no launch
-       finds its inputs in L2.
+       CUDA graph whose first and last nodes record the two timing events;
+       consecutive launches read different input sets whose total exceeds 3x
+       the L2 size, so no launch finds its inputs in L2.
+host_us_per_call  host time to enqueue one call, through the C entry point
+       and through the Python binding, and the device time per call when the
+       K calls are launched one by one (no graph).
 e2e    the same metric through the public call with host buffers: pinned
        host -> device copies of Q, K, V (and lengths), mha_fwd, device -> host
        copy of the output, every step, inside the timed region; two device
@@ -48,7 +55,10 @@ import numpy as np  # noqa: E402
 
 import gen  # noqa: E402
 
-DEFAULT_WORKLOAD = "enc_pad_bf16_b256_h8_l64_d64"
+# BASELINE's headline metric: TFLOP/s and fraction of the bf16 tensor peak for
+# long sequences, GB/s and fraction of HBM bandwidth for short ones
+BASELINE_METRIC = ("attention fwd TFLOP/s & % bf16 tensor peak (long n); GB/s & % HBM "
+                   "(short n)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_NAMES = {1: "attn_f32_simt_kernel", 2: "attn_short_tc_kernel", 3: "attn_long_tc_kernel",
                 4: "zero_fill_kernel", 5: "attn_decode_tc_kernel"}
@@ -368,22 +378,99 @@ def oracle_baseline(spec, q, k, v, lens, budget_s=12.0):
 
 
 # ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+_EVENT_RECORD = None
+
+
+def _event_record_fn():
+    """cuEventRecordWithFlags from the CUDA driver (one per process), or None."""
+    global _EVENT_RECORD
+    if _EVENT_RECORD is None:
+        import ctypes
+        try:
+            drv = ctypes.CDLL("libcuda.so.1")
+            fn = drv.cuEventRecordWithFlags
+            fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+            fn.restype = ctypes.c_int
+            _EVENT_RECORD = fn
+        except (OSError, AttributeError):
+            _EVENT_RECORD = False
+    return _EVENT_RECORD or None
+
+
+def graph_timer(stream, fn, steps):
+    """Captures fn(i, stream) for i < steps in one CUDA graph whose first and
+    last nodes record two timing events (external event-record nodes), so the
+    elapsed time covers the launches and not the graph launch before them.
+    Returns (run, elapsed_seconds, how); run() replays the graph on `stream`."""
+    import ctypes
+
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)  # materialise the events
+    ev1.record(stream)
+    stream.synchronize()
+    rec = _event_record_fn()
+    inside = False
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        if rec is not None:
+            inside = rec(ctypes.c_void_p(ev0.cuda_event), ctypes.c_void_p(stream.cuda_stream),
+                         1) == 0
+        for i in range(steps):
+            fn(i, stream)
+        if inside:
+            inside = rec(ctypes.c_void_p(ev1.cuda_event), ctypes.c_void_p(stream.cuda_stream),
+                         1) == 0
+
+    def run():
+        with torch.cuda.stream(stream):
+            if not inside:
+                ev0.record(stream)
+            graph.replay()
+            if not inside:
+                ev1.record(stream)
+
+    how = ("CUDA graph of %d launches, CUDA events recorded as the graph's first and last "
+           "nodes" % steps) if inside else "CUDA graph of %d launches, CUDA events" % steps
+    return run, (lambda: ev0.elapsed_time(ev1) / 1e3), how
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def run_ours(args):
+# the configurations of the headline metric: the long causal one (TFLOP/s,
+# bf16 tensor peak) heads the line; the sentence-length ones (GB/s, HBM) and
+# the fp32 parity configuration follow under "configs"
+HEADLINE_WORKLOAD = "long_causal_bf16_b4_h16_l8192_d128"
+CONFIG_WORKLOADS = ("enc_f32_b2_h8_l32_d64", "enc_pad_bf16_b256_h8_l64_d64",
+                    "dec_causal_bf16_b128_h8_l128_d64", "cross_pad_bf16_b64_h16_lq96_lk128_d64")
+DEFAULT_WORKLOAD = "all"
+
+
+def gpu_context():
     import torch
-
-    import transformer_head_scaled_mha_gb300 as mha
-
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    # every rank runs the same workload on its own GPU (weak scaling)
+    return world, rank, local, dev
 
-    spec = gen.WORKLOADS[args.workload]
+
+def measure_forward(name, args, world, rank, local, dev, cpu_budget):
+    """Everything the JSON line reports for one forward workload: device
+    throughput, end-to-end throughput, roofline, host and eager per-call
+    times, clocks, the oracle's CPU baseline (rank 0, one process only)."""
+    import ctypes
+
+    import torch
+
+    import transformer_head_scaled_mha_gb300 as mha
+
+    spec = gen.WORKLOADS[name]
     dt = spec["dtype"]
     q, k, v, lens = gen.make_inputs(spec, seed=args.seed)
     nbytes, flops = algorithmic(spec, lens)
@@ -391,8 +478,9 @@ def run_ours(args):
     scale = gen.default_scale(spec["dk"])
     mask = spec["mask"]
     B, H, Lq, Lk, dk, dv = (spec[x] for x in ("B", "H", "Lq", "Lk", "dk", "dv"))
-    path = mha.mha_fwd_path_ex(B, H, spec.get("Hkv", H), Lq, Lk, dk, dv, mask,
-                               1 if dt == "bf16" else 0)
+    Hkv = spec.get("Hkv", H)
+    layout = spec.get("layout", "bhsd")
+    path = mha.mha_fwd_path_ex(B, H, Hkv, Lq, Lk, dk, dv, mask, 1 if dt == "bf16" else 0)
     kernel = KERNEL_NAMES.get(path, "?")
 
     def host_tensor(a):
@@ -400,7 +488,7 @@ def run_ours(args):
         return t.view(torch.bfloat16) if dt == "bf16" else t
 
     hq, hk, hv = host_tensor(q), host_tensor(k), host_tensor(v)
-    out_shape = (B, Lq, H, dv) if spec.get("layout", "bhsd") == "bshd" else (B, H, Lq, dv)
+    out_shape = (B, Lq, H, dv) if layout == "bshd" else (B, H, Lq, dv)
     set_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     set_bytes += B * H * Lq * dv * hq.element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -411,15 +499,14 @@ def run_ours(args):
                      torch.empty(out_shape, dtype=hq.dtype, device=dev)))
     kl = torch.from_numpy(lens).to(dev) if lens is not None else None
     stream = torch.cuda.Stream(device=dev)
-
-    plain = spec.get("Hkv", H) == H and spec.get("layout", "bhsd") == "bhsd"
+    plain = Hkv == H and layout == "bhsd"
 
     def call(qq, kk, vv, oo, lens_dev, s):
         if plain:
             mha.mha_fwd(qq, kk, vv, oo, mask_kind=mask, key_lengths=lens_dev, scale=scale,
                         stream=s)
         else:
-            mha.mha_fwd_ex(qq, kk, vv, oo, layout=spec["layout"], mask_kind=mask,
+            mha.mha_fwd_ex(qq, kk, vv, oo, layout=layout, mask_kind=mask,
                            key_lengths=lens_dev, scale=scale, stream=s)
 
     def step(i, s=None):
@@ -432,22 +519,19 @@ def run_ours(args):
             step(i, stream)
     stream.synchronize()
 
-    # capture the K timed launches (one graph, one launch per step)
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
-                step(i, stream)
+    if args.no_graph:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def run_steps():
-        # graph.replay() launches on the current stream: make it `stream`
-        with torch.cuda.stream(stream):
-            if graph is not None:
-                graph.replay()
-            else:
+        def run_steps():
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
                 for i in range(args.steps):
                     step(i, stream)
+                ev1.record(stream)
+        elapsed_of = lambda: ev0.elapsed_time(ev1) / 1e3
+        timing = "eager launches, CUDA events"
+    else:
+        run_steps, elapsed_of, timing = graph_timer(stream, step, args.steps)
 
     # Clocks are sampled from the start of an untimed soak (the same launches,
     # so the GPU is at its loaded clocks) to the end of the timed region.
@@ -457,24 +541,54 @@ def run_ours(args):
     while time.time() - t_soak < args.soak:
         run_steps()
         stream.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    ev0.record(stream)
     run_steps()
-    ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier(world)
     sampler.mark(t_soak + min(0.2, args.soak / 2), t_wall1)
     clocks = sampler.stop()
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    elapsed = max_over_ranks(elapsed, world, dev)
+    elapsed = max_over_ranks(elapsed_of(), world, dev)
     per_launch = elapsed / args.steps
     value = weak_scaling_value(spec, nbytes, flops, per_launch, world)
     st = mha.mha_debug_status(stream)
     if st != mha.MHA_OK:
         raise RuntimeError("device status after timing: %s" % mha.mha_status_string(st))
+
+    # host cost of one call: the C entry point with its arguments already
+    # converted (what a C caller pays), and the Python binding (marshalling
+    # included); both only enqueue.  Eager: the same K calls launched one by
+    # one from the binding, timed on the device.
+    qq, kk, vv, oo = sets[0]
+    raw_args = [ctypes.c_void_p(t.data_ptr()) for t in (qq, kk, vv, oo)]
+    lens_ptr = ctypes.c_void_p(kl.data_ptr() if kl is not None else 0)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    n_host = max(args.steps, 50)
+    dtype_code = mha.MHA_DTYPE_BF16 if dt == "bf16" else mha.MHA_DTYPE_F32
+    lay = 1 if layout == "bshd" else 0
+    stream.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_host):
+        rc = mha.lib.mha_fwd_ex(*raw_args, B, H, Hkv, Lq, Lk, dk, dv, lay, mask, lens_ptr,
+                                ctypes.c_float(scale), dtype_code, sh)
+    host_c = (time.perf_counter() - t0) / n_host
+    if rc != mha.MHA_OK:
+        raise RuntimeError("mha_fwd_ex: %s" % mha.mha_status_string(rc))
+    stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_host):
+        step(i, stream)
+    host_py = (time.perf_counter() - t0) / n_host
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i, stream)
+        e1.record(stream)
+    stream.synchronize()
+    eager = e0.elapsed_time(e1) / 1e3 / args.steps
 
     # e2e: pinned host buffers, copies inside the timed region
     pq, pk, pv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
@@ -492,9 +606,9 @@ def run_ours(args):
                 for d in e2e_dev]
     slots_out = [[(pout, d[3])] for d in e2e_dev]
 
-    def e2e_launch(s, st):
+    def e2e_launch(s, st_):
         d = e2e_dev[s]
-        call(d[0], d[1], d[2], d[3], d[4], st)
+        call(d[0], d[1], d[2], d[3], d[4], st_)
 
     e2e_t = max_over_ranks(e2e_seconds_per_step(slots_in, e2e_launch, slots_out, e2e_steps,
                                                 stream, world), world, dev)
@@ -507,38 +621,70 @@ def run_ours(args):
         peak, achieved, runit = peaks["hbm_gbs"], nbytes / per_launch / 1e9, "GB/s"
     roofline = {"bound": bound_of(spec), "achieved": round(achieved, 2), "peak": peak,
                 "unit": runit, "frac": round(achieved / peak, 4), "traffic":
-                recorded_traffic(args.workload), "kernel": kernel,
+                recorded_traffic(name), "kernel": kernel,
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback", "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_baseline(spec, q, k, v, lens, budget_s=args.cpu_budget)
+        cpu = oracle_baseline(spec, q, k, v, lens, budget_s=cpu_budget)
+    del sets, e2e_dev
+    torch.cuda.empty_cache()
+    return {
+        "metric": metric, "value": round(value, 3), "unit": unit, "steps": args.steps,
+        "ms_per_step": round(per_launch * 1e3, 6),
+        "dtype": dt, "data": "synthetic (seeded N(0,1)%s inputs, seed %d)" % (
+            "*%g" % spec["amp"] if spec["amp"] != 1.0 else "", args.seed),
+        "config": {"workload": name, "B": B, "H": H, "H_kv": Hkv, "layout": layout, "Lq": Lq,
+                   "Lk": Lk, "d_k": dk, "d_v": dv, "mask_kind": mask,
+                   "len_range": spec["len_range"], "scale": scale,
+                   "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
+                         % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
+                   "timing": timing,
+                   "parallelism": "weak: same workload per rank, no collective" if world > 1
+                   else "1 GPU"},
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "pipeline": E2E_PIPELINE},
+        "gpu_launches": args.steps,
+        "host_us_per_call": {"c_abi": round(host_c * 1e6, 2), "python_binding":
+                             round(host_py * 1e6, 2), "kernel": round(per_launch * 1e6, 2),
+                             "eager_device_per_call": round(eager * 1e6, 2),
+                             "note": "host time to enqueue one call (no synchronisation), "
+                                     "mean of %d; eager: %d calls launched one by one, device "
+                                     "time per call" % (n_host, args.steps)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
 
+
+def run_ours(args):
+    world, rank, local, dev = gpu_context()
+    if args.workload == "all":
+        head = measure_forward(HEADLINE_WORKLOAD, args, world, rank, local, dev, args.cpu_budget)
+        configs = {}
+        for name in CONFIG_WORKLOADS:
+            c = measure_forward(name, args, world, rank, local, dev, args.config_cpu_budget)
+            configs[name] = {k_: c[k_] for k_ in ("value", "unit", "ms_per_step", "dtype",
+                                                  "config", "roofline", "e2e",
+                                                  "host_us_per_call", "cpu_baseline", "clocks",
+                                                  "gpu_launches")}
+            if name == "enc_f32_b2_h8_l32_d64":
+                configs[name]["note"] = ("parity configuration (0.5 MB, 4.2 MFLOP): "
+                                         "launch-bound, not a throughput target")
+        line = dict(head)
+        line["metric"] = BASELINE_METRIC
+        line["configs"] = configs
+        line["gpu_launches"] = head["gpu_launches"]
+    else:
+        line = measure_forward(args.workload, args, world, rank, local, dev, args.cpu_budget)
     if rank == 0:
-        line = {
-            "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_launch * 1e3, 6),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": dt, "data": "synthetic (seeded N(0,1)%s inputs, seed %d)" % (
-                "*%g" % spec["amp"] if spec["amp"] != 1.0 else "", args.seed),
-            "config": {"workload": args.workload, "B": B, "H": H, "H_kv": spec.get("Hkv", H),
-                       "layout": spec.get("layout", "bhsd"), "Lq": Lq, "Lk": Lk,
-                       "d_k": dk, "d_v": dv, "mask_kind": mask,
-                       "len_range": spec["len_range"], "scale": scale,
-                       "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
-                             % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graph of %d launches, CUDA events" % args.steps
-                       if graph is not None else "eager launches, CUDA events",
-                       "parallelism": "weak: same workload per rank, no collective" if world > 1
-                       else "1 GPU"},
-            "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "pipeline": E2E_PIPELINE},
-            "gpu_launches": args.steps,
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "clocks": clocks,
-        }
+        line = {"metric": line["metric"], "value": line["value"], "unit": line["unit"],
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": line["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                **{k_: v_ for k_, v_ in line.items()
+                   if k_ not in ("metric", "value", "unit", "steps", "ms_per_step")}}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -634,23 +780,15 @@ def run_sublayer(args):
             for i in range(args.warmup):
                 fn(i, stream)
         stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(steps):
-                fn(i, stream)
-        with torch.cuda.stream(stream):
-            graph.replay()
+        run, elapsed_of, _ = graph_timer(stream, fn, steps)
+        run()
         stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            graph.replay()
-        e1.record(stream)
+        run()
         torch.cuda.synchronize(dev)
         barrier(world)
-        return e0.elapsed_time(e1) / 1e3 / steps
+        return elapsed_of() / steps
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -726,8 +864,8 @@ def run_sublayer(args):
                        "len_range": spec["len_range"], "cross": spec["cross"],
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
                              % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graph of %d calls (5 launches each), CUDA events"
-                                 % args.steps,
+                       "timing": "CUDA graph of %d calls (5 launches each), CUDA events "
+                                 "recorded as the graph's first and last nodes" % args.steps,
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
@@ -773,7 +911,7 @@ def run_reference_sublayer(args):
                        "S": spec["S"], "d_model": spec["d_model"], "H": spec["H"],
                        "H_kv": spec["H_kv"], "mask_kind": spec["mask"]},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
-                             "cores": min(oracle.max_threads(), len(units)), "kind": "oracle",
+                             "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -943,14 +1081,7 @@ def run_backward(args):
         for i in range(args.warmup):
             step(i, stream)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(args.steps):
-            step(i, stream)
-
-    def replay():
-        with torch.cuda.stream(stream):
-            graph.replay()
+    replay, elapsed_of, timing = graph_timer(stream, step, args.steps)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -958,18 +1089,15 @@ def run_backward(args):
     while time.time() - t_soak < args.soak:
         replay()
         stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    e0.record(stream)
     replay()
-    e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier(world)
     sampler.mark(t_soak + min(0.2, args.soak / 2), t_wall1)
     clocks = sampler.stop()
-    per_step = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev) / args.steps
+    per_step = max_over_ranks(elapsed_of(), world, dev) / args.steps
     value = flops / per_step / 1e12 * world
     st = mha.mha_debug_status(stream)
     if st != mha.MHA_OK:
@@ -1041,7 +1169,7 @@ def run_backward(args):
                        "scale": scale,
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
                              % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graph of %d mha_bwd calls, CUDA events" % args.steps,
+                       "timing": timing.replace("launches", "mha_bwd calls"),
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
@@ -1104,13 +1232,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(gen.WORKLOADS) + sorted(gen.SUBLAYERS) +
+                    choices=["all"] + sorted(gen.WORKLOADS) + sorted(gen.SUBLAYERS) +
                     sorted(BWD_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="eager launches instead of a graph")
     ap.add_argument("--soak", type=float, default=1.0, help="untimed load before timing, s")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="oracle baseline budget, s")
+    ap.add_argument("--config-cpu-budget", type=float, default=4.0,
+                    help="oracle baseline budget of each non-headline configuration, s")
     ap.add_argument("--ref-step-budget", type=float, default=2.0, help="reference arm s/step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -1125,6 +1255,8 @@ def main(argv=None):
         (run_reference_backward if args.impl == "reference" else run_backward)(args)
         return
     sub = args.workload in gen.SUBLAYERS
+    if args.impl == "reference" and args.workload == "all":
+        args.workload = HEADLINE_WORKLOAD  # the reference arm times the headline configuration
     if args.impl == "reference":
         (run_reference_sublayer if sub else run_reference)(args)
     else:

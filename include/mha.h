@@ -308,6 +308,27 @@ const char *mha_status_string(int status);
    MHA_OK, MHA_ERR_TIMEOUT, or MHA_ERR_CUDA if the read itself failed. */
 int mha_debug_status(void *stream);
 
+/*
+ * mha_debug_set_wait -- test hook for the kernels' give-up path (the pages
+ * have no counterpart).
+ *
+ * Every wait inside the tensor-core kernels is bounded: after `limit_ns` of
+ * wall time (default 2 s) the waiting warp gives up, the CTA lets the copies
+ * and products it has in flight finish, frees its tensor memory and records
+ * MHA_ERR_TIMEOUT in the status word that mha_debug_status() reads.  This call
+ * sets that limit for the calls enqueued after it (0 restores the default)
+ * and, for tests, `stall` bits that make a kernel wait on a barrier nothing
+ * signals, so the give-up path runs without any fault:
+ *   1  packed short-sequence kernel: the MMA issuer stalls before its first
+ *      product;
+ *   2  long-sequence kernel: the MMA issuer stalls before its third key
+ *      tile, with products and copies in flight.
+ * The output of a stalled call is undefined.  Process-wide setting; not for
+ * use while other threads enqueue work.  Returns MHA_ERR_INVALID_ARGUMENT for
+ * unknown stall bits.
+ */
+int mha_debug_set_wait(unsigned long long limit_ns, int stall);
+
 /* Library version as 10000*major + 100*minor + patch. */
 int mha_version(void);
 

@@ -29,7 +29,7 @@ def test_header_declares_the_entry_points():
         ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
          "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
          "mha_fwd_path", "mha_fwd_path_ex",
-         "mha_status_string", "mha_debug_status",
+         "mha_status_string", "mha_debug_status", "mha_debug_set_wait",
          "mha_version"])
 
 
@@ -46,6 +46,11 @@ def test_status_strings(mha):
     assert "unsupported" in mha.mha_status_string(2)
     assert mha.mha_status_string(99) == "unknown status"
     assert mha.mha_version() >= 100
+
+
+def test_debug_wait_hook_rejects_unknown_stall_bits(mha):
+    assert mha.mha_debug_set_wait(0, 4) == mha.MHA_ERR_INVALID_ARGUMENT
+    assert mha.mha_debug_set_wait(0, 0) == mha.MHA_OK  # the defaults
 
 
 def test_path_selection(mha):
@@ -118,6 +123,8 @@ def test_rejects_before_launch(mha):
     assert call(mha, out=FAKE + 4096) == E_ARG  # out overlaps q
     assert call(mha, out=FAKE + (2 << 24) + 64) == E_ARG  # out overlaps v
     assert call(mha, mask=2, kl=FAKE + (3 << 24) + 128) == E_ARG  # out overlaps key_lengths
+    assert call(mha, mask=2, kl=FAKE + (5 << 24) + 2) == E_ARG  # int32 lengths not 4-byte aligned
+    assert call(mha, mask=4, kl=FAKE + (5 << 24) + 1) == E_ARG
     assert call(mha, scale=math.inf) == E_ARG
     assert call(mha, scale=math.nan) == E_ARG
     assert call(mha, dtype=3) == E_ARG
@@ -212,6 +219,12 @@ def test_sublayer_rejects_before_launch(mha):
     assert call(work=out) == E_ARG  # workspace overlaps out
     assert call(scale=math.nan) == E_ARG
     assert call(mask=2, kl=ws + 512) == E_ARG  # lengths inside the workspace
+    assert call(mask=2, kl=p[9] + 2) == E_ARG  # lengths not 4-byte aligned
+    # H d_k past INT_MAX: rejected, not wrapped to a small projection width
+    big = (1 << 26) + 1
+    assert call(H=big, Hkv=big, work_n=mha.mha_sublayer_workspace_size(
+        2, 64, 64, 512, big, big, 64, 64)) == E_UNS
+    assert call(H=big, Hkv=1, work_n=1 << 62) == E_UNS
     assert call(B=0) == mha.MHA_OK
 
 
@@ -267,6 +280,7 @@ def test_bwd_rejects_before_launch(mha):
     assert call(ws=p[3] + 1024) == E_ARG  # workspace overlaps out
     assert call(mask=2, kl=p[5] + 64) == E_ARG  # lengths inside dq
     assert call(mask=2, kl=p[8] + 64) == E_ARG  # lengths inside the workspace
+    assert call(mask=2, kl=p[9] + 2) == E_ARG  # lengths not 4-byte aligned
     assert call(B=0) == mha.MHA_OK  # empty: nothing to do
 
 

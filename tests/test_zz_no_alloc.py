@@ -59,3 +59,43 @@ def test_static_scratch_refuses_shapes_beyond_it():
     with pytest.raises(mha.MhaError) as e:
         mha.mha_sublayer_fwd_static(x, w, w, w, w, H=8)
     assert e.value.status == mha.MHA_ERR_UNSUPPORTED
+
+
+def test_static_entry_point_allocates_no_device_memory():
+    """After a first call (which loads the kernels' code and looks the scratch
+    up), further calls through the C entry point leave the device's free
+    memory, and everything the caching allocator holds, exactly as they were."""
+    import ctypes
+
+    import torch
+    import transformer_head_scaled_mha_gb300 as mha
+    B, T, d, H = 8, 64, 512, 8
+    x, _, w, b, lens = _inputs(B, T, T, d, H, H, gen.MASK_KEY_PADDING | gen.MASK_QUERY_PADDING,
+                               False, seed=7)
+    dev = lambda a: to_device(a, "bf16")
+    xd, wd, bd = dev(x), [dev(t) for t in w], [dev(t) for t in b]
+    kl = torch.from_numpy(lens).cuda()
+    out = torch.empty((B, T, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+
+    def call():
+        return mha.lib.mha_sublayer_fwd_static(
+            p(xd), None, p(out), *[p(t) for t in wd], *[p(t) for t in bd], B, T, T, d, H, H,
+            d // H, d // H, gen.MASK_KEY_PADDING | gen.MASK_QUERY_PADDING, p(kl),
+            ctypes.c_float((d // H) ** -0.5), mha.MHA_DTYPE_BF16,
+            ctypes.c_void_p(stream.cuda_stream))
+
+    assert call() == mha.MHA_OK
+    torch.cuda.synchronize()
+    first = from_device(out)
+    before = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
+              torch.cuda.memory_reserved())
+    for _ in range(2):
+        assert call() == mha.MHA_OK
+    torch.cuda.synchronize()
+    after = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
+             torch.cuda.memory_reserved())
+    assert after == before
+    np.testing.assert_array_equal(from_device(out), first)
+    assert mha.mha_debug_status() == mha.MHA_OK

@@ -258,9 +258,7 @@ cudaError_t launch_bwd_simt_t(const BwdArgs &a, const Problem &p, cudaStream_t s
   }
   if (p.Lk > 0 && p.B > 0 && p.Hkv > 0) {
     const size_t sm = sizeof(float) * (2 * 32 * (p.dk + 1) + 2 * 32 * (p.dv + 1) + p.dk + p.dv);
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_simt_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sm));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(bwd_dkdv_simt_kernel<T>), static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     dim3 grid((p.Lk + 31) / 32, p.Hkv, p.B);
     bwd_dkdv_simt_kernel<T><<<grid, 32, sm, stream>>>(
@@ -272,9 +270,7 @@ cudaError_t launch_bwd_simt_t(const BwdArgs &a, const Problem &p, cudaStream_t s
   }
   if (rows > 0) {
     const size_t sm = sizeof(float) * (2 * 32 * (p.dk + 1) + 32 * (p.dv + 1) + p.dk + p.dv);
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_simt_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sm));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(bwd_dq_simt_kernel<T>), static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     dim3 grid((p.Lq + 31) / 32, p.H, p.B);
     bwd_dq_simt_kernel<T><<<grid, 32, sm, stream>>>(

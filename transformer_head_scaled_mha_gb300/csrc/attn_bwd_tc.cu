@@ -57,13 +57,6 @@ struct Geo {
   static constexpr int kTile = (D / 64) * kBlk;      // one [128 x D] tile
 };
 
-__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity))
-    if (global_timer_ns() - t0 > 100000000ull) return false;
-  return true;
-}
-
 __device__ __forceinline__ int clamp_len(const Problem &p, int b) {
   if (!(p.mask & (kMaskKeyPadding | kMaskQueryPadding))) return p.Lk;
   const int l = p.key_lengths[b];
@@ -1297,7 +1290,7 @@ cudaError_t launch_one(K kernel, size_t smem, long long grid, const LongMaps &ma
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      set_smem_once(reinterpret_cast<const void *>(kernel), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(maps, p, a);
   return cudaGetLastError();

@@ -112,13 +112,6 @@ constexpr size_t smem_bytes() {
          2 * C::kPBytes + sizeof(Shared);
 }
 
-__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity))
-    if (global_timer_ns() - t0 > 100000000ull) return false;
-  return true;
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -599,9 +592,7 @@ cudaError_t launch_decode_impl(const DecodeMaps &maps, const Problem &p, void *o
   static_assert(smem_bytes<D>() <= 232448, "shared memory budget");
   static_assert(Cfg<D>::kSlots <= kMaxSlots, "ring size");
   constexpr size_t kSmem = smem_bytes<D>();
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_tc_kernel<D, RP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(attn_decode_tc_kernel<D, RP>), static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
   const long long npairs = static_cast<long long>(p.B) * p.Hkv;
   if (npairs <= 0) return cudaSuccess;

@@ -185,9 +185,7 @@ cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, floa
   const size_t smem =
       sizeof(float) * (kRowsPerCta * p.dk + kKeysPerTile * (p.dk + 1) + kKeysPerTile * p.dv);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(attn_f32_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(attn_f32_simt_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   attn_f32_simt_kernel<<<static_cast<unsigned>(grid), kWarps * 32, smem, stream>>>(q, k, v, out,

@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "common.cuh"
@@ -71,16 +72,10 @@ struct __align__(8) Barriers {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
+  uint64_t drain;  // teardown: every tcgen05 op of the CTA has finished
   uint32_t tmem_base;
   int abort_flag;
 };
-
-__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity))
-    if (global_timer_ns() - t0 > 100000000ull) return false;
-  return true;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -136,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->p_full[w], kWgThreads);
       mbar_init(&bars->pv_done[w], 1);
     }
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -149,9 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   // TMEM columns: S_w / P_w at [128 w, 128 w + 128), O_w at [256 + 128 w, +D)
 
-  int issued = 0;  // producer: K/V loads issued
-  uint64_t *last_commit = nullptr;
-  uint32_t last_parity = 0;
+  int issued = 0;           // producer: K/V loads issued
+  bool mma_issued = false;  // MMA lane: a product was issued
 
   if (warp >= 8) {
    regs_dec<kRegsControl>();
@@ -171,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         blk * 64, q0 + w * kBM, h, b);
       for (int idx = 0; idx < 2 * n_kv; ++idx) {
         const int slot = idx % C::kSlots, round = idx / C::kSlots;
-        if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, abort_flag, p.wait_ns)) break;
         const int j = idx >> 1;
         const CUtensorMap *map = (idx & 1) ? &maps.v : &maps.k;
         mbar_arrive_expect_tx(&bars->kv_full[slot], C::kTileBytes);
@@ -182,25 +177,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ---- MMA issuer (lane 0 issues; the warp waits together) ---------------
+    // ---- MMA issuer: lane 0 alone (tcgen05.mma and commit are single-thread
+    // instructions); the other lanes wait at the end ---------------------------
     // iteration j, per warpgroup w: O_w += P_w(j-1) V_{j-1}, then S_w(j) = Q_w K_j^T
-    const uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0);
-    const uint32_t idesc_o = idesc_bf16_f32(128, D, 1);
-    constexpr uint32_t kVLbo = C::kBlkBytes, kVSbo = 1024;
-    bool ok = n_kv == 0 || mbar_wait(&bars->q_full, 0, abort_flag);
-    for (int j = 0; ok && j <= n_kv; ++j) {
-      const int ks = (2 * j) % C::kSlots, kr = (2 * j) / C::kSlots;
-      const int vi = 2 * j - 1 < 0 ? 0 : 2 * j - 1;
-      const int vs = vi % C::kSlots, vr = vi / C::kSlots;
-      if (j < n_kv && !(ok = mbar_wait(&bars->kv_full[ks], kr & 1, abort_flag))) break;
-      if (j >= 1 && !(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag))) break;
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0);
+      const uint32_t idesc_o = idesc_bf16_f32(128, D, 1);
+      constexpr uint32_t kVLbo = C::kBlkBytes, kVSbo = 1024;
+      bool ok = n_kv == 0 || mbar_wait(&bars->q_full, 0, abort_flag, p.wait_ns);
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        // test hook: a wait on a barrier that nothing signals before the
+        // teardown, with products and copies in flight
+        if ((p.stall & kStallLongMma) && j == 2 &&
+            !(ok = mbar_wait(&bars->drain, 0, abort_flag, p.wait_ns)))
+          break;
+        const int ks = (2 * j) % C::kSlots, kr = (2 * j) / C::kSlots;
+        const int vi = 2 * j - 1 < 0 ? 0 : 2 * j - 1;
+        const int vs = vi % C::kSlots, vr = vi / C::kSlots;
+        if (j < n_kv && !(ok = mbar_wait(&bars->kv_full[ks], kr & 1, abort_flag, p.wait_ns)))
+          break;
+        if (j >= 1 && !(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag, p.wait_ns)))
+          break;
 #pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const bool do_pv = j >= 1 && j - 1 < n_tiles[w];
-        const bool do_s = j < n_tiles[w];
-        if (do_pv && !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        if (lane == 0) {
+        for (int w = 0; w < 2; ++w) {
+          const bool do_pv = j >= 1 && j - 1 < n_tiles[w];
+          const bool do_s = j < n_tiles[w];
+          if (do_pv && !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag, p.wait_ns)))
+            break;
+          tc_fence_after();
           if (do_pv) {
             const uint32_t sv = smem_addr(kv_smem + vs * C::kTileBytes);
 #pragma unroll
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (j - 1 > 0) || kk > 0);
             }
             tc_commit(&bars->pv_done[w]);
+            mma_issued = true;
           }
           if (do_s) {
             const uint32_t sq = smem_addr(q_smem + w * C::kTileBytes);
@@ -224,25 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         smem_desc_sw128(sk + off, 16, 1024), idesc_s, kk > 0);
             }
             tc_commit(&bars->s_full[w]);
+            mma_issued = true;
           }
         }
-        __syncwarp();
+        if (!ok) break;
+        if (j < n_kv) tc_commit(&bars->kv_empty[ks]);
+        if (j >= 1) tc_commit(&bars->kv_empty[vs]);
       }
-      if (!ok) break;
-      if (lane == 0) {
-        if (j < n_kv) {
-          tc_commit(&bars->kv_empty[ks]);
-          last_commit = &bars->kv_empty[ks];
-          last_parity = kr & 1;
-        }
-        if (j >= 1) {
-          tc_commit(&bars->kv_empty[vs]);
-          last_commit = &bars->kv_empty[vs];
-          last_parity = vr & 1;
-        }
-      }
-      __syncwarp();
     }
+    __syncwarp();
    }
   } else {
     regs_inc<kRegsSoftmax>();
@@ -265,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       // S_w(j) is ready, and so is P_w(j-1) V_{j-1} (same commit)
-      if (!(ok = mbar_wait(&bars->s_full[w], j & 1, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(&bars->s_full[w], j & 1, abort_flag, p.wait_ns))) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
@@ -322,14 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O / l -> bf16 -> staging (this warpgroup's Q tile) -> TMA
+    // (the decision to store is taken by the whole warpgroup at once: its
+    // warps meet at a named barrier below, which a warp that gave up would
+    // never reach)
+    if (ok && nt > 0) ok = mbar_wait_warp(&bars->pv_done[w], (nt - 1) & 1, abort_flag, p.wait_ns);
+    ok = named_barrier_and(1 + w, kWgThreads, ok);
     if (ok && wg_rows[w]) {
       const bool zero_row = qpad || l_run == 0.f || nt == 0;
       const float inv = zero_row ? 0.f : 1.f / l_run;
-      if (nt > 0) {
-        ok = mbar_wait(&bars->pv_done[w], (nt - 1) & 1, abort_flag);
-        tc_fence_after();
-      }
-      if (ok) {
+      if (nt > 0) tc_fence_after();
+      {
         uint8_t *stage = q_smem + w * C::kTileBytes;
         const uint32_t so = smem_addr(stage);
 #pragma unroll
@@ -371,8 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx >= 0) (void)wait_teardown(&bars->kv_full[idx % C::kSlots], (idx / C::kSlots) & 1);
     if (n_kv > 0) (void)wait_teardown(&bars->q_full, 0);
   }
-  if (*abort_flag && warp == 9 && lane == 0 && last_commit != nullptr)
-    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && warp == 9 && lane == 0 && mma_issued) {
+    // tcgen05 ops of one thread complete in order: one more commit covers
+    // every product issued before it
+    tc_commit(&bars->drain);
+    (void)wait_teardown(&bars->drain, 0);
+  }
   if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
   tc_fence_before();
   __syncthreads();
@@ -386,15 +387,21 @@ cudaError_t launch_long_impl(const LongMaps &maps, const Problem &p, cudaStream_
   static_assert(Cfg<D>::kSlots <= kMaxSlots, "ring size");
   // setmaxnreg.inc only succeeds if the launch reserved the registers it hands
   // out; refuse to launch a build whose register count would not cover them.
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, attn_long_tc_kernel<D>);
-  if (e != cudaSuccess) return e;
-  if (static_cast<long long>(fa.numRegs) * kThreads <
-      2LL * 128 * kRegsSoftmax + 128LL * kRegsControl)
-    return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(attn_long_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cfg<D>::kSmem));
+  // (checked once per process: the register count is a property of the build)
+  static std::atomic<int> regs_ok{0};  // 0 unknown, 1 enough, 2 too few
+  if (regs_ok.load(std::memory_order_acquire) == 0) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, attn_long_tc_kernel<D>);
+    if (e != cudaSuccess) return e;
+    regs_ok.store(static_cast<long long>(fa.numRegs) * kThreads >=
+                          2LL * 128 * kRegsSoftmax + 128LL * kRegsControl
+                      ? 1
+                      : 2,
+                  std::memory_order_release);
+  }
+  if (regs_ok.load(std::memory_order_acquire) != 1) return cudaErrorInvalidConfiguration;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(attn_long_tc_kernel<D>),
+                                static_cast<int>(Cfg<D>::kSmem));
   if (e != cudaSuccess) return e;
   const int nqb = (p.Lq + 2 * kBM - 1) / (2 * kBM);
   const long long grid = static_cast<long long>(p.B) * p.H * nqb;

@@ -67,6 +67,7 @@ struct __align__(8) Barriers {
   uint64_t p_full[kWGs];   // the warpgroup read its S and wrote P
   uint64_t pv_done[kWGs];  // P V done: O ready
   uint64_t o_free[kWGs];   // the warpgroup read O: its columns are free
+  uint64_t drain;          // teardown: every tcgen05 op of the CTA has finished
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -102,13 +103,6 @@ struct UnitWalk {
 // memory wavefront) never share a bank group, writing or reading
 __device__ __forceinline__ uint32_t stage64_offset(uint32_t row, uint32_t c) {
   return row * 64u + ((c ^ ((row >> 1) & 3u)) << 4);
-}
-
-__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity))
-    if (global_timer_ns() - t0 > 100000000ull) return false;
-  return true;
 }
 
 // Rows [0, rows) of one pair (rounded up to a multiple of 8) as one TMA box
@@ -209,9 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // sub-partition q.  Warpgroup w holds query-row block (j + w) % 4 in tile
   // rows 32 j .. 32 j + 31, so each sub-partition gets every kind of block.
   const bool rot = (p.mask & kMaskCausal) && g.Rq == 128 && !g.rows_q;
-  const int n_local = (static_cast<int>(blockIdx.x) < g.units)
-                          ? (g.units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
-                          : 0;
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int n_local = c < g.units ? (g.units - 1 - c) / G + 1 : 0;
 
   // ---- setup -------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -227,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->pv_done[w], 1);
       mbar_init(&bars->o_free[w], kWgThreads);
     }
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -274,8 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
 
   int issued = 0;                   // producers: units whose loads were issued
-  uint64_t *last_commit = nullptr;  // MMA issuer: barrier of the last commit
-  uint32_t last_commit_parity = 0;
+  bool mma_issued = false;          // MMA issuer: a product was issued
   if (warp >= 4 * kWGs) {
    if (warp == kWarpProdQK || warp == kWarpProdV) {
     // ---- TMA producers (lane pp handles pair pp of the unit) ---------------
@@ -317,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!rows_k) bytes += g.P * g.Rk * 128;
       uint64_t *full = is_qk ? &bars->qk_full[s] : &bars->v_full[s];
       uint64_t *empty = is_qk ? &bars->qk_empty[s] : &bars->v_empty[s];
-      if (!mbar_wait(empty, ((n / kStages) & 1) ^ 1, abort_flag)) break;
+      if (!mbar_wait_warp(empty, ((n / kStages) & 1) ^ 1, abort_flag, p.wait_ns)) break;
       uint8_t *dq = qk_base + s * 2 * kTileBytes;  // Q tile (Q|K stage)
       uint8_t *dk = is_qk ? dq + kTileBytes : v_base + s * kTileBytes;  // K or V tile
       const CUtensorMap *kv_full = is_qk ? &maps.k_full : &maps.v_full;
@@ -357,39 +350,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S for unit ns needs its Q|K stage and its warpgroup's columns (free
     // once O of unit ns - 4 was read); P V for unit np needs P and the V
     // stage.  Issue whichever is ready; each stream stays in unit order.
-    int ns = 0, np = 0;
-    const uint64_t t0 = global_timer_ns();
-    uint32_t idle = 0;
-    while (np < n_local) {
-      bool did = false;
-      if (ns < n_local) {
-        const int s = ns % kStages, w = ns % kWGs;
-        if (mbar_probe(&bars->qk_full[s], (ns / kStages) & 1) &&
-            (ns < kWGs || mbar_probe(&bars->o_free[w], ((ns - kWGs) / kWGs) & 1))) {
-          tc_fence_after();
-          if (lane == 0) {
+    // Lane 0 alone polls the barriers and issues (tcgen05.mma and commit are
+    // single-thread instructions); the other lanes wait at the end.  A wait
+    // gives up after wait_ns without progress.
+    if (lane == 0) {
+      int ns = 0, np = 0;
+      uint64_t t_idle = 0;  // start of the current stretch without progress
+      uint32_t idle = 0;
+      // test hook: a wait on a barrier that nothing signals before the teardown
+      const bool run = !(p.stall & kStallShortMma) ||
+                       mbar_wait(&bars->drain, 0, abort_flag, p.wait_ns);
+      while (run && np < n_local) {
+        bool did = false;
+        if (ns < n_local) {
+          const int s = ns % kStages, w = ns % kWGs;
+          if (mbar_probe(&bars->qk_full[s], (ns / kStages) & 1) &&
+              (ns < kWGs || mbar_probe(&bars->o_free[w], ((ns - kWGs) / kWGs) & 1))) {
+            tc_fence_after();
             const uint32_t sq = smem_addr(qk_base + s * 2 * kTileBytes);
             const uint32_t sk = sq + kTileBytes;
-#pragma unroll
+  #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               tc_mma_ss(tmem + w * 128, smem_desc_sw128(sq + kk * 32, 16, 1024),
                         smem_desc_sw128(sk + kk * 32, 16, 1024), idesc_s, kk > 0);
             tc_commit(&bars->s_full[w]);
             tc_commit(&bars->qk_empty[s]);
+            mma_issued = true;
+            ++ns;
+            did = true;
           }
-          __syncwarp();
-          last_commit = &bars->qk_empty[s];
-          last_commit_parity = (ns / kStages) & 1;
-          ++ns;
-          did = true;
         }
-      }
-      if (np < ns) {
-        const int s = np % kStages, w = np % kWGs;
-        if (mbar_probe(&bars->p_full[w], (np / kWGs) & 1) &&
-            mbar_probe(&bars->v_full[s], (np / kStages) & 1)) {
-          tc_fence_after();
-          if (lane == 0) {
+        if (np < ns) {
+          const int s = np % kStages, w = np % kWGs;
+          if (mbar_probe(&bars->p_full[w], (np / kWGs) & 1) &&
+              mbar_probe(&bars->v_full[s], (np / kStages) & 1)) {
+            tc_fence_after();
             const uint32_t sv = smem_addr(v_base + s * kTileBytes);
             for (uint32_t kk = 0; kk < n_keys / 16; ++kk)
               // A = P (TMEM, 16 keys = 8 columns per step); B = V (MN-major)
@@ -397,22 +392,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         smem_desc_sw128(sv + kk * 16 * 128, 1024, 1024), idesc_o, kk > 0);
             tc_commit(&bars->pv_done[w]);
             tc_commit(&bars->v_empty[s]);
+            mma_issued = true;
+            ++np;
+            did = true;
           }
-          __syncwarp();
-          last_commit = &bars->v_empty[s];
-          last_commit_parity = (np / kStages) & 1;
-          ++np;
-          did = true;
         }
-      }
-      if (!did && (++idle & 63u) == 0) {
-        if (*abort_flag) break;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          *abort_flag = 1;
-          break;
+        if (did) {
+          t_idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (*abort_flag) break;
+          if (now - t_idle > p.wait_ns) {
+            *abort_flag = 1;
+            break;
+          }
         }
       }
     }
+    __syncwarp();
    }
   } else {
     // ---- softmax + epilogue: warpgroup w takes units n = w, w + 4, ... -----
@@ -465,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ch_lo = hi > 0 ? static_cast<int>(lo / 32) : 4;
       const int ch_hi = hi > 0 ? static_cast<int>((hi + 31) / 32) : 0;
 
-      if (!mbar_wait(&bars->s_full[w], k & 1, abort_flag)) break;
+      if (!mbar_wait_warp(&bars->s_full[w], k & 1, abort_flag, p.wait_ns)) break;
       tc_fence_after();
       // keep only this row's keys [col_lo, col_lo + jmax).  One pass over
       // the chunks: exponents are taken against the first chunk's max m;
@@ -509,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->p_full[w]);
 
       // ---- epilogue: O / rowsum -> bf16 -> global, 32 columns at a time ----
-      if (!mbar_wait(&bars->pv_done[w], k & 1, abort_flag)) break;
+      if (!mbar_wait_warp(&bars->pv_done[w], k & 1, abort_flag, p.wait_ns)) break;
       tc_fence_after();
       const float inv = zero_row ? 0.f : 1.f / rowsum;
       const int b = cur.b, h0 = cur.hu * g.P;
@@ -565,9 +563,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = issued - kStages; n < issued; ++n)
       if (n >= 0) (void)wait_teardown(&fulls[n % kStages], (n / kStages) & 1);
   }
-  if (*abort_flag && warp == kWarpMma && lane == 0 && last_commit != nullptr) {
-    // tcgen05 ops complete in order: the last commit covers all of them
-    (void)wait_teardown(last_commit, last_commit_parity);
+  if (*abort_flag && warp == kWarpMma && lane == 0 && mma_issued) {
+    // tcgen05 ops of one thread complete in order: one more commit covers
+    // every product issued before it
+    tc_commit(&bars->drain);
+    (void)wait_teardown(&bars->drain, 0);
   }
   if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
   tc_fence_before();
@@ -581,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             void *out, int num_sms, cudaStream_t stream) {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(attn_short_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(attn_short_tc_kernel),
+                                static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = g.units < num_sms ? g.units : num_sms;
   if (grid <= 0) return cudaSuccess;

@@ -32,7 +32,18 @@ struct Problem {
   const int32_t *key_lengths;  // device [B] or nullptr
   float scale_log2;            // scale * log2(e)
   int *status;                 // device status word (kStatusTimeout on a given-up wait)
+  uint64_t wait_ns;            // a bounded wait gives up after this long
+  int stall;                   // test hook: kStall* bits make a kernel wait on a barrier
+                               // that nothing signals (0 in normal use)
 };
+
+// Test hooks for the give-up path of the bounded waits (Problem::stall).
+constexpr int kStallShortMma = 1;  // short kernel: the MMA issuer waits before its first product
+constexpr int kStallLongMma = 2;   // long kernel: the MMA issuer waits before its third iteration
+
+// Sets the dynamic shared-memory limit of a kernel once per device context
+// (a driver call per launch costs host time on every call).
+cudaError_t set_smem_once(const void *kernel, int bytes);
 
 // ---- kernel launchers (defined next to each kernel) ----------------------
 cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, float *out,
@@ -55,6 +66,7 @@ struct ShortGeom {
   int units_per_b;     // ceil(H / P): a unit never spans two batch elements
   int units;           // B * units_per_b
   int rows_q, rows_k;  // load Q / K,V only up to each pair's length (padding)
+  const void *q, *k, *v;  // the tensors themselves (L2 prefetch by address)
 };
 cudaError_t launch_short_tc(const ShortMaps &maps, const ShortGeom &g, const Problem &p,
                             void *out, int num_sms, cudaStream_t stream);

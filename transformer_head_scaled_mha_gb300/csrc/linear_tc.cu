@@ -64,13 +64,6 @@ struct Tiling {
                                   sizeof(Barriers);
 };
 
-__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_test(bar, parity))
-    if (global_timer_ns() - t0 > 100000000ull) return false;
-  return true;
-}
-
 template <bool kSlabs>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_tc_kernel(const __grid_constant__ LinearMaps maps, const uint16_t *__restrict__ bias,
@@ -263,8 +256,7 @@ cudaError_t launch_linear_tc(const LinearMaps &maps, const void *bias, void *y, 
                 "barrier slots");
   auto kernel = slabs ? linear_tc_kernel<true> : linear_tc_kernel<false>;
   const size_t smem = slabs ? Tiling<true>::kSmem : Tiling<false>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kernel), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long tiles =
       static_cast<long long>((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);

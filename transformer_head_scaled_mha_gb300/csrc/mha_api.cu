@@ -20,6 +20,10 @@ namespace {
 // kStatusTimeout here.  One per device, in the module's static memory.
 __device__ int g_status = 0;
 
+// Wait limit and test stall handed to every kernel (mha_debug_set_wait).
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
+std::atomic<int> g_stall{0};
+
 enum Path { kPathNone = 0, kPathF32 = 1, kPathShort = 2, kPathLong = 3, kPathZero = 4, kPathDecode = 5 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -49,16 +53,99 @@ int sm_count(int dev) {
   return v;
 }
 
-std::atomic<int *> g_status_ptr[kMaxDevices];
+// ---- per-context caches ----------------------------------------------------
+// Device addresses of the module's symbols, and whether a kernel's attributes
+// were set, belong to a CUDA context: after a device reset (or in another
+// context on the same device) the module is loaded again and its symbols may
+// move.  Entries are therefore keyed by the context's process-unique id; a
+// thread with no current context (id 0) gets no cached answer.
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
 
-int *status_ptr(int dev) {
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  int *v = g_status_ptr[dev].load(std::memory_order_acquire);
-  if (v != nullptr) return v;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&v), g_status) != cudaSuccess) return nullptr;
-  g_status_ptr[dev].store(v, std::memory_order_release);
+unsigned long long current_ctx_id() {
+  std::call_once(g_ctx_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(fn);
+  });
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (g_ctx_get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// (context id, key) -> value, a small table searched under a lock; when full,
+// the oldest entry is replaced
+struct CtxEntry {
+  unsigned long long ctx;
+  const void *key;
+  void *value;
+};
+constexpr int kCtxEntries = 256;
+CtxEntry g_ctx_table[kCtxEntries];
+int g_ctx_next = 0;
+std::mutex g_ctx_mu;
+
+bool ctx_lookup(unsigned long long ctx, const void *key, void **value) {
+  if (ctx == 0) return false;
+  std::lock_guard<std::mutex> lock(g_ctx_mu);
+  for (const CtxEntry &e : g_ctx_table)
+    if (e.ctx == ctx && e.key == key) {
+      *value = e.value;
+      return true;
+    }
+  return false;
+}
+void ctx_store(unsigned long long ctx, const void *key, void *value) {
+  if (ctx == 0) return;
+  std::lock_guard<std::mutex> lock(g_ctx_mu);
+  for (CtxEntry &e : g_ctx_table)
+    if (e.ctx == ctx && e.key == key) {
+      e.value = value;
+      return;
+    }
+  g_ctx_table[g_ctx_next] = CtxEntry{ctx, key, value};
+  g_ctx_next = (g_ctx_next + 1) % kCtxEntries;
+}
+
+// Device address of a module symbol in the current context.
+void *symbol_ptr(const void *symbol) {
+  const unsigned long long ctx = current_ctx_id();
+  void *v = nullptr;
+  if (ctx_lookup(ctx, symbol, &v)) return v;
+  if (cudaGetSymbolAddress(&v, symbol) != cudaSuccess) return nullptr;
+  ctx_store(ctx, symbol, v);
   return v;
 }
+
+int *status_ptr() { return static_cast<int *>(symbol_ptr(reinterpret_cast<const void *>(&g_status))); }
+
+}  // namespace
+
+cudaError_t set_smem_once(const void *kernel, int bytes) {
+  const unsigned long long ctx = current_ctx_id();
+  void *v = nullptr;
+  if (ctx_lookup(ctx, kernel, &v) && reinterpret_cast<intptr_t>(v) == bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) ctx_store(ctx, kernel, reinterpret_cast<void *>(static_cast<intptr_t>(bytes)));
+  return e;
+}
+
+namespace {
 
 int next_pow2(int x) {
   int r = 1;
@@ -180,7 +267,8 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   if (path == kPathNone) return MHA_OK;
   const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
-  if (padded && key_lengths == nullptr) return MHA_ERR_INVALID_ARGUMENT;
+  if (padded && (key_lengths == nullptr || reinterpret_cast<uintptr_t>(key_lengths) % 4 != 0))
+    return MHA_ERR_INVALID_ARGUMENT;
   const size_t esz = dtype == MHA_DTYPE_F32 ? 4 : 2;
   const size_t nq = static_cast<size_t>(B) * H * Lq * d_k * esz;
   const size_t nk = static_cast<size_t>(B) * H_kv * Lk * d_k * esz;
@@ -198,7 +286,7 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
-  Problem p;
+  Problem p{};
   p.B = B;
   p.H = H;
   p.Hkv = H_kv;
@@ -210,8 +298,10 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   p.mask = mask_kind;
   p.key_lengths = padded ? key_lengths : nullptr;
   p.scale_log2 = scale * kLog2e;
-  p.status = status_ptr(dev);
+  p.status = status_ptr();
   if (p.status == nullptr) return MHA_ERR_CUDA;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.stall = g_stall.load(std::memory_order_relaxed);
 
   cudaError_t err = cudaSuccess;
   if (path == kPathZero) {
@@ -223,7 +313,7 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
     const int sms = sm_count(dev);
     if (sms <= 0) return MHA_ERR_CUDA;
     if (path == kPathShort) {
-      ShortGeom g;
+      ShortGeom g{};
       g.Rq = next_pow2(Lq < 8 ? 8 : Lq);
       g.Rk = next_pow2(Lk < 16 ? 16 : Lk);
       g.P = 128 / (g.Rq > g.Rk ? g.Rq : g.Rk);
@@ -233,6 +323,9 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
       g.units = B * g.units_per_b;
       g.rows_q = (mask_kind & kMaskQueryPadding) ? 1 : 0;
       g.rows_k = (mask_kind & kMaskKeyPadding) ? 1 : 0;
+      g.q = q;
+      g.k = k;
+      g.v = v;
       ShortMaps m;
       std::memset(&m, 0, sizeof m);
       const bool shared_kv = H_kv != H;
@@ -307,7 +400,9 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
   if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
-  if (padded && key_lengths == nullptr && B > 0) return MHA_ERR_INVALID_ARGUMENT;
+  if (padded && B > 0 &&
+      (key_lengths == nullptr || reinterpret_cast<uintptr_t>(key_lengths) % 4 != 0))
+    return MHA_ERR_INVALID_ARGUMENT;
   const size_t esz = dtype == MHA_DTYPE_F32 ? 4 : 2;
   const size_t nq = static_cast<size_t>(B) * H * Lq * d_k * esz;
   const size_t nk = static_cast<size_t>(B) * H_kv * Lk * d_k * esz;
@@ -346,7 +441,7 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
-  Problem p;
+  Problem p{};
   p.B = B;
   p.H = H;
   p.Hkv = H_kv;
@@ -358,8 +453,10 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
   p.mask = mask_kind;
   p.key_lengths = padded ? key_lengths : nullptr;
   p.scale_log2 = scale * kLog2e;
-  p.status = status_ptr(dev);
+  p.status = status_ptr();
   if (p.status == nullptr) return MHA_ERR_CUDA;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.stall = g_stall.load(std::memory_order_relaxed);
   cudaError_t err = cudaSuccess;
   if (Lk == 0 || nq == 0) {
     // no keys: nothing reads q, k or v; every gradient is zero
@@ -427,7 +524,7 @@ int run_linear(const void *x, const void *w, const void *b, void *y, int M, int 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
   const int sms = sm_count(dev);
-  int *status = status_ptr(dev);
+  int *status = status_ptr();
   if (sms <= 0 || status == nullptr) return MHA_ERR_CUDA;
   LinearMaps m;
   std::memset(&m, 0, sizeof m);
@@ -494,17 +591,24 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
   const SublayerWs ws = sublayer_ws(B, T, S, H, H_kv, d_k, d_v);
   uint8_t *wsb = static_cast<uint8_t *>(workspace);
   void *q = wsb + ws.q, *k = wsb + ws.k, *v = wsb + ws.v, *heads = wsb + ws.heads;
-  if ((st = check_linear(x, w_q, b_q, out, Mq, d_model, H * d_k, dtype)) != MHA_OK ||
-      (st = check_linear(mem, w_k, b_k, out, Mk, d_model, H_kv * d_k, dtype)) != MHA_OK ||
-      (st = check_linear(mem, w_v, b_v, out, Mk, d_model, H_kv * d_v, dtype)) != MHA_OK ||
-      (st = check_linear(heads, w_o, b_o, out, Mq, H * d_v, d_model, dtype)) != MHA_OK)
+  // projection widths in 64 bits: a product past INT_MAX would otherwise wrap
+  // to a small, valid-looking width
+  const long long nq = static_cast<long long>(H) * d_k, nk = static_cast<long long>(H_kv) * d_k;
+  const long long nv = static_cast<long long>(H_kv) * d_v, no = static_cast<long long>(H) * d_v;
+  if (nq > 0x7fffffffLL || nk > 0x7fffffffLL || nv > 0x7fffffffLL || no > 0x7fffffffLL)
+    return MHA_ERR_UNSUPPORTED;
+  if ((st = check_linear(x, w_q, b_q, out, Mq, d_model, static_cast<int>(nq), dtype)) != MHA_OK ||
+      (st = check_linear(mem, w_k, b_k, out, Mk, d_model, static_cast<int>(nk), dtype)) != MHA_OK ||
+      (st = check_linear(mem, w_v, b_v, out, Mk, d_model, static_cast<int>(nv), dtype)) != MHA_OK ||
+      (st = check_linear(heads, w_o, b_o, out, Mq, static_cast<int>(no), d_model, dtype)) != MHA_OK)
     return st;
   const int path = select_path(B, H, H_kv, T, S, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
   if (!std::isfinite(scale)) return MHA_ERR_INVALID_ARGUMENT;
   if (Mq == 0) return MHA_OK;
   const bool padded = (mask_kind & (kMaskKeyPadding | kMaskQueryPadding)) != 0;
-  if (padded && key_lengths == nullptr) return MHA_ERR_INVALID_ARGUMENT;
+  if (padded && (key_lengths == nullptr || reinterpret_cast<uintptr_t>(key_lengths) % 4 != 0))
+    return MHA_ERR_INVALID_ARGUMENT;
   if (workspace == nullptr || workspace_bytes < ws.total ||
       reinterpret_cast<uintptr_t>(workspace) % kWsAlign != 0)
     return MHA_ERR_INVALID_ARGUMENT;
@@ -517,12 +621,12 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
     return MHA_ERR_INVALID_ARGUMENT;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   // 1. projections (head i of each is columns [i d, (i + 1) d): [B, L, heads, d])
-  if ((st = run_linear(x, w_q, b_q, q, static_cast<int>(Mq), d_model, H * d_k, stream)) != MHA_OK)
+  if ((st = run_linear(x, w_q, b_q, q, static_cast<int>(Mq), d_model, static_cast<int>(nq), stream)) != MHA_OK)
     return st;
   if (Mk > 0) {
-    if ((st = run_linear(mem, w_k, b_k, k, static_cast<int>(Mk), d_model, H_kv * d_k, stream)) !=
+    if ((st = run_linear(mem, w_k, b_k, k, static_cast<int>(Mk), d_model, static_cast<int>(nk), stream)) !=
             MHA_OK ||
-        (st = run_linear(mem, w_v, b_v, v, static_cast<int>(Mk), d_model, H_kv * d_v, stream)) !=
+        (st = run_linear(mem, w_v, b_v, v, static_cast<int>(Mk), d_model, static_cast<int>(nv), stream)) !=
             MHA_OK)
       return st;
   }
@@ -531,7 +635,7 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
                        key_lengths, scale, dtype, stream)) != MHA_OK)
     return st;
   // 3. concatenated heads [B, T, H d_v] times W_o
-  return run_linear(heads, w_o, b_o, out, static_cast<int>(Mq), H * d_v, d_model, stream);
+  return run_linear(heads, w_o, b_o, out, static_cast<int>(Mq), static_cast<int>(no), d_model, stream);
 }
 
 namespace {
@@ -543,17 +647,12 @@ namespace {
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(64) << 20;
 __device__ __align__(256) uint8_t g_sublayer_scratch[kStaticScratchBytes];
 
-std::atomic<void *> g_scratch_ptr[kMaxDevices];
-
-// Device address of this device's scratch, looked up once per device (a
-// symbol lookup, not an allocation).
-void *scratch_ptr(int dev) {
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  void *v = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (v != nullptr) return v;
-  if (cudaGetSymbolAddress(&v, g_sublayer_scratch) != cudaSuccess) return nullptr;
-  g_scratch_ptr[dev].store(v, std::memory_order_release);
-  return v;
+// Device address of the current device's scratch: a symbol lookup
+// (cudaGetSymbolAddress, not an allocation), made by the first call in each
+// CUDA context and cached for that context; the host-side name of the array
+// is only a stand-in and is never handed to a kernel.
+void *scratch_ptr() {
+  return symbol_ptr(reinterpret_cast<const void *>(&g_sublayer_scratch[0]));
 }
 
 }  // namespace
@@ -581,9 +680,7 @@ extern "C" int mha_sublayer_fwd_static(const void *x, const void *mem, void *out
     return mha_sublayer_fwd(x, mem, out, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, B, T, S,
                             d_model, H, H_kv, d_k, d_v, mask_kind, key_lengths, scale, dtype,
                             nullptr, 0, stream);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
-  void *scratch = scratch_ptr(dev);
+  void *scratch = scratch_ptr();
   if (scratch == nullptr) return MHA_ERR_CUDA;
   return mha_sublayer_fwd(x, mem, out, w_q, w_k, w_v, w_o, b_q, b_k, b_v, b_o, B, T, S, d_model,
                           H, H_kv, d_k, d_v, mask_kind, key_lengths, scale, dtype, scratch,
@@ -613,6 +710,13 @@ extern "C" int mha_debug_status(void *stream_) {
     return MHA_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MHA_ERR_CUDA;
   return host == 0 ? MHA_OK : MHA_ERR_TIMEOUT;
+}
+
+extern "C" int mha_debug_set_wait(unsigned long long limit_ns, int stall) {
+  if (stall & ~(kStallShortMma | kStallLongMma)) return MHA_ERR_INVALID_ARGUMENT;
+  g_wait_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+  g_stall.store(stall, std::memory_order_relaxed);
+  return MHA_OK;
 }
 
 extern "C" int mha_version(void) { return 100; }

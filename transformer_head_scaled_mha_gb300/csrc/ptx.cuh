@@ -85,19 +85,38 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // false and sets the CTA's abort flag) after kWaitLimitNs of wall time, or at
 // once when another warp of the CTA has given up.  The kernel reports an
 // abort through the status word at its teardown.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         return false;
       }
     }
   }
+}
+
+// Warp-uniform bounded wait: every lane gets the same answer, so a warp
+// never reaches a later collective instruction (tcgen05.ld/st, shuffles,
+// barriers) with only part of its lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort_flag, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
+}
+
+// Teardown after a given-up wait: waits (at most 100 ms) for a phase that
+// copies or products already in flight will complete, so the CTA's shared
+// memory and TMEM outlive every access to them.
+__device__ __forceinline__ bool wait_teardown(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity))
+    if (global_timer_ns() - t0 > 100000000ull) return false;
+  return true;
 }
 
 // ---------------------------------------------------------------------------

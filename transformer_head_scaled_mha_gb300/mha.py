@@ -23,7 +23,7 @@ MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
             "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
             "mha_fwd_path", "mha_fwd_path_ex",
-            "mha_status_string", "mha_debug_status", "mha_version")
+            "mha_status_string", "mha_debug_status", "mha_debug_set_wait", "mha_version")
 
 
 class MhaError(RuntimeError):
@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.mha_status_string.argtypes = [i32]
     lib.mha_debug_status.restype = i32
     lib.mha_debug_status.argtypes = [vp]
+    lib.mha_debug_set_wait.restype = i32
+    lib.mha_debug_set_wait.argtypes = [ctypes.c_ulonglong, i32]
     lib.mha_version.restype = i32
     lib.mha_version.argtypes = []
     return lib
@@ -104,6 +106,12 @@ def _stream_handle(stream):
 
 def mha_debug_status(stream=None) -> int:
     return int(lib.mha_debug_status(_stream_handle(stream)))
+
+
+def mha_debug_set_wait(limit_ns: int = 0, stall: int = 0) -> int:
+    """Test hook: the kernels' wait limit in ns (0: the default 2 s) and the
+    stall bits that make a kernel wait on a barrier nothing signals."""
+    return int(lib.mha_debug_set_wait(int(limit_ns), int(stall)))
 
 
 def _lengths_ptr(key_lengths, B, device):
