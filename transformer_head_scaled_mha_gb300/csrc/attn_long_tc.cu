@@ -77,6 +77,65 @@ struct __align__(8) Barriers {
   int abort_flag;
 };
 
+// share of the exponentials of an unmasked chunk taken on the FMA pipes
+// (exp2_poly2) instead of the MUFU unit: pairs k of the chunk with
+// k % kPolyEvery == kPolyEvery - 1 (0: none)
+constexpr int kPolyEvery = 0;
+
+// Row maximum of one 32-column chunk (raw fp32 bits); a tree of 3-input
+// maxima, depth 4.
+__device__ __forceinline__ float chunk_max32(const uint32_t (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int k = 0; k < 10; ++k)
+    t[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]),
+                 __uint_as_float(v[3 * k + 2]));
+  t[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+  return fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]),
+               fmax3(fmax3(t[6], t[7], t[8]), t[9], t[10]));
+}
+
+// p_c = exp2(s_c * sl - m) for one 32-column chunk, packed into 16 bf16x2
+// columns; returns the chunk's sum of p (fp32)
+__device__ __forceinline__ float chunk_exp_pack32(const uint32_t (&v)[32], float sl, float m,
+                                                  uint32_t (&pk)[16]) {
+  const uint64_t sc = f2_pack(sl, sl);
+  const uint64_t nm = f2_pack(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float a, b;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc, nm), a, b);
+    if (kPolyEvery > 0 && (e >> 1) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1) {
+      exp2_poly2(a, b);
+    } else {
+      a = ex2_approx(a);
+      b = ex2_approx(b);
+    }
+    acc[(e >> 1) & 3] = f2_add(acc[(e >> 1) & 3], f2_pack(a, b));
+    pk[e >> 1] = pack_bf16x2(a, b);
+  }
+  acc[0] = f2_add(acc[0], acc[1]);
+  acc[2] = f2_add(acc[2], acc[3]);
+  acc[0] = f2_add(acc[0], acc[2]);
+  float lo, hi;
+  f2_unpack(acc[0], lo, hi);
+  return lo + hi;
+}
+
+// Multiplies the 32 bf16 P values of one chunk (16 TMEM columns) by f, after
+// the stores in flight have landed.
+__device__ __noinline__ void rescale_p16(uint32_t taddr, float f) {
+  uint32_t r[16];
+  tmem_wait_st();
+  tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+    r[t] = pack_bf16x2(__uint_as_float(r[t] << 16) * f, __uint_as_float(r[t] & 0xffff0000u) * f);
+  tmem_st16(taddr, r);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_long_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p) {
@@ -178,12 +237,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ---- MMA issuer: lane 0 alone (tcgen05.mma and commit are single-thread
-    // instructions); the other lanes wait at the end ---------------------------
-    // iteration j, per warpgroup w: O_w += P_w(j-1) V_{j-1}, then S_w(j) = Q_w K_j^T
+    // instructions); the other lanes wait at the end --------------------------
+    // iteration j, per warpgroup w: O_w += P_w(j-1) V_{j-1}, then S_w(j) = Q_w K_j^T.
+    // The K/V slots are released by the warpgroup whose S_w(j) comes last
+    // (its commit covers every earlier product), which spares this thread
+    // two commits per iteration.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0);
       const uint32_t idesc_o = idesc_bf16_f32(128, D, 1);
       constexpr uint32_t kVLbo = C::kBlkBytes, kVSbo = 1024;
+      // descriptors: a constant high half, a low half stepped per piece
+      const uint32_t hi_s = smem_desc_hi(1024), hi_v = smem_desc_hi(kVSbo);
+      const uint32_t q_lo[2] = {smem_desc_lo(smem_addr(q_smem), 16),
+                                smem_desc_lo(smem_addr(q_smem + C::kTileBytes), 16)};
+      const uint32_t kv_lo = smem_desc_lo(smem_addr(kv_smem), 16);
+      const uint32_t v_lo = smem_desc_lo(smem_addr(kv_smem), kVLbo);
+      constexpr uint32_t kSlotLo = C::kTileBytes >> 4;  // low-half step between ring slots
+      // ring position of K_j (index 2 j) and V_{j-1} (index 2 j - 1): slot
+      // and round, stepped without divisions
+      int ks = 0, kr = 0, vs = 0, vr = 0;
       bool ok = n_kv == 0 || mbar_wait(&bars->q_full, 0, abort_flag, p.wait_ns);
       for (int j = 0; ok && j <= n_kv; ++j) {
         // test hook: a wait on a barrier that nothing signals before the
@@ -191,50 +263,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((p.stall & kStallLongMma) && j == 2 &&
             !(ok = mbar_wait(&bars->drain, 0, abort_flag, p.wait_ns)))
           break;
-        const int ks = (2 * j) % C::kSlots, kr = (2 * j) / C::kSlots;
-        const int vi = 2 * j - 1 < 0 ? 0 : 2 * j - 1;
-        const int vs = vi % C::kSlots, vr = vi / C::kSlots;
-        if (j < n_kv && !(ok = mbar_wait(&bars->kv_full[ks], kr & 1, abort_flag, p.wait_ns)))
+        if (j < n_kv && !(ok = mbar_wait_spin(&bars->kv_full[ks], kr & 1, abort_flag, p.wait_ns)))
           break;
-        if (j >= 1 && !(ok = mbar_wait(&bars->kv_full[vs], vr & 1, abort_flag, p.wait_ns)))
+        if (j >= 1 && !(ok = mbar_wait_spin(&bars->kv_full[vs], vr & 1, abort_flag, p.wait_ns)))
           break;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
           const bool do_pv = j >= 1 && j - 1 < n_tiles[w];
           const bool do_s = j < n_tiles[w];
-          if (do_pv && !(ok = mbar_wait(&bars->p_full[w], (j - 1) & 1, abort_flag, p.wait_ns)))
+          if (do_pv &&
+              !(ok = mbar_wait_spin(&bars->p_full[w], (j - 1) & 1, abort_flag, p.wait_ns)))
             break;
           tc_fence_after();
           if (do_pv) {
-            const uint32_t sv = smem_addr(kv_smem + vs * C::kTileBytes);
+            const uint32_t lo = v_lo + vs * kSlotLo;
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
+            for (int kk = 0; kk < kBN / 16; ++kk)
               // B = V_{j-1}, MN-major: 16 key rows per step (8-row groups 1024 B
-              // apart); its D/64 blocks of 64 value columns lie kBlkBytes apart
-              const uint64_t db = smem_desc_sw128(sv + kk * 16 * 128, kVLbo, kVSbo);
+              // apart); its D/64 blocks of 64 value columns lie kBlkBytes apart.
               // A = P_w(j-1): 16 keys = 8 TMEM columns per step
-              tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8, db, idesc_o,
+              tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
+                        desc_join(lo + ((kk * 16 * 128) >> 4), hi_v), idesc_o,
                         (j - 1 > 0) || kk > 0);
-            }
             tc_commit(&bars->pv_done[w]);
             mma_issued = true;
           }
           if (do_s) {
-            const uint32_t sq = smem_addr(q_smem + w * C::kTileBytes);
-            const uint32_t sk = smem_addr(kv_smem + ks * C::kTileBytes);
+            const uint32_t lo = kv_lo + ks * kSlotLo;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kBlkBytes + (kk & 3) * 32;
-              tc_mma_ss(tmem + w * 128, smem_desc_sw128(sq + off, 16, 1024),
-                        smem_desc_sw128(sk + off, 16, 1024), idesc_s, kk > 0);
+              const uint32_t off = ((kk >> 2) * C::kBlkBytes + (kk & 3) * 32) >> 4;
+              tc_mma_ss(tmem + w * 128, desc_join(q_lo[w] + off, hi_s),
+                        desc_join(lo + off, hi_s), idesc_s, kk > 0);
             }
             tc_commit(&bars->s_full[w]);
             mma_issued = true;
           }
         }
-        if (!ok) break;
-        if (j < n_kv) tc_commit(&bars->kv_empty[ks]);
-        if (j >= 1) tc_commit(&bars->kv_empty[vs]);
+        // next iteration: K_{j+1} at index 2 j + 2, V_j at 2 j + 1
+        vs = ks + 1;
+        vr = kr;
+        if (vs == C::kSlots) {
+          vs = 0;
+          ++vr;
+        }
+        ks += 2;
+        if (ks >= C::kSlots) {
+          ks -= C::kSlots;
+          ++kr;
+        }
       }
     }
     __syncwarp();
@@ -258,46 +335,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_use = -INFINITY;  // max used for the exponentials (log2 units)
     float l_run = 0.f;
     bool ok = true;
+    // the warpgroup with the most key tiles (WG1, unless its rows lie past
+    // the end) releases the K/V slots: once it holds S_w(j), every product
+    // issued before -- both warpgroups' reads of K_j and V_{j-1} -- is done
+    const bool releaser = w == (wg_rows[1] ? 1 : 0);
     for (int j = 0; j < nt; ++j) {
       // S_w(j) is ready, and so is P_w(j-1) V_{j-1} (same commit)
       if (!(ok = mbar_wait_warp(&bars->s_full[w], j & 1, abort_flag, p.wait_ns))) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, sr[ch]);
-      tmem_wait_ld();
-
+      if (releaser && r == 0) {
+        mbar_arrive(&bars->kv_empty[(2 * j) % C::kSlots]);
+        if (j >= 1) mbar_arrive(&bars->kv_empty[(2 * j - 1) % C::kSlots]);
+      }
       // columns c < lim are allowed; a row may allow none of this tile's
       // columns (rows of one tile see different key counts under the
       // cached-decoding mask), so clamp to [0, kBN]
       const int lim = min(max(jmax - j * kBN, 0), kBN);
       const bool need_mask = __any_sync(0xffffffffu, lim < kBN);
-      // positive scale: max over the raw scores, then one FMA per score;
-      // otherwise scale first (the max of scale * s is not scale * max s)
       const bool pos = p.scale_log2 > 0.f;
-      const float mt = pos ? mask_max128(sr, need_mask, 0, lim) * p.scale_log2
-                           : scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
-      const float m_new = fmaxf(m_use, mt);
       float alpha = 1.f;
-      if (m_new > m_use + kRescaleThreshold) {
-        if (m_use != -INFINITY) alpha = ex2_approx(m_use - m_new);
-        m_use = m_new;
-      }
-      const bool live = m_use != -INFINITY;
-      l_run = l_run * alpha + (pos ? exp2_fma_sum128(sr, p.scale_log2, m_use, live)
-                                   : exp2_sum128(sr, m_use, live));
-
-      // P_w(j) as bf16 pairs over the first 64 columns of S_w
+      if (pos && !need_mask && __all_sync(0xffffffffu, m_use != -INFINITY)) {
+        // Unmasked tile, every row of the warp has a running max: 32-column
+        // chunks, exponents against the running max, the next chunk's TMEM
+        // load in flight while this one is computed.  A chunk whose max
+        // exceeds the running max by more than 2^8 moves it first (and
+        // rescales the P of the chunks already stored).  P of chunk ch goes
+        // to columns [16 ch, 16 ch + 16), whose scores are already read.
+        uint32_t va[32], vb[32];
+        tmem_ld32(s_tmem, va);
+        tmem_wait_ld();
+        float tsum = 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const int c = h * 64 + 2 * t;
-          pk[t] = pack_bf16x2(__uint_as_float(sr[c >> 5][c & 31]),
-                              __uint_as_float(sr[c >> 5][(c + 1) & 31]));
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+          uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+          if (ch < 3) tmem_ld32(s_tmem + (ch + 1) * 32, nxt);
+          const float cm = chunk_max32(cur) * p.scale_log2;
+          const bool climb = cm > m_use + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, climb)) {
+            const float f = climb ? ex2_approx(m_use - cm) : 1.f;
+            if (climb) m_use = cm;
+            alpha *= f;
+            tsum *= f;
+#pragma unroll 1
+            for (int c = 0; c < ch; ++c) rescale_p16(s_tmem + c * 16, f);
+          }
+          uint32_t pk[16];
+          tsum += chunk_exp_pack32(cur, p.scale_log2, m_use, pk);
+          tmem_st16(s_tmem + ch * 16, pk);
+          if (ch < 3) tmem_wait_ld();
         }
-        tmem_st32(s_tmem + h * 32, pk);
+        l_run = l_run * alpha + tsum;
+      } else {
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, sr[ch]);
+        tmem_wait_ld();
+        // positive scale: max over the raw scores, then one FMA per score;
+        // otherwise scale first (the max of scale * s is not scale * max s)
+        const float mt = pos ? mask_max128(sr, need_mask, 0, lim) * p.scale_log2
+                             : scale_mask_max128(sr, p.scale_log2, need_mask, 0, lim);
+        const float m_new = fmaxf(m_use, mt);
+        if (m_new > m_use + kRescaleThreshold) {
+          if (m_use != -INFINITY) alpha = ex2_approx(m_use - m_new);
+          m_use = m_new;
+        }
+        const bool live = m_use != -INFINITY;
+        l_run = l_run * alpha + (pos ? exp2_fma_sum128(sr, p.scale_log2, m_use, live)
+                                     : exp2_sum128(sr, m_use, live));
+        // P_w(j) as bf16 pairs over the first 64 columns of S_w
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const int c = h * 64 + 2 * t;
+            pk[t] = pack_bf16x2(__uint_as_float(sr[c >> 5][c & 31]),
+                                __uint_as_float(sr[c >> 5][(c + 1) & 31]));
+          }
+          tmem_st32(s_tmem + h * 32, pk);
+        }
       }
       // the running max moved: rescale this row of O (rare, warp-wide)
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {

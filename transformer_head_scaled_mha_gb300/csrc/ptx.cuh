@@ -101,6 +101,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait for a thread that must react at once: polls with test_wait,
+// which never suspends the thread (try_wait may sleep for a while first).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort_flag, uint64_t limit_ns) {
+  if (mbar_probe(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_probe(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform bounded wait: every lane gets the same answer, so a warp
 // never reaches a later collective instruction (tcgen05.ld/st, shuffles,
 // barriers) with only part of its lanes.
@@ -430,6 +448,24 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The two 32-bit halves of smem_desc_sw128: the low half holds the start
+// address (>> 4) and the leading-dimension offset, the high half the stride
+// offset, version and layout.  A later 16-byte-aligned piece of the same
+// operand has the same high half and a low half larger by offset / 16 (no
+// carry below 256 KiB of shared memory), so an issuing loop can keep the
+// high half in one register and step the low half with one add.
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D.
 //   [4,6) D format (1 = f32)  [7,10) A format (1 = bf16)  [10,13) B format
 //   [15] A major (0 = K)  [16] B major (0 = K, 1 = MN)
@@ -551,8 +587,41 @@ __device__ __forceinline__ float mask_max128(uint32_t (&r)[4][32], bool mask, in
   return fmax3(fmax3(a, b, c), fmax3(d, e, m[15]), -INFINITY);
 }
 
+// 2^x for a pair of floats on the FMA pipes instead of the MUFU unit.  Range
+// reduction as in Cody and Waite (exact in base 2): x is clamped to >= -126,
+// n = round(x) comes from adding 1.5 * 2^23 (the sum's last bit is the units
+// place), f = x - n lies in [-1/2, 1/2], 2^f is a cubic with the smallest
+// largest relative error on that interval (7.5e-5; coefficients fitted by
+// fit_exp2_poly.py next to the sources), and n is added to the result's
+// exponent field: the shifted sum keeps n's two's complement in its low bits,
+// so (bits(sum) << 23) is n << 23 modulo 2^32.  For x >= -125 the relative
+// error stays below 7.5e-5; below, results are under 2^-125.  x must not be
+// -inf (a clamped -inf gives 2^-126, not 0) nor NaN.
+constexpr float kExp2Shift = 12582912.0f;  // 1.5 * 2^23
+constexpr float kExp2C0 = 9.999280572e-01f;
+constexpr float kExp2C1 = 6.932609677e-01f;
+constexpr float kExp2C2 = 2.426111251e-01f;
+constexpr float kExp2C3 = 5.517166853e-02f;
+__device__ __forceinline__ void exp2_poly2(float &a, float &b) {
+  const uint64_t x = f2_pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
+  const uint64_t shift = f2_pack(kExp2Shift, kExp2Shift);
+  const uint64_t t = f2_add(x, shift);
+  const uint64_t f = f2_sub(x, f2_sub(t, shift));
+  uint64_t q = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  q = f2_fma(q, f, f2_pack(kExp2C1, kExp2C1));
+  q = f2_fma(q, f, f2_pack(kExp2C0, kExp2C0));
+  float tl, th, ql, qh;
+  f2_unpack(t, tl, th);
+  f2_unpack(q, ql, qh);
+  a = __uint_as_float(__float_as_uint(ql) + (__float_as_uint(tl) << 23));
+  b = __uint_as_float(__float_as_uint(qh) + (__float_as_uint(th) << 23));
+}
+
 // p_c = exp2(s_c * scale_log2 - m) in place, one packed FMA per pair (0 when
-// !live); returns sum_c p_c
+// !live); returns sum_c p_c.  kPoly: pairs 1 and 3 of every five take the
+// exponential on the FMA pipes (exp2_poly2), the rest on the MUFU unit, so
+// both units share the work (no score may then be -inf: unmasked tiles only).
+template <bool kPoly = false>
 __device__ __forceinline__ float exp2_fma_sum128(uint32_t (&r)[4][32], float scale_log2, float m,
                                                  bool live) {
   const uint64_t sc = f2_pack(scale_log2, scale_log2);
@@ -567,8 +636,14 @@ __device__ __forceinline__ float exp2_fma_sum128(uint32_t (&r)[4][32], float sca
                              __uint_as_float(r[c >> 5][(c + 1) & 31])),
                      sc, nm),
               a, b);
-    a = live ? ex2_approx(a) : 0.f;
-    b = live ? ex2_approx(b) : 0.f;
+    if (kPoly && ((c >> 1) % 5 == 1 || (c >> 1) % 5 == 3)) {
+      exp2_poly2(a, b);
+      a = live ? a : 0.f;
+      b = live ? b : 0.f;
+    } else {
+      a = live ? ex2_approx(a) : 0.f;
+      b = live ? ex2_approx(b) : 0.f;
+    }
     r[c >> 5][c & 31] = __float_as_uint(a);
     r[c >> 5][(c + 1) & 31] = __float_as_uint(b);
     acc[(c >> 1) & 7] = f2_add(acc[(c >> 1) & 7], f2_pack(a, b));
