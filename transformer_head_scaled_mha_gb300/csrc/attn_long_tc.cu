@@ -25,8 +25,8 @@
 // The running max is moved (and O rescaled in TMEM) only when it grows by more
 // than 2^8; numerator and denominator share the stale max, so the quotient is
 // unchanged.  Under a causal mask the tiles above the diagonal are never
-// loaded nor multiplied, which halves the work; CTAs are issued heaviest
-// query block first.
+// loaded nor multiplied, which halves the work; CTAs are issued in bands of
+// query blocks, heaviest band first, a head's blocks of a band together.
 //
 // Warp roles (384 threads): warps 0-3 softmax WG0, 4-7 softmax WG1, warp 8 TMA
 // producer, warp 9 TMEM owner + MMA issuer, warps 10-11 idle (they complete the
@@ -56,6 +56,7 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "re
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O may grow to 2^8 before a rescale
 constexpr int kMaxSlots = 8;
+constexpr int kBand = 8;  // query blocks per band of the CTA order
 
 template <int D>
 struct Cfg {
@@ -151,8 +152,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqb = (p.Lq + 2 * kBM - 1) / (2 * kBM);
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / BH;  // heaviest first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // CTA order: bands of kBand query blocks, heaviest band first; inside a
+  // band, all its query blocks of one head side by side (heaviest first), so
+  // the CTAs running at one time that read a head's keys and values read the
+  // same tiles at about the same time and mostly find them in L2
+  int qb, bh;
+  {
+    const int x = static_cast<int>(blockIdx.x);
+    const int full = nqb / kBand;  // full bands; a partial one (the lightest) ends the order
+    const int t = min(x / (BH * kBand), full);
+    const int hi = nqb - t * kBand;  // the band's query blocks are [hi - size, hi)
+    const int size = min(kBand, hi);
+    const int local = x - t * BH * kBand;
+    bh = local / size;
+    qb = hi - 1 - local % size;
+  }
   const int b = bh / p.H, h = bh % p.H;
   const int hkv = h / (p.H / p.Hkv);  // key/value head this query head reads
   const int q0 = qb * 2 * kBM;
@@ -285,7 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
                         desc_join(lo + ((kk * 16 * 128) >> 4), hi_v), idesc_o,
                         (j - 1 > 0) || kk > 0);
-            tc_commit(&bars->pv_done[w]);
+            // only the epilogue waits for P V on its own, after the last
+            // one; every earlier P V is covered by the next S's commit
+            if (j == n_tiles[w]) tc_commit(&bars->pv_done[w]);
             mma_issued = true;
           }
           if (do_s) {
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (the decision to store is taken by the whole warpgroup at once: its
     // warps meet at a named barrier below, which a warp that gave up would
     // never reach)
-    if (ok && nt > 0) ok = mbar_wait_warp(&bars->pv_done[w], (nt - 1) & 1, abort_flag, p.wait_ns);
+    if (ok && nt > 0) ok = mbar_wait_warp(&bars->pv_done[w], 0, abort_flag, p.wait_ns);
     ok = named_barrier_and(1 + w, kWgThreads, ok);
     if (ok && wg_rows[w]) {
       const bool zero_row = qpad || l_run == 0.f || nt == 0;

@@ -488,6 +488,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x for two bfloat16 values at once on the MUFU unit (one instruction for
+// the pair); lo in the low half
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // Pairs of fp32 in one 64-bit register: sm_100-class parts execute add, sub
 // and mul on both halves with one f32x2 instruction.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
