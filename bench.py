@@ -1056,27 +1056,46 @@ def run_backward(args):
 
     hq, hk, hv, hdo = host(q), host(k), host(v), host(dout)
     kl = torch.from_numpy(lens).to(dev) if lens is not None else None
-    # the forward output the backward reads, from the forward kernel itself
-    out0 = mha.mha_fwd_ex(hq.to(dev), hk.to(dev), hv.to(dev), layout=layout, mask_kind=mask,
-                          key_lengths=kl, scale=scale)
-    hout = out0.cpu()
+    # the forward output and row statistics the backward reads, from the
+    # forward kernel itself (as a training step keeps them)
+    out0, lse0 = mha.mha_fwd_lse(hq.to(dev), hk.to(dev), hv.to(dev), layout=layout,
+                                 mask_kind=mask, key_lengths=kl, scale=scale)
+    hout, hlse = out0.cpu(), lse0.cpu()
     ins = (hq, hk, hv, hout, hdo)
-    set_bytes = sum(t.numel() * 2 for t in ins) + (hq.numel() + hk.numel() + hv.numel()) * 2
+    set_bytes = sum(t.numel() * 2 for t in ins) + (hq.numel() + hk.numel() + hv.numel()) * 2 + \
+        hlse.numel() * 4
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = max(1, math.ceil(3 * l2 / set_bytes))
     sets = [tuple(t.to(dev) for t in ins) + (torch.empty_like(hq, device=dev),
                                              torch.empty_like(hk, device=dev),
-                                             torch.empty_like(hv, device=dev))
+                                             torch.empty_like(hv, device=dev), hlse.to(dev))
             for _ in range(n_sets)]
     ws = torch.empty(max(1, mha.mha_bwd_workspace_size(B, H, Lq)), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(i, s):
-        qq, kk, vv, oo, gg, dq, dk_, dv_ = sets[i % n_sets]
-        mha.mha_bwd(qq, kk, vv, oo, gg, layout=layout, mask_kind=mask, key_lengths=kl,
-                    scale=scale, workspace=ws, dq=dq, dk=dk_, dv=dv_, stream=s)
+    def step_with(use_lse):
+        def step(i, s):
+            qq, kk, vv, oo, gg, dq, dk_, dv_, ls = sets[i % n_sets]
+            mha.mha_bwd(qq, kk, vv, oo, gg, layout=layout, mask_kind=mask, key_lengths=kl,
+                        scale=scale, workspace=ws, dq=dq, dk=dk_, dv=dv_, stream=s,
+                        lse=ls if use_lse else None)
+        return step
 
+    # the call without the forward's statistics (a statistics pass first),
+    # timed for comparison only
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step_with(False)(i, stream)
+    stream.synchronize()
+    replay0, elapsed0, _ = graph_timer(stream, step_with(False), args.steps)
+    for _ in range(2):  # the first replay uploads the graph
+        replay0()
+        torch.cuda.synchronize(dev)
+    stats_pass_ms = max_over_ranks(elapsed0(), world, dev) / args.steps * 1e3
+    del replay0
+
+    step = step_with(True)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i, stream)
@@ -1113,29 +1132,31 @@ def run_backward(args):
                 "traffic_kernel": "bwd_short_tc_kernel" if spec["dk"] == 64 and Lq <= 128 and
                                   Lk <= 128 else "bwd_dkdv_tc_kernel (the largest share of the call)",
                 "kernel": "bwd_short_tc_kernel (one launch)" if spec["dk"] == 64 and Lq <= 128
-                          and Lk <= 128 else "bwd_stats_tc_kernel + bwd_dq_tc_kernel + "
-                          "bwd_dkdv_tc_kernel (one mha_bwd call, 3 launches)",
+                          and Lk <= 128 else "bwd_dsum_kernel + bwd_dq_tc_kernel + "
+                          "bwd_dkdv_tc_kernel (one mha_bwd_lse call, 3 launches)",
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback", "algorithmic_flops": flops}
 
     # e2e: q, k, v, out, dout (and lengths) in, dq, dk, dv back, every step
     pins = [t.pin_memory() for t in ins]
+    plse = hlse.pin_memory()
     pl = torch.from_numpy(lens).pin_memory() if lens is not None else None
     pouts = [torch.empty_like(t).pin_memory() for t in (hq, hk, hv)]
-    h2d = sum(t.numel() * 2 for t in pins) + (pl.numel() * 4 if pl is not None else 0)
+    h2d = sum(t.numel() * 2 for t in pins) + plse.numel() * 4 + \
+        (pl.numel() * 4 if pl is not None else 0)
     d2h = sum(t.numel() * 2 for t in pouts)
-    # per slot: q, k, v, out, dout, dq, dk, dv, lengths, workspace (slot 0
-    # reuses the first set)
-    e2e_dev = [list(sets[0][:8]) + [torch.empty_like(kl) if kl is not None else None, ws]]
+    # per slot: q, k, v, out, dout, dq, dk, dv, lse, lengths, workspace (slot
+    # 0 reuses the first set)
+    e2e_dev = [list(sets[0][:9]) + [torch.empty_like(kl) if kl is not None else None, ws]]
     e2e_dev.append([torch.empty_like(t) if t is not None else None for t in e2e_dev[0]])
-    slots_in = [list(zip(e[:5], pins)) + ([(e[8], pl)] if pl is not None else [])
-                for e in e2e_dev]
+    slots_in = [list(zip(e[:5], pins)) + [(e[8], plse)] +
+                ([(e[9], pl)] if pl is not None else []) for e in e2e_dev]
     slots_out = [list(zip(pouts, e[5:8])) for e in e2e_dev]
 
     def e2e_launch(s, st):
         e = e2e_dev[s]
-        mha.mha_bwd(*e[:5], layout=layout, mask_kind=mask, key_lengths=e[8], scale=scale,
-                    workspace=e[9], dq=e[5], dk=e[6], dv=e[7], stream=st)
+        mha.mha_bwd(*e[:5], layout=layout, mask_kind=mask, key_lengths=e[9], scale=scale,
+                    workspace=e[10], dq=e[5], dk=e[6], dv=e[7], stream=st, lse=e[8])
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e2e_t = max_over_ranks(e2e_seconds_per_step(slots_in, e2e_launch, slots_out, e2e_steps,
@@ -1169,7 +1190,10 @@ def run_backward(args):
                        "scale": scale,
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
                              % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": timing.replace("launches", "mha_bwd calls"),
+                       "timing": timing.replace("launches", "mha_bwd_lse calls"),
+                       "statistics": "the forward's (mha_fwd_lse) row statistics, as a "
+                                     "training step keeps them",
+                       "ms_per_step_with_statistics_pass": round(stats_pass_ms, 6),
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",

@@ -154,6 +154,32 @@ int mha_fwd_ex(const void *q, const void *k, const void *v, void *out,
                float scale, int dtype, void *stream);
 
 /*
+ * mha_fwd_lse -- mha_fwd_ex that also stores each query row's softmax
+ * statistics for the backward pass:
+ *
+ *     lse[b,h,i] = log2( sum_j 2^(scale * log2(e) * q[b,h,i,:] . k[b,g,j,:]) ),
+ *
+ * over the allowed keys j (the logarithm, in base 2, of the denominator of
+ * step 3 of trishampatil.com, "Scaled Dot-Product Attention: Step by Step";
+ * multiply by ln 2 for the natural logarithm).  Rows stored as +0.0 (query
+ * padding, no allowed key) get +inf.  Training keeps these statistics from
+ * the forward pass so that the backward pass need not recompute the scores a
+ * second time (mha_bwd_lse).
+ *
+ * lse                   device pointer to float[B, H, Lq] (that order, whatever
+ *                       the layout), 4-byte aligned, caller-owned; written in
+ *                       full; must not overlap any other argument.  NULL is
+ *                       MHA_ERR_INVALID_ARGUMENT unless B*H*Lq == 0.
+ *
+ * Every other argument, the ownership rules and the errors are those of
+ * mha_fwd_ex; `out` is the same as mha_fwd_ex's.
+ */
+int mha_fwd_lse(const void *q, const void *k, const void *v, void *out, float *lse,
+                int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
+                int mask_kind, const int32_t *key_lengths,
+                float scale, int dtype, void *stream);
+
+/*
  * mha_linear_fwd -- y = x W + b, asynchronous on `stream`.
  *
  * The learned projection of token vectors that surrounds the attention
@@ -283,6 +309,23 @@ int mha_bwd(const void *q, const void *k, const void *v, const void *out, const 
             void *dq, void *dk, void *dv, int B, int H, int H_kv, int Lq, int Lk, int d_k,
             int d_v, int layout, int mask_kind, const int32_t *key_lengths, float scale,
             int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mha_bwd_lse -- mha_bwd given the forward pass's row statistics `lse` (from
+ * mha_fwd_lse with the same arguments): the weights are formed from them, so
+ * no statistics pass recomputes the scores (6 products per allowed (query,
+ * key) pair instead of 8 on the tensor cores); only D = dout . out is formed
+ * first.  lse: device float[B, H, Lq], 4-byte aligned, read only, must not
+ * overlap dq, dk, dv or the workspace; NULL is MHA_ERR_INVALID_ARGUMENT
+ * unless B*H*Lq == 0.  The fp32 path and the single-tile bf16 path (d = 64,
+ * Lq, Lk <= 128: one fused kernel that forms the statistics itself) read it
+ * not.  Every other argument, the workspace and the errors are those of
+ * mha_bwd.
+ */
+int mha_bwd_lse(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                const float *lse, void *dq, void *dk, void *dv, int B, int H, int H_kv, int Lq,
+                int Lk, int d_k, int d_v, int layout, int mask_kind, const int32_t *key_lengths,
+                float scale, int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Which kernel mha_fwd would launch for these arguments:
    0 = none (empty problem), 1 = fp32 CUDA-core kernel, 2 = packed

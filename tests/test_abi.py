@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted(
-        ["mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
+        ["mha_fwd", "mha_fwd_ex", "mha_fwd_lse", "mha_bwd_lse", "mha_linear_fwd",
+         "mha_sublayer_workspace_size",
          "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
          "mha_fwd_path", "mha_fwd_path_ex",
          "mha_status_string", "mha_debug_status", "mha_debug_set_wait",
@@ -170,6 +171,31 @@ def test_binding_refuses_cpu_tensors(mha):
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mha.mha_fwd(q, q, q)
+
+
+def test_lse_entry_points_reject_before_launch(mha):
+    E_ARG = mha.MHA_ERR_INVALID_ARGUMENT
+    q, k, v, out = FAKE, FAKE + (1 << 24), FAKE + (2 << 24), FAKE + (3 << 24)
+    lse = FAKE + (4 << 24)
+
+    def fwd(lse_=lse, B=2, mask=0, kl=None):
+        return mha.lib.mha_fwd_lse(q, k, v, out, lse_, B, 4, 2, 64, 64, 64, 64, 0, mask, kl,
+                                   0.125, 1, None)
+    assert fwd(lse_=None) == E_ARG  # the statistics are this call's purpose
+    assert fwd(lse_=lse + 2) == E_ARG  # not 4-byte aligned
+    assert fwd(lse_=out + 64) == E_ARG  # overlaps out
+    assert fwd(lse_=q + 128) == E_ARG  # overlaps q
+    assert fwd(lse_=None, B=0) == mha.MHA_OK  # empty
+    ws_n = mha.mha_bwd_workspace_size(2, 4, 64)
+    p = [FAKE + (i << 24) for i in range(11)]
+
+    def bwd(lse_=p[10], ws=p[8]):
+        return mha.lib.mha_bwd_lse(p[0], p[1], p[2], p[3], p[4], lse_, p[5], p[6], p[7], 2, 4, 2,
+                                   64, 64, 64, 64, 0, 0, None, 0.125, 1, ws, ws_n, None)
+    assert bwd(lse_=None) == E_ARG
+    assert bwd(lse_=p[10] + 1) == E_ARG  # not 4-byte aligned
+    assert bwd(lse_=p[5] + 64) == E_ARG  # inside dq
+    assert bwd(lse_=p[8] + 64) == E_ARG  # inside the workspace
 
 
 def test_linear_rejects_before_launch(mha):
@@ -401,6 +427,11 @@ def test_bindings_pass_each_entry_point_its_declared_arguments(mha, monkeypatch)
     mha.mha.mha_bwd(q, k, v, o, F((2, 4, 8, 64)), mask_kind=2, key_lengths=kl, stream=0,
                     workspace=F((4096,), "u8"), dq=F((2, 4, 8, 64)), dk=F((2, 2, 8, 64)),
                     dv=F((2, 2, 8, 64)))
+    mha.mha.mha_fwd_lse(q, k, v, out=o, lse=F((2, 4, 8), "f32"), mask_kind=2, key_lengths=kl,
+                        stream=0)
+    mha.mha.mha_bwd(q, k, v, o, F((2, 4, 8, 64)), mask_kind=2, key_lengths=kl, stream=0,
+                    workspace=F((4096,), "u8"), dq=F((2, 4, 8, 64)), dk=F((2, 2, 8, 64)),
+                    dv=F((2, 2, 8, 64)), lse=F((2, 4, 8), "f32"))
     mha.mha.mha_linear_fwd(F((4, 16, 64)), F((64, 32)), F((32,)), out=F((4, 16, 32)), stream=0)
     B, T, S, d, H, Hkv, dk = 2, 16, 24, 128, 2, 1, 64
     sub = dict(mem=F((B, S, d)), H=H, H_kv=Hkv, mask_kind=2, key_lengths=kl, out=F((B, T, d)),
@@ -410,8 +441,8 @@ def test_bindings_pass_each_entry_point_its_declared_arguments(mha, monkeypatch)
     mha.mha.mha_sublayer_fwd_static(*ws, **sub)
     rec.calls = [c for c in rec.calls if not c[0].endswith("_workspace_size")]
     names = [c[0] for c in rec.calls]
-    assert names == ["mha_fwd", "mha_fwd_ex", "mha_bwd", "mha_linear_fwd", "mha_sublayer_fwd",
-                     "mha_sublayer_fwd_static"]
+    assert names == ["mha_fwd", "mha_fwd_ex", "mha_bwd", "mha_fwd_lse", "mha_bwd_lse",
+                     "mha_linear_fwd", "mha_sublayer_fwd", "mha_sublayer_fwd_static"]
     for name, args in rec.calls:
         assert len(args) == len(getattr(real, name).argtypes), name
     a = dict(rec.calls)
@@ -419,6 +450,8 @@ def test_bindings_pass_each_entry_point_its_declared_arguments(mha, monkeypatch)
     assert a["mha_fwd_ex"][4:13] == (2, 4, 2, 8, 8, 64, 64, 0, 2)  # ..., H_kv, ..., layout, mask
     assert a["mha_bwd"][8:17] == (2, 4, 2, 8, 8, 64, 64, 0, 2)
     assert a["mha_bwd"][-2] == 4096  # workspace bytes
+    assert a["mha_fwd_lse"][5:14] == (2, 4, 2, 8, 8, 64, 64, 0, 2)  # after out and lse
+    assert a["mha_bwd_lse"][9:18] == (2, 4, 2, 8, 8, 64, 64, 0, 2)  # after the gradients
     assert a["mha_linear_fwd"][4:8] == (64, 64, 32, 1)  # M, K, N, dtype
     assert a["mha_sublayer_fwd"][11:19] == (B, T, S, d, H, Hkv, dk, dk)
     assert a["mha_sublayer_fwd"][-2] == 1 << 20

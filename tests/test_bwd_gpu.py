@@ -28,7 +28,10 @@ C, KP, QP, TAIL = gen.MASK_CAUSAL, gen.MASK_KEY_PADDING, gen.MASK_QUERY_PADDING,
 BWD_TOL = {"f32": dict(max=1e-4, mean=1e-4), "bf16": dict(max=2e-2, mean=2e-3)}
 
 
-def run_bwd(s, seed, lens=None, scale=None):
+def run_bwd(s, seed, lens=None, scale=None, use_lse=False):
+    """Forward then backward on the GPU; with ``use_lse`` the forward is
+    mha_fwd_lse (its output must equal mha_fwd_ex's bit for bit) and the
+    backward takes its row statistics."""
     import torch
     import transformer_head_scaled_mha_gb300 as mha
     q, k, v, glens = gen.make_inputs(s, seed=seed)
@@ -40,8 +43,14 @@ def run_bwd(s, seed, lens=None, scale=None):
     Q, K, V, DO = (to_device(a, dt) for a in (q, k, v, dout))
     out = mha.mha_fwd_ex(Q, K, V, layout=layout, mask_kind=s["mask"], key_lengths=kl, scale=scale)
     assert np.isfinite(gen.as_f64(from_device(out), dt)).all(), "forward output non-finite"
+    lse = None
+    if use_lse:
+        out2, lse = mha.mha_fwd_lse(Q, K, V, layout=layout, mask_kind=s["mask"], key_lengths=kl,
+                                    scale=scale)
+        assert torch.equal(out2.view(torch.int16 if dt == "bf16" else torch.int32),
+                           out.view(torch.int16 if dt == "bf16" else torch.int32))
     dq, dk, dv = mha.mha_bwd(Q, K, V, out, DO, layout=layout, mask_kind=s["mask"], key_lengths=kl,
-                             scale=scale)
+                             scale=scale, lse=lse)
     torch.cuda.synchronize()
     assert mha.mha_debug_status() == mha.MHA_OK
     got = [gen.as_f64(from_device(t), dt) for t in (dq, dk, dv)]
@@ -130,6 +139,21 @@ CASES = [
 def test_backward_parity(s):
     got, ref = run_bwd(s, seed=41)
     compare_grads(got, ref, s["dtype"], label=_id(s))
+
+
+@pytest.mark.parametrize("s", CASES, ids=_id)
+def test_backward_parity_with_forward_lse(s):
+    # mha_bwd_lse: the forward's statistics in place of the statistics pass
+    got, ref = run_bwd(s, seed=41, use_lse=True)
+    compare_grads(got, ref, s["dtype"], label=_id(s) + " lse")
+
+
+def test_backward_with_forward_lse_padding_edges():
+    s = spec(4, 2, 64, 64, 64, mask=KP | QP, layout="bshd", Hkv=1)
+    got, ref = run_bwd(s, seed=42, lens=[0, 1, 64, 33], use_lse=True)
+    compare_grads(got, ref, "bf16", label="padding edges lse")
+    dq, dk, dv = got
+    assert np.all(dq[0] == 0) and np.all(dk[0] == 0) and np.all(dv[0] == 0)
 
 
 def test_backward_padding_edges():

@@ -1296,15 +1296,57 @@ cudaError_t launch_one(K kernel, size_t smem, long long grid, const LongMaps &ma
   return cudaGetLastError();
 }
 
+// D_i = dout_i . out_i per query row (bf16 tensors, fp32 sums): D / 8 lanes
+// per row, 16 bytes of each tensor per lane and step, a shuffle tree per row
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dsum_kernel(const Problem p, const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8, kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow, c = (lane % kLanesPerRow) * 8;
+  const size_t rows = static_cast<size_t>(p.B) * p.H * p.Lq;
+  const size_t warp0 = (blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x) >> 5;
+  const size_t nwarps = (gridDim.x * static_cast<size_t>(blockDim.x)) >> 5;
+  for (size_t r0 = warp0 * kRowsPerWarp; r0 < rows; r0 += nwarps * kRowsPerWarp) {
+    const size_t row = r0 + sub;
+    float s = 0.f;
+    if (row < rows) {
+      const int i = static_cast<int>(row % p.Lq);
+      const size_t bh = row / p.Lq;
+      const int b = static_cast<int>(bh / p.H), h = static_cast<int>(bh % p.H);
+      const size_t at = row_at(p.layout, b, h, i, p.H, p.Lq, D) + c;
+      const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.out) + at);
+      const uint4 gv = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + at);
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        s = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), s);
+        s = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u), s);
+      }
+    }
+#pragma unroll
+    for (int o = kLanesPerRow / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (row < rows && c == 0) a.dsum[row] = s;
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_tc_impl(const LongMaps &maps, const Problem &p, const BwdArgs &a,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool have_lse) {
   static_assert(StatsCfg<D>::kSmem <= 232448 && DqCfg<D>::kSmem <= 232448 &&
                     DkdvCfg<D>::kSmem <= 232448,
                 "shared memory budget");
   const long long nqb = (p.Lq + kT - 1) / kT, nkb = (p.Lk + kT - 1) / kT;
   const long long q_grid = nqb * p.B * p.H, k_grid = nkb * p.B * p.Hkv;
-  cudaError_t e = launch_one(bwd_stats_tc_kernel<D>, StatsCfg<D>::kSmem, q_grid, maps, p, a, stream);
+  cudaError_t e = cudaSuccess;
+  if (have_lse) {
+    // the row statistics came with the forward pass: only D is left to form
+    const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
+    const long long blocks = (rows + 63) / 64;  // grid-stride beyond 8192 blocks
+    bwd_dsum_kernel<D><<<static_cast<unsigned>(blocks < 8192 ? blocks : 8192), 256, 0, stream>>>(p, a);
+    e = cudaGetLastError();
+  } else {
+    e = launch_one(bwd_stats_tc_kernel<D>, StatsCfg<D>::kSmem, q_grid, maps, p, a, stream);
+  }
   if (e != cudaSuccess) return e;
   e = launch_one(bwd_dq_tc_kernel<D>, DqCfg<D>::kSmem, q_grid, maps, p, a, stream);
   if (e != cudaSuccess) return e;
@@ -1315,15 +1357,15 @@ cudaError_t launch_bwd_tc_impl(const LongMaps &maps, const Problem &p, const Bwd
 }  // namespace
 
 cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a, int num_sms,
-                          cudaStream_t stream) {
-  if (p.dk == 128) return launch_bwd_tc_impl<128>(maps, p, a, stream);
+                          cudaStream_t stream, bool have_lse) {
+  if (p.dk == 128) return launch_bwd_tc_impl<128>(maps, p, a, stream, have_lse);
   if (p.Lq <= kT && p.Lk <= kT) {
     // one tile each way: the fused persistent kernel (no statistics pass)
     const long long units = static_cast<long long>(p.B) * p.Hkv;
     return launch_one(bwd_short_tc_kernel, kSbSmem, units < num_sms ? units : num_sms, maps, p,
                       a, stream);
   }
-  return launch_bwd_tc_impl<64>(maps, p, a, stream);
+  return launch_bwd_tc_impl<64>(maps, p, a, stream, have_lse);
 }
 
 }  // namespace mha

@@ -431,10 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                : (static_cast<size_t>(b) * p.Lq + pos) * p.H + h;
         return out + row * D + vdim;
       };
+      // statistics row of row r (the [B, H, Lq] lse)
+      auto lse_at = [&](int r) -> float * {
+        const int hl = r / p.Lq, pos = r - hl * p.Lq;
+        return p.lse + (static_cast<size_t>(b) * p.H + g * group + hl) * p.Lq + pos;
+      };
       if (nt == 0) {
         // no key at all: the rows are +0.0
         if (stores)
           for (int r = 0; r < R; ++r) *out_at(r) = 0;
+        if (p.lse != nullptr && k == 0)
+          for (int r = 0; r < R; ++r) *lse_at(r) = INFINITY;
         continue;
       }
       // keys j < jbase (+ the row's position under the cached-decoding mask)
@@ -563,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (D == 64) acc += sh->xo[r][vdim];
             // a row with no allowed key is stored as +0.0
             *out_at(r) = bf16_bits(lt > 0.f ? acc * (1.f / lt) : 0.f);
+            if (p.lse != nullptr && k == 0) *lse_at(r) = lt > 0.f ? m[r] + __log2f(lt) : INFINITY;
           }
       }
       // lsum and xo are rewritten only after the next pair's first tile

@@ -158,6 +158,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (i >= p.Lq) continue;
     const bool zero_row = (l[r] == 0.f) || ((p.mask & kMaskQueryPadding) && i >= len);
     const float inv = zero_row ? 0.f : 1.f / l[r];
+    if (p.lse != nullptr && lane == 0)
+      p.lse[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] =
+          zero_row ? INFINITY : m[r] + __log2f(l[r]);
 #pragma unroll
     for (int t = 0; t < kMaxD / 32; ++t) {
       const int c = lane + 32 * t;
@@ -190,6 +193,20 @@ cudaError_t launch_f32_simt(const float *q, const float *k, const float *v, floa
   }
   attn_f32_simt_kernel<<<static_cast<unsigned>(grid), kWarps * 32, smem, stream>>>(q, k, v, out,
                                                                                   p);
+  return cudaGetLastError();
+}
+
+__global__ void fill_f32_kernel(float *__restrict__ dst, size_t n, float value) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += stride)
+    dst[i] = value;
+}
+
+cudaError_t launch_fill_f32(float *dst, size_t n, float value, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  unsigned grid = static_cast<unsigned>(n / 256 + 1);
+  if (grid > 4096) grid = 4096;
+  fill_f32_kernel<<<grid, 256, 0, stream>>>(dst, n, value);
   return cudaGetLastError();
 }
 

@@ -458,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && wg_rows[w]) {
       const bool zero_row = qpad || l_run == 0.f || nt == 0;
       const float inv = zero_row ? 0.f : 1.f / l_run;
+      if (p.lse != nullptr && i < p.Lq)
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] =
+            zero_row ? INFINITY : m_use + __log2f(l_run);
       if (nt > 0) tc_fence_after();
       {
         uint8_t *stage = q_smem + w * C::kTileBytes;

@@ -511,6 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = zero_row ? 0.f : 1.f / rowsum;
       const int b = cur.b, h0 = cur.hu * g.P;
+      if (p.lse != nullptr && valid)
+        p.lse[(static_cast<size_t>(b) * p.H + h0 + pr) * p.Lq + i] =
+            zero_row ? INFINITY : ms + __log2f(rowsum);
       uint8_t *obase = static_cast<uint8_t *>(out) + b * batch_stride;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {

@@ -35,6 +35,9 @@ struct Problem {
   uint64_t wait_ns;            // a bounded wait gives up after this long
   int stall;                   // test hook: kStall* bits make a kernel wait on a barrier
                                // that nothing signals (0 in normal use)
+  float *lse;                  // device [B, H, Lq] or nullptr: each row's log2 of the
+                               // softmax denominator of the scaled scores (+inf for a
+                               // row stored as zeros), for the backward pass
 };
 
 // Test hooks for the give-up path of the bounded waits (Problem::stall).
@@ -97,12 +100,17 @@ struct BwdArgs {
   float scale;  // dq and dk carry this factor
 };
 cudaError_t launch_bwd_simt(const BwdArgs &a, const Problem &p, bool bf16, cudaStream_t stream);
+// D = dout . out per query row into a.dsum (bf16 tensors), when the row
+// statistics lse come from the forward pass instead of a statistics pass
+cudaError_t launch_bwd_dsum(const BwdArgs &a, const Problem &p, cudaStream_t stream);
 // bf16, d in {64, 128}: maps q, k, v and (in the `o` slot) dout, box
 // (64, 128, 1, 1)
 cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a, int num_sms,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool have_lse = false);
 
 cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
+// dst[0, n) = value
+cudaError_t launch_fill_f32(float *dst, size_t n, float value, cudaStream_t stream);
 
 // y = x W + b (bf16), 128-byte swizzle.  Slab tiling (K, N multiples of 64):
 // x viewed as (64, M, K/64) box (64, 128, 2), W as (64, K, N/64) box

@@ -258,9 +258,12 @@ extern "C" int mha_fwd_path_ex(int B, int H, int H_kv, int Lq, int Lk, int d_k, 
   return select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
 }
 
-extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H,
-                          int H_kv, int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
-                          const int32_t *key_lengths, float scale, int dtype, void *stream_) {
+namespace {
+
+// mha_fwd_ex, and with `lse` non-null each row's statistics for the backward
+int fwd_impl(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+             int H_kv, int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
+             const int32_t *key_lengths, float scale, int dtype, void *stream_) {
   const int path = select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
   if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
@@ -282,6 +285,12 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   if (overlaps(out, no, q, nq) || overlaps(out, no, k, nk) || overlaps(out, no, v, nv) ||
       (padded && overlaps(out, no, key_lengths, sizeof(int32_t) * B)))
     return MHA_ERR_INVALID_ARGUMENT;
+  const size_t nl = sizeof(float) * static_cast<size_t>(B) * H * Lq;
+  if (lse != nullptr &&
+      (reinterpret_cast<uintptr_t>(lse) % 4 != 0 || overlaps(lse, nl, out, no) ||
+       overlaps(lse, nl, q, nq) || overlaps(lse, nl, k, nk) || overlaps(lse, nl, v, nv) ||
+       (padded && overlaps(lse, nl, key_lengths, sizeof(int32_t) * B))))
+    return MHA_ERR_INVALID_ARGUMENT;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev = 0;
@@ -302,10 +311,14 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   if (p.status == nullptr) return MHA_ERR_CUDA;
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   p.stall = g_stall.load(std::memory_order_relaxed);
+  p.lse = lse;
 
   cudaError_t err = cudaSuccess;
   if (path == kPathZero) {
+    // no keys: every row is stored as zeros and has no statistics
     err = launch_zero_fill(out, no, stream);
+    if (err == cudaSuccess && lse != nullptr)
+      err = launch_fill_f32(lse, nl / sizeof(float), INFINITY, stream);
   } else if (path == kPathF32) {
     err = launch_f32_simt(static_cast<const float *>(q), static_cast<const float *>(k),
                           static_cast<const float *>(v), static_cast<float *>(out), p, stream);
@@ -371,6 +384,24 @@ extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" int mha_fwd_ex(const void *q, const void *k, const void *v, void *out, int B, int H,
+                          int H_kv, int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
+                          const int32_t *key_lengths, float scale, int dtype, void *stream) {
+  return fwd_impl(q, k, v, out, nullptr, B, H, H_kv, Lq, Lk, d_k, d_v, layout, mask_kind,
+                  key_lengths, scale, dtype, stream);
+}
+
+extern "C" int mha_fwd_lse(const void *q, const void *k, const void *v, void *out, float *lse,
+                           int B, int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
+                           int mask_kind, const int32_t *key_lengths, float scale, int dtype,
+                           void *stream) {
+  if (lse == nullptr && static_cast<long long>(B) * H * Lq > 0) return MHA_ERR_INVALID_ARGUMENT;
+  return fwd_impl(q, k, v, out, lse, B, H, H_kv, Lq, Lk, d_k, d_v, layout, mask_kind,
+                  key_lengths, scale, dtype, stream);
+}
+
 extern "C" int mha_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
                        int Lq, int Lk, int d_k, int d_v, int mask_kind,
                        const int32_t *key_lengths, float scale, int dtype, void *stream) {
@@ -390,11 +421,14 @@ extern "C" size_t mha_bwd_workspace_size(int B, int H, int Lq) {
   return 2 * bwd_round(static_cast<size_t>(B) * H * Lq * sizeof(float));
 }
 
-extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *out,
-                       const void *dout, void *dq, void *dk, void *dv, int B, int H, int H_kv,
-                       int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
-                       const int32_t *key_lengths, float scale, int dtype, void *workspace,
-                       size_t workspace_bytes, void *stream_) {
+namespace {
+
+// mha_bwd, and with `lse_in` non-null the forward's row statistics in place of
+// a statistics pass
+int bwd_impl(const void *q, const void *k, const void *v, const void *out, const void *dout,
+             const float *lse_in, void *dq, void *dk, void *dv, int B, int H, int H_kv, int Lq,
+             int Lk, int d_k, int d_v, int layout, int mask_kind, const int32_t *key_lengths,
+             float scale, int dtype, void *workspace, size_t workspace_bytes, void *stream_) {
   const int path = select_path(B, H, H_kv, Lq, Lk, d_k, d_v, mask_kind, dtype);
   if (path < 0) return -path;
   if (layout != kLayoutBHSD && layout != kLayoutBSHD) return MHA_ERR_INVALID_ARGUMENT;
@@ -437,6 +471,13 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
     if (overlaps(workspace, nws, ins[i], in_n[i])) return MHA_ERR_INVALID_ARGUMENT;
   if (padded && overlaps(workspace, nws, key_lengths, sizeof(int32_t) * B))
     return MHA_ERR_INVALID_ARGUMENT;
+  const size_t nl = sizeof(float) * static_cast<size_t>(B) * H * Lq;
+  if (lse_in != nullptr) {
+    if (reinterpret_cast<uintptr_t>(lse_in) % 4 != 0 || overlaps(lse_in, nl, workspace, nws))
+      return MHA_ERR_INVALID_ARGUMENT;
+    for (int o = 0; o < 3; ++o)
+      if (overlaps(outs[o], out_n[o], lse_in, nl)) return MHA_ERR_INVALID_ARGUMENT;
+  }
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int dev = 0;
@@ -488,11 +529,34 @@ extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *
     if (!ok) return MHA_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return MHA_ERR_CUDA;
-    err = launch_bwd_tc(m, p, a, sms, stream);
+    if (lse_in != nullptr) a.lse = const_cast<float *>(lse_in);  // read only
+    err = launch_bwd_tc(m, p, a, sms, stream, lse_in != nullptr);
   } else {
+    // the fp32 path recomputes the statistics (its lse and D come together)
     err = launch_bwd_simt(a, p, false, stream);
   }
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int mha_bwd(const void *q, const void *k, const void *v, const void *out,
+                       const void *dout, void *dq, void *dk, void *dv, int B, int H, int H_kv,
+                       int Lq, int Lk, int d_k, int d_v, int layout, int mask_kind,
+                       const int32_t *key_lengths, float scale, int dtype, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  return bwd_impl(q, k, v, out, dout, nullptr, dq, dk, dv, B, H, H_kv, Lq, Lk, d_k, d_v, layout,
+                  mask_kind, key_lengths, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int mha_bwd_lse(const void *q, const void *k, const void *v, const void *out,
+                           const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                           int H, int H_kv, int Lq, int Lk, int d_k, int d_v, int layout,
+                           int mask_kind, const int32_t *key_lengths, float scale, int dtype,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  if (lse == nullptr && static_cast<long long>(B) * H * Lq > 0) return MHA_ERR_INVALID_ARGUMENT;
+  return bwd_impl(q, k, v, out, dout, lse, dq, dk, dv, B, H, H_kv, Lq, Lk, d_k, d_v, layout,
+                  mask_kind, key_lengths, scale, dtype, workspace, workspace_bytes, stream);
 }
 
 namespace {

@@ -20,7 +20,8 @@ PATH_NAMES = {0: "none", 1: "f32_simt", 2: "short_tc", 3: "long_tc", 4: "zero_fi
 
 MHA_LAYOUT_BHSD, MHA_LAYOUT_BSHD = 0, 1
 
-EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_linear_fwd", "mha_sublayer_workspace_size",
+EXPORTED = ("mha_fwd", "mha_fwd_ex", "mha_fwd_lse", "mha_bwd_lse", "mha_linear_fwd",
+            "mha_sublayer_workspace_size",
             "mha_sublayer_fwd", "mha_sublayer_fwd_static", "mha_bwd_workspace_size", "mha_bwd",
             "mha_fwd_path", "mha_fwd_path_ex",
             "mha_status_string", "mha_debug_status", "mha_debug_set_wait", "mha_version")
@@ -46,6 +47,12 @@ def _load() -> ctypes.CDLL:
     lib.mha_fwd_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, vp,
                                ctypes.c_float, i32, vp]
     lib.mha_linear_fwd.restype = i32
+    lib.mha_fwd_lse.restype = i32
+    lib.mha_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                vp, ctypes.c_float, i32, vp]
+    lib.mha_bwd_lse.restype = i32
+    lib.mha_bwd_lse.argtypes = [vp] * 9 + [i32] * 9 + [vp, ctypes.c_float, i32, vp,
+                                                       ctypes.c_size_t, vp]
     lib.mha_linear_fwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.mha_sublayer_workspace_size.restype = ctypes.c_size_t
     lib.mha_sublayer_workspace_size.argtypes = [i32] * 8
@@ -220,17 +227,48 @@ def mha_fwd_ex(q, k, v, out=None, *, layout: str = "bhsd", mask_kind: int = 0,
     return out
 
 
+def _lse_tensor(lse, B, H, Lq, device):
+    import torch
+    if lse is None:
+        return torch.empty((B, H, Lq), dtype=torch.float32, device=device)
+    if tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != device:
+        raise ValueError("lse must be a contiguous float32 tensor of shape %s on q's device"
+                         % ((B, H, Lq),))
+    return lse
+
+
+def mha_fwd_lse(q, k, v, out=None, lse=None, *, layout: str = "bhsd", mask_kind: int = 0,
+                key_lengths=None, scale=None, stream=None):
+    """mha_fwd_ex that also returns each row's softmax statistics ``lse``
+    [B, H, Lq] (float32, base 2, +inf for rows stored as zeros), which
+    mha_bwd_lse takes.  Returns (out, lse)."""
+    import torch
+    out, (B, H, Hkv, Lq, Lk, dk, dv), kl_ptr, scale, dtype = _marshal(q, k, v, out, key_lengths,
+                                                                      scale, layout)
+    lse = _lse_tensor(lse, B, H, Lq, q.device)
+    with torch.cuda.device(q.device):
+        st = lib.mha_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, H, Hkv, Lq, Lk, dk, dv,
+                             MHA_LAYOUT_BSHD if layout == "bshd" else MHA_LAYOUT_BHSD,
+                             int(mask_kind), kl_ptr, scale, dtype, _stream_handle(stream))
+    if st != MHA_OK:
+        raise MhaError(st, "mha_fwd_lse")
+    return out, lse
+
+
 def mha_bwd_workspace_size(B, H, Lq) -> int:
     return int(lib.mha_bwd_workspace_size(B, H, Lq))
 
 
 def mha_bwd(q, k, v, out, dout, *, layout: str = "bhsd", mask_kind: int = 0, key_lengths=None,
-            scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+            scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None, lse=None):
     """Gradients (dq, dk, dv) of a loss through mha_fwd_ex, given its output
     ``out`` and the incoming gradient ``dout`` (out's shape).  Same layouts,
     shared key/value heads, masks and scale as mha_fwd_ex.  ``workspace``: a
     uint8 CUDA tensor of at least mha_bwd_workspace_size(B, H, Lq) bytes, or
-    None to allocate one."""
+    None to allocate one.  ``lse``: the forward's row statistics from
+    mha_fwd_lse (then mha_bwd_lse runs: no statistics pass), or None."""
     import torch
     _, (B, H, Hkv, Lq, Lk, dk_, dv_), kl_ptr, scale, dtype = _marshal(q, k, v, out, key_lengths,
                                                                       scale, layout)
@@ -248,14 +286,22 @@ def mha_bwd(q, k, v, out, dout, *, layout: str = "bhsd", mask_kind: int = 0, key
     if workspace is None:
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     ws_bytes = _workspace_bytes(workspace, q.device)
+    lay = MHA_LAYOUT_BSHD if layout == "bshd" else MHA_LAYOUT_BHSD
     with torch.cuda.device(q.device):
-        st = lib.mha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv,
-                         Lq, Lk, dk_, dv_, MHA_LAYOUT_BSHD if layout == "bshd" else MHA_LAYOUT_BHSD,
-                         int(mask_kind), kl_ptr, scale, dtype, workspace.data_ptr(), ws_bytes,
-                         _stream_handle(stream))
+        if lse is None:
+            st = lib.mha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H,
+                             Hkv, Lq, Lk, dk_, dv_, lay, int(mask_kind), kl_ptr, scale, dtype,
+                             workspace.data_ptr(), ws_bytes, _stream_handle(stream))
+        else:
+            lse = _lse_tensor(lse, B, H, Lq, q.device)
+            st = lib.mha_bwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, H, Hkv, Lq, Lk, dk_, dv_, lay, int(mask_kind),
+                                 kl_ptr, scale, dtype, workspace.data_ptr(), ws_bytes,
+                                 _stream_handle(stream))
     if st != MHA_OK:
-        raise MhaError(st, "mha_bwd")
+        raise MhaError(st, "mha_bwd" if lse is None else "mha_bwd_lse")
     return dq, dk, dv
 
 
