@@ -32,8 +32,9 @@
 // the next S (its warpgroup free, Q and K landed) and the next P V (P
 // posted, V landed) is ready.
 // Padded sequences load only their first ceil(len/8)*8 rows, as one TMA box
-// of that height per tensor and pair, so padding costs no HBM reads (a CTA's
-// first unit loads whole tiles instead, so it does not wait for the lengths).
+// of that height per tensor and pair.  Before the dependency wait a CTA warms
+// L2 with the whole tiles of its first two units: that traffic overlaps the
+// previous grid's tail, when HBM would otherwise idle.
 // Masked keys get exactly zero weight; padded query rows and rows without any
 // allowed key are stored as +0.  All tensor maps are 4-D (d, L, heads, B), so
 // the [B, H, L, d] and [B, L, H, d] layouts run the same code.
@@ -293,11 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // never stored, reads the last head so every box is in bounds)
       const int hq = min(h0 + pp, p.H - 1);
       const int hkv = group == 1 ? hq : hq / group;
-      // the first unit loads whole tiles: no wait for the lengths
-      const bool rows_q = g.rows_q && n > 0, rows_k = g.rows_k && n > 0;
+      const bool rows_q = g.rows_q != 0, rows_k = g.rows_k != 0;
       const bool has_pair = pp < g.P && h0 + pp < p.H;
       if (n > 0 && (n & 31) == 0) lens = load_lens(n);
-      const int len = n > 0 ? __shfl_sync(0xffffffffu, lens, n & 31) : 0;
+      const int len = __shfl_sync(0xffffffffu, lens, n & 31);
       // with unshared key/value heads the P pairs' first ceil8(len) key rows
       // come in as one box, packed back to back (see the softmax)
       const bool packed = rows_k && group == 1;
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!valid || qpad) jmax = 0;
       // key columns of this row's pair: packed units hold pair pr's keys at
       // [pr * ceil8(len), ...); whole-tile units (a CTA's first) at pr * Rk
-      const bool packed = g.rows_k && group == 1 && n > 0;
+      const bool packed = g.rows_k && group == 1;
       const int col_lo = pr * (packed ? ((len + 7) & ~7) : g.Rk);
       // 32-column chunks any row of this warp can use
       const unsigned lo = __reduce_min_sync(0xffffffffu, jmax > 0 ? col_lo : 1 << 20);
