@@ -128,6 +128,12 @@ CASES = [
     spec(2, 2, 200, 333, 64, mask=KP, len_range=(0, 333)),
     spec(1, 4, 257, 257, 128, mask=C | KP, len_range=(100, 257), Hkv=1, layout="bshd"),
     spec(3, 2, 1, 500, 64, mask=TAIL | KP, len_range=(1, 500)),
+    # short tiles packed several (batch, head) pairs to a tile, heads past
+    # the last one in a tile's final group
+    spec(3, 5, 20, 20, 64, mask=KP | QP, len_range=(0, 20)),
+    spec(2, 16, 8, 8, 64, mask=C),
+    spec(2, 3, 50, 33, 64, mask=KP, len_range=(1, 33), layout="bshd"),
+    spec(4, 8, 64, 64, 64, mask=KP | QP, len_range=(8, 64), layout="bshd"),
     # several query and key tiles with shared key/value heads
     spec(2, 4, 640, 640, 128, mask=C, amp=0.5, Hkv=2, layout="bshd"),
     spec(2, 6, 333, 555, 64, mask=KP, len_range=(100, 555), Hkv=3),

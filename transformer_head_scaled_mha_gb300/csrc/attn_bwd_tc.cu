@@ -953,33 +953,52 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
 // ============================================================================
 // short: query and key lengths of one tile (<= 128), d = 64 -- the whole
-// backward of a (batch, key/value head) pair in one persistent CTA
+// backward of a unit of (batch, key/value head) pairs in one persistent CTA
 // ============================================================================
-// Per query head of the pair's group, two phases over the same tiles:
-//   A  S = Q K^T, dP = dout V^T (rows on the lanes): the row's exact softmax
-//      over its one key tile gives lse, dS = w (dP - D) goes over dP in TMEM,
-//      dQ = dS K
-//   B  S^T = K Q^T, dP^T = V dout^T (keys on the lanes): w^T and dS^T from the
-//      lse and D of phase A, dV += w^T dout, dK += dS^T Q over the group
-// K and V of the next pair, and Q and dout of the next head, load while the
-// current one computes.  TMEM: S | dP | dQ | dV | dK (448 columns).
+// A unit holds a.pack pairs of one batch element (packed like the forward's
+// short kernel: pair p in tile rows [p R, p R + R), R = 128 / pack; products
+// between different pairs land in blocks that are masked to zero) or, with
+// shared key/value heads, one pair and the query heads of its group.  Per
+// query head (thread r of the softmax warpgroup owns tile row r):
+//   S = Q K^T, dP = dout V^T          tcgen05.mma -> TMEM (rows on the lanes)
+//   w = softmax(S) over the row's allowed keys (its one key tile gives the
+//   exact statistics), dS = w (dP - D), D = dout . out
+//   w, dS (bf16) -> shared memory, one [128 x 128] tile each in the 128-byte
+//   swizzled layout (two 64-key slabs): read K-major it is the A operand
+//   [queries x keys] of dQ = dS K, read MN-major the A operand [keys x
+//   queries] of dV += w^T dout and dK += dS^T Q, so nothing is recomputed
+//   with the keys on the lanes
+// S and dP of head n + 1 go out as soon as the softmax has read those of head
+// n, so the products of one head overlap the softmax of the next; the softmax
+// stores dQ of head n (and dV, dK of a finished unit) after the exponentials
+// of head n + 1.  K and V of the next unit and Q and dout of the next head
+// load while the current one computes.  TMEM: S | dP | dQ | dV | dK (448
+// columns).
 struct ShortBwdBars {
-  uint64_t kv_full[2], kv_empty[2];  // K, V of a pair (by pair parity)
+  uint64_t kv_full[2], kv_empty[2];  // K, V of a unit (by unit parity)
   uint64_t qd_full[2], qd_empty[2];  // Q, dout of a head (by iteration parity)
-  uint64_t a_full;    // S, dP in TMEM
-  uint64_t ds_ready;  // dS in TMEM, lse and D in smem (softmax threads)
+  uint64_t sd_full;   // S, dP in TMEM
+  uint64_t sd_free;   // S, dP read (softmax threads)
+  uint64_t wd_full;   // w, dS in shared memory (softmax threads)
+  uint64_t wd_free;   // the gradient products that read w, dS are done
   uint64_t dq_full;   // dQ in TMEM
   uint64_t dq_free;   // dQ read (softmax threads)
-  uint64_t b_full;    // S^T, dP^T in TMEM
-  uint64_t pds_ready; // w^T, dS^T in TMEM (softmax threads)
-  uint64_t dkv_full;  // dV, dK of a pair complete
+  uint64_t dkv_full;  // dV, dK of a unit complete
   uint64_t dkv_free;  // dV, dK read (softmax threads)
+  uint64_t drain;     // teardown: the MMA thread's products have finished
   uint32_t tmem_base;
   int abort_flag;
 };
 constexpr int kSbTile = 128 * 128;  // one [128 x 64] bf16 tile
-constexpr size_t kSbSmem = 1024 + 8 * static_cast<size_t>(kSbTile) + 2 * 2 * kT * 4 + 512;
+// K, V (two units), Q, dout (two heads), w and dS (two 64-key slabs each)
+constexpr size_t kSbSmem = 1024 + 12 * static_cast<size_t>(kSbTile) + 512;
 constexpr uint32_t kSbS = 0, kSbDp = 128, kSbDq = 256, kSbDv = 320, kSbDk = 384;
+
+// byte offset of 16-byte piece c (0..15: keys 8c .. 8c + 7) of row r in a
+// [128 x 128] bf16 tile stored as two 128-byte-swizzled 64-key slabs
+__device__ __forceinline__ uint32_t wd_offset(uint32_t r, uint32_t c) {
+  return (c >> 3) * kSbTile + r * 128u + (((c & 7u) ^ (r & 7u)) << 4);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_short_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
@@ -988,17 +1007,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *kv_smem = smem;                   // 2 x (K, V)
   uint8_t *qd_smem = kv_smem + 4 * kSbTile;  // 2 x (Q, dout)
-  float *stat = reinterpret_cast<float *>(qd_smem + 4 * kSbTile);  // 2 x (lse[128], D[128])
-  ShortBwdBars *bars = reinterpret_cast<ShortBwdBars *>(reinterpret_cast<uint8_t *>(stat) +
-                                                        2 * 2 * kT * 4);
+  uint8_t *w_smem = qd_smem + 4 * kSbTile;   // w: two slabs
+  uint8_t *ds_smem = w_smem + 2 * kSbTile;   // dS: two slabs
+  ShortBwdBars *bars = reinterpret_cast<ShortBwdBars *>(ds_smem + 2 * kSbTile);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int group = p.H / p.Hkv;
-  const int units = p.B * p.Hkv;
+  const int P = a.pack, R = kT / a.pack;  // pairs per unit (1 when group > 1), rows per pair
+  const int upb = (p.Hkv + P - 1) / P;    // units per batch element
+  const int units = p.B * upb;
+  const int G = static_cast<int>(gridDim.x);
   const int n_local = static_cast<int>(blockIdx.x) < units
-                          ? (units - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                          ? (units - 1 - static_cast<int>(blockIdx.x)) / G + 1
                           : 0;
+  const int n_it = n_local * group;  // (unit, query head) iterations of this CTA
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -1007,14 +1030,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qd_full[i], 1);
       mbar_init(&bars->qd_empty[i], 1);
     }
-    mbar_init(&bars->a_full, 1);
-    mbar_init(&bars->ds_ready, kWg);
+    mbar_init(&bars->sd_full, 1);
+    mbar_init(&bars->sd_free, kWg);
+    mbar_init(&bars->wd_full, kWg);
+    mbar_init(&bars->wd_free, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, kWg);
-    mbar_init(&bars->b_full, 1);
-    mbar_init(&bars->pds_ready, kWg);
     mbar_init(&bars->dkv_full, 1);
     mbar_init(&bars->dkv_free, kWg);
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -1027,15 +1051,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   int kv_issued = 0, qd_issued = 0;
-  uint64_t *last_commit = nullptr;
-  uint32_t last_parity = 0;
+  bool mma_issued = false;
 
   if (warp == 4) {
-    // ---- producer: per pair K and V, then Q and dout of each query head ----
+    // ---- producer: per unit K and V, then Q and dout of each query head ----
     int it = 0;
     for (int ul = 0; ul < n_local; ++ul) {
-      const int u = static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x);
-      const int b = u / p.Hkv, hk = u % p.Hkv;
+      const int u = static_cast<int>(blockIdx.x) + ul * G;
+      const int b = u / upb, hk0 = (u % upb) * P;
       const int kb = ul & 1;
       if (!__all_sync(0xffffffffu,
                       mbar_wait(&bars->kv_empty[kb], ((ul >> 1) & 1) ^ 1, abort_flag)))
@@ -1043,8 +1066,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         uint8_t *dst = kv_smem + 2 * kb * kSbTile;
         mbar_arrive_expect_tx(&bars->kv_full[kb], 2 * kSbTile);
-        tma_load_4d(dst, &maps.k, &bars->kv_full[kb], 0, 0, hk, b);
-        tma_load_4d(dst + kSbTile, &maps.v, &bars->kv_full[kb], 0, 0, hk, b);
+        tma_load_4d(dst, &maps.k, &bars->kv_full[kb], 0, 0, hk0, b);
+        tma_load_4d(dst + kSbTile, &maps.v, &bars->kv_full[kb], 0, 0, hk0, b);
       }
       kv_issued = ul + 1;
       bool ok = true;
@@ -1056,201 +1079,141 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           uint8_t *dst = qd_smem + 2 * st * kSbTile;
           mbar_arrive_expect_tx(&bars->qd_full[st], 2 * kSbTile);
-          tma_load_4d(dst, &maps.q, &bars->qd_full[st], 0, 0, hk * group + hl, b);
-          tma_load_4d(dst + kSbTile, &maps.o, &bars->qd_full[st], 0, 0, hk * group + hl, b);
+          tma_load_4d(dst, &maps.q, &bars->qd_full[st], 0, 0, hk0 * group + hl, b);
+          tma_load_4d(dst + kSbTile, &maps.o, &bars->qd_full[st], 0, 0, hk0 * group + hl, b);
         }
         qd_issued = it + 1;
       }
       if (!ok) break;
     }
   } else if (warp == 5) {
-    // ---- MMA issuer: per head A1 (S, dP), A2 (dQ), B1 (S^T, dP^T), B2 (dV, dK)
-    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);
-    const uint32_t idesc_g = idesc_bf16_f32(128, 64, 1);
-    bool ok = true;
-    int it = 0;
-    for (int ul = 0; ok && ul < n_local; ++ul) {
-      const int kb = ul & 1;
-      if (!(ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->kv_full[kb], (ul >> 1) & 1, abort_flag))))
-        break;
-      const uint32_t sk = smem_addr(kv_smem + 2 * kb * kSbTile), sv = sk + kSbTile;
-      for (int hl = 0; hl < group; ++hl, ++it) {
-        const int st = it & 1;
+    // ---- MMA issuer: S, dP of iteration n + 1 before the gradients of n ------
+    const uint32_t idesc_s = idesc_bf16_f32(128, kT, 0);  // A, B K-major
+    const uint32_t idesc_q = idesc_bf16_f32(128, 64, 1);  // A K-major, B MN-major
+    const uint32_t idesc_kv = idesc_q | (1u << 15);       // A and B MN-major
+    const uint32_t sw = smem_addr(w_smem), sds = smem_addr(ds_smem);
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    };
+    auto scores = [&](int it) -> bool {
+      const int ul = it / group, hl = it - ul * group, kb = ul & 1, st = it & 1;
+      if (hl == 0 && !wait(&bars->kv_full[kb], (ul >> 1) & 1)) return false;
+      if (!wait(&bars->qd_full[st], (it >> 1) & 1)) return false;
+      if (it >= 1 && !wait(&bars->sd_free, (it - 1) & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sk = smem_addr(kv_smem + 2 * kb * kSbTile), sv = sk + kSbTile;
         const uint32_t sq = smem_addr(qd_smem + 2 * st * kSbTile), sdo = sq + kSbTile;
-        if (!(ok = __all_sync(0xffffffffu,
-                              mbar_wait(&bars->qd_full[st], (it >> 1) & 1, abort_flag))))
-          break;
-        tc_fence_after();
-        if (lane == 0) {
-          mma_scores<64>(tmem + kSbS, sq, sk, idesc_s);     // S = Q K^T
-          mma_scores<64>(tmem + kSbDp, sdo, sv, idesc_s);   // dP = dout V^T
-          tc_commit(&bars->a_full);
-        }
-        __syncwarp();
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->ds_ready, it & 1, abort_flag));
-        // dQ of the previous head has been read
-        if (ok && it >= 1)
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->dq_free, (it - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          mma_grad<64>(tmem + kSbDq, tmem + kSbDp, sk, idesc_g, false);  // dQ = dS K
-          tc_commit(&bars->dq_full);
-          mma_scores<64>(tmem + kSbS, sk, sq, idesc_s);    // S^T = K Q^T
-          mma_scores<64>(tmem + kSbDp, sv, sdo, idesc_s);  // dP^T = V dout^T
-          tc_commit(&bars->b_full);
-          if (hl == group - 1) tc_commit(&bars->kv_empty[kb]);
-        }
-        __syncwarp();
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->pds_ready, it & 1, abort_flag));
-        // the pair's first head overwrites dV, dK: the previous pair's were read
-        if (ok && hl == 0 && ul >= 1)
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_free, (ul - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          mma_grad<64>(tmem + kSbDv, tmem + kSbS, sdo, idesc_g, hl > 0);  // dV += w^T dout
-          mma_grad<64>(tmem + kSbDk, tmem + kSbDp, sq, idesc_g, hl > 0);  // dK += dS^T Q
-          tc_commit(&bars->qd_empty[st]);
-          if (hl == group - 1) tc_commit(&bars->dkv_full);
-        }
-        __syncwarp();
-        last_commit = &bars->qd_empty[st];
-        last_parity = (it >> 1) & 1;
+        mma_scores<64>(tmem + kSbS, sq, sk, idesc_s);    // S = Q K^T
+        mma_scores<64>(tmem + kSbDp, sdo, sv, idesc_s);  // dP = dout V^T
+        tc_commit(&bars->sd_full);
       }
+      __syncwarp();
+      mma_issued = true;
+      return true;
+    };
+    auto grads = [&](int it) -> bool {
+      const int ul = it / group, hl = it - ul * group, kb = ul & 1, st = it & 1;
+      if (!wait(&bars->wd_full, it & 1)) return false;
+      if (it >= 1 && !wait(&bars->dq_free, (it - 1) & 1)) return false;
+      // the unit's first head overwrites dV, dK: the previous unit's were read
+      if (hl == 0 && ul >= 1 && !wait(&bars->dkv_free, (ul - 1) & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sk = smem_addr(kv_smem + 2 * kb * kSbTile);
+        const uint32_t sq = smem_addr(qd_smem + 2 * st * kSbTile), sdo = sq + kSbTile;
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          // dQ = dS K: A = dS K-major (16 keys = 32 bytes of a slab row), B =
+          // K MN-major (16 key rows = 2 KiB)
+          tc_mma_ss(tmem + kSbDq,
+                    smem_desc_sw128(sds + (kk >> 2) * kSbTile + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(sk + kk * 2048, kSbTile, 1024), idesc_q, kk > 0);
+        tc_commit(&bars->dq_full);
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          // dV += w^T dout, dK += dS^T Q: A MN-major (16 queries = 2 KiB; the
+          // two 64-key slabs one tile apart), B MN-major
+          const uint32_t acc = (hl > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_ss(tmem + kSbDv, smem_desc_sw128(sw + kk * 2048, kSbTile, 1024),
+                    smem_desc_sw128(sdo + kk * 2048, kSbTile, 1024), idesc_kv, acc);
+          tc_mma_ss(tmem + kSbDk, smem_desc_sw128(sds + kk * 2048, kSbTile, 1024),
+                    smem_desc_sw128(sq + kk * 2048, kSbTile, 1024), idesc_kv, acc);
+        }
+        tc_commit(&bars->wd_free);
+        tc_commit(&bars->qd_empty[st]);
+        if (hl == group - 1) {
+          tc_commit(&bars->kv_empty[kb]);
+          tc_commit(&bars->dkv_full);
+        }
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = n_it == 0 || scores(0);
+    for (int it = 0; ok && it < n_it; ++it) {
+      if (it + 1 < n_it && !(ok = scores(it + 1))) break;
+      ok = grads(it);
     }
   } else {
-    // ---- softmax: phase A thread r = query row r, phase B thread r = key r ---
+    // ---- softmax: thread r = tile row r (pair r / R, query r % R); for dV and
+    // dK thread r = tile row r of the keys ----------------------------------
     const int r = threadIdx.x;
+    const int pr = r / R, ri = r - pr * R;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    bool ok = true;
-    int it = 0;
-    for (int ul = 0; ok && ul < n_local; ++ul) {
-      const int u = static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x);
-      const int b = u / p.Hkv, hk = u % p.Hkv;
-      const int len = clamp_len(p, b);
-      const int jmax = r < p.Lq ? row_limit(p, len, r) : 0;  // phase A: keys j < jmax
-      // phase B: queries [i_min, i_max) may read key r
-      const bool key_ok = r < p.Lk && !((p.mask & kMaskKeyPadding) && r >= len);
-      int i_min = 0, i_max = p.Lq;
-      if (p.mask & kMaskCausal) i_min = r;
-      if (p.mask & kMaskCausalTail) i_min = max(i_min, r - len + p.Lq);
-      if (p.mask & kMaskQueryPadding) i_max = min(i_max, len);
-      if (!key_ok) i_max = i_min;
-      for (int hl = 0; hl < group; ++hl, ++it) {
-        const int h = hk * group + hl;
-        float *st = stat + (it & 1) * 2 * kT;
-        // D of row r, loaded while the scores are computed
-        float dd = 0.f;
-        if (r < p.Lq) {
-          const size_t ro = row_at(p.layout, b, h, r, p.H, p.Lq, 64);
-          const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.out) + ro);
-          const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + ro);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 ov = o4[c], gv = g4[c];
-            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              dd = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), dd);
-              dd = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u), dd);
-            }
-          }
-        }
-        // ---- phase A: the row's softmax over its one key tile, dS over dP
-        const bool oka = __all_sync(0xffffffffu, mbar_wait(&bars->a_full, it & 1, abort_flag));
-        if (oka) {
-          tc_fence_after();
-          uint32_t sr[4][32];
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
-          tmem_wait_ld();
-          const bool need_mask = __any_sync(0xffffffffu, jmax < kT);
-          const bool pos = p.scale_log2 > 0.f;
-          const float m = pos ? mask_max128(sr, need_mask, 0, jmax) * p.scale_log2
-                              : scale_mask_max128(sr, p.scale_log2, need_mask, 0, jmax);
-          const float l = pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
-                              : exp2_sum128(sr, m, m != -INFINITY);
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          st[r] = l > 0.f ? m + __log2f(l) : INFINITY;
-          st[kT + r] = dd;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t pv[32], pk[16];
-            tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float w0 = __uint_as_float(sr[ch][e]) * inv;
-              const float w1 = __uint_as_float(sr[ch][e + 1]) * inv;
-              pk[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
-                                       w1 * (__uint_as_float(pv[e + 1]) - dd));
-            }
-            tmem_st16(tmem + lane_base + kSbDp + ch * 16, pk);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        // every row's lse and D are in smem before phase B reads them
-        ok = named_barrier_and(1, kWg, ok && oka);
-        if (!ok) break;
-        mbar_arrive(&bars->ds_ready);
-        // ---- phase B: keys on the lanes, w^T and dS^T over S^T and dP^T
-        const bool okb = __all_sync(0xffffffffu, mbar_wait(&bars->b_full, it & 1, abort_flag));
-        if (okb) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t sv[32], pv[32], pw[16], pd[16];
-            tmem_ld32(tmem + lane_base + kSbS + ch * 32, sv);
-            tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
-            tmem_wait_ld();
-            const int lo = i_min - ch * 32, hi = i_max - ch * 32;
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float4 l4 = *reinterpret_cast<const float4 *>(st + ch * 32 + (e & ~3));
-              const float4 d4 = *reinterpret_cast<const float4 *>(st + kT + ch * 32 + (e & ~3));
-              const float la = (e & 2) ? l4.z : l4.x, lb = (e & 2) ? l4.w : l4.y;
-              const float da = (e & 2) ? d4.z : d4.x, db = (e & 2) ? d4.w : d4.y;
-              const bool oka2 = e >= lo && e < hi, okb2 = e + 1 >= lo && e + 1 < hi;
-              const float w0 = oka2 ? ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - la) : 0.f;
-              const float w1 = okb2 ? ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lb) : 0.f;
-              pw[e >> 1] = pack_bf16x2(w0, w1);
-              pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - da),
-                                       w1 * (__uint_as_float(pv[e + 1]) - db));
-            }
-            tmem_st16(tmem + lane_base + kSbS + ch * 16, pw);
-            tmem_st16(tmem + lane_base + kSbDp + ch * 16, pd);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->pds_ready);
-        // ---- dQ of this head (thread r = row r)
-        const bool okq = okb && __all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag));
-        if (okq) {
-          tc_fence_after();
-          uint16_t *dst = static_cast<uint16_t *>(a.dq) +
-                          (r < p.Lq ? row_at(p.layout, b, h, r, p.H, p.Lq, 64) : 0);
-#pragma unroll 1
-          for (int ch = 0; ch < 2; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kSbDq + ch * 32, v);
-            tmem_wait_ld();
-            if (r < p.Lq) store_row32(dst + ch * 32, v, a.scale);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->dq_free);
-        ok = okq;
-      }
-      // ---- dV and dK of the pair (thread r = key r)
-      const bool okd = ok && __all_sync(0xffffffffu, mbar_wait(&bars->dkv_full, ul & 1, abort_flag));
-      ok = named_barrier_and(1, kWg, okd);
-      if (!ok) break;
+    const uint32_t swr = smem_addr(w_smem), sdsr = smem_addr(ds_smem);
+    // query row (b, head h, position ri) of iteration `it` for this thread,
+    // nullptr-free: `valid` says whether it exists
+    struct RowAt {
+      int b, h;
+      bool valid;
+    };
+    auto row_of = [&](int it) -> RowAt {
+      const int ul = it / group, hl = it - ul * group;
+      const int u = static_cast<int>(blockIdx.x) + ul * G;
+      const int b = u / upb, hk0 = (u % upb) * P;
+      RowAt x;
+      x.b = b;
+      x.h = (hk0 + pr) * group + hl;  // pr == 0 when group > 1
+      x.valid = hk0 + pr < p.Hkv && ri < p.Lq;
+      return x;
+    };
+    auto prefetch_row = [&](int it) {
+      const RowAt x = row_of(it);
+      if (!x.valid) return;
+      const size_t ro = row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64);
+      prefetch_l2(static_cast<const uint16_t *>(a.out) + ro);
+      prefetch_l2(static_cast<const uint16_t *>(a.out) + ro + 63);
+      prefetch_l2(static_cast<const uint16_t *>(a.dout) + ro);
+      prefetch_l2(static_cast<const uint16_t *>(a.dout) + ro + 63);
+    };
+    // dQ of iteration `it` (thread r = row r) to global memory
+    auto store_dq = [&](int it) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag))) return false;
       tc_fence_after();
-      const size_t ko = r < p.Lk ? row_at(p.layout, b, hk, r, p.Hkv, p.Lk, 64) : 0;
+      const RowAt x = row_of(it);
+      uint16_t *dst = static_cast<uint16_t *>(a.dq) +
+                      (x.valid ? row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64) : 0);
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kSbDq + ch * 32, v);
+        tmem_wait_ld();
+        if (x.valid) store_row32(dst + ch * 32, v, a.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      return true;
+    };
+    // dV and dK of unit ul (thread r = key row r: pair r / R, key r % R)
+    auto store_dkv = [&](int ul) -> bool {
+      const bool okd = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_full, ul & 1, abort_flag));
+      if (!named_barrier_and(1, kWg, okd)) return false;
+      tc_fence_after();
+      const int u = static_cast<int>(blockIdx.x) + ul * G;
+      const int b = u / upb, hk = (u % upb) * P + pr;
+      const bool key = hk < p.Hkv && ri < p.Lk;
+      const size_t ko = key ? row_at(p.layout, b, hk, ri, p.Hkv, p.Lk, 64) : 0;
       uint16_t *dvr = static_cast<uint16_t *>(a.dv) + ko;
       uint16_t *dkr = static_cast<uint16_t *>(a.dk) + ko;
 #pragma unroll 1
@@ -1258,14 +1221,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kSbDv + ch * 32, v);
         tmem_wait_ld();
-        if (r < p.Lk) store_row32(dvr + ch * 32, v, 1.f);
+        if (key) store_row32(dvr + ch * 32, v, 1.f);
         tmem_ld32(tmem + lane_base + kSbDk + ch * 32, v);
         tmem_wait_ld();
-        if (r < p.Lk) store_row32(dkr + ch * 32, v, a.scale);
+        if (key) store_row32(dkr + ch * 32, v, a.scale);
       }
       tc_fence_before();
       mbar_arrive(&bars->dkv_free);
+      return true;
+    };
+
+    bool ok = true;
+    if (n_it > 0) prefetch_row(0);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int ul = it / group, hl = it - ul * group;
+      const RowAt x = row_of(it);
+      const int len = clamp_len(p, x.b);
+      // allowed tile columns [lo, hi): the row's own pair, keys j < jmax
+      const int lo = pr * R;
+      const int hi = lo + (x.valid ? row_limit(p, len, ri) : 0);
+      // D of the row (its lines were prefetched one iteration ahead)
+      float dd = 0.f;
+      if (x.valid) {
+        const size_t ro = row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64);
+        const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.out) + ro);
+        const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + ro);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 ov = o4[c], gv = g4[c];
+          const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            dd = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), dd);
+            dd = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u), dd);
+          }
+        }
+      }
+      if (it + 1 < n_it) prefetch_row(it + 1);
+      // ---- the row's softmax over its allowed keys, dS over dP
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sd_full, it & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
+      tmem_wait_ld();
+      const bool need_mask = __any_sync(0xffffffffu, lo > 0 || hi < kT);
+      const bool pos = p.scale_log2 > 0.f;
+      const float m = pos ? mask_max128(sr, need_mask, lo, hi) * p.scale_log2
+                          : scale_mask_max128(sr, p.scale_log2, need_mask, lo, hi);
+      const float l = pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
+                          : exp2_sum128(sr, m, m != -INFINITY);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // the previous head's dQ, and the previous unit's dV and dK
+      if (it >= 1 && !(ok = store_dq(it - 1))) break;
+      if (it >= 1 && hl == 0 && !(ok = store_dkv(ul - 1))) break;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pv[32], pw[16], pd[16];
+        tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
+        tmem_wait_ld();
+        if (ch == 3) {
+          // every read of S and dP is done: the next head's may go out
+          tc_fence_before();
+          mbar_arrive(&bars->sd_free);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float w0 = __uint_as_float(sr[ch][e]) * inv;
+          const float w1 = __uint_as_float(sr[ch][e + 1]) * inv;
+          pw[e >> 1] = pack_bf16x2(w0, w1);
+          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                                   w1 * (__uint_as_float(pv[e + 1]) - dd));
+        }
+        // the previous head's gradient products have read w and dS
+        if (ch == 0 && it >= 1 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(&bars->wd_free, (it - 1) & 1, abort_flag))))
+          break;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t off = wd_offset(r, ch * 4 + t);
+          st_shared_v4(swr + off, pw[4 * t], pw[4 * t + 1], pw[4 * t + 2], pw[4 * t + 3]);
+          st_shared_v4(sdsr + off, pd[4 * t], pd[4 * t + 1], pd[4 * t + 2], pd[4 * t + 3]);
+        }
+      }
+      if (!ok) break;
+      // generic-proxy stores, read by the tensor core (async proxy)
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->wd_full);
     }
+    if (ok && n_it > 0) ok = store_dq(n_it - 1) && store_dkv(n_local - 1);
   }
 
   if (*abort_flag && warp == 4 && lane == 0) {
@@ -1274,8 +1319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = qd_issued - 2; i < qd_issued; ++i)
       if (i >= 0) (void)wait_teardown(&bars->qd_full[i & 1], (i >> 1) & 1);
   }
-  if (*abort_flag && warp == 5 && lane == 0 && last_commit != nullptr)
-    (void)wait_teardown(last_commit, last_parity);
+  if (*abort_flag && warp == 5 && lane == 0 && mma_issued) {
+    // tcgen05 ops of one thread complete in order: one more commit covers
+    // every product issued before it
+    tc_commit(&bars->drain);
+    (void)wait_teardown(&bars->drain, 0);
+  }
   if (*abort_flag && threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
   tc_fence_before();
   __syncthreads();
@@ -1361,7 +1410,7 @@ cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs 
   if (p.dk == 128) return launch_bwd_tc_impl<128>(maps, p, a, stream, have_lse);
   if (p.Lq <= kT && p.Lk <= kT) {
     // one tile each way: the fused persistent kernel (no statistics pass)
-    const long long units = static_cast<long long>(p.B) * p.Hkv;
+    const long long units = static_cast<long long>(p.B) * ((p.Hkv + a.pack - 1) / a.pack);
     return launch_one(bwd_short_tc_kernel, kSbSmem, units < num_sms ? units : num_sms, maps, p,
                       a, stream);
   }

@@ -98,13 +98,17 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   float *lse, *dsum;
   float scale;  // dq and dk carry this factor
+  // d = 64 with query and key lengths <= 128: (batch, head) pairs packed per
+  // 128-row tile by the fused short kernel (its maps have box (64, 128 /
+  // pack, pack, 1)); 1 otherwise
+  int pack;
 };
 cudaError_t launch_bwd_simt(const BwdArgs &a, const Problem &p, bool bf16, cudaStream_t stream);
 // D = dout . out per query row into a.dsum (bf16 tensors), when the row
 // statistics lse come from the forward pass instead of a statistics pass
 cudaError_t launch_bwd_dsum(const BwdArgs &a, const Problem &p, cudaStream_t stream);
 // bf16, d in {64, 128}: maps q, k, v and (in the `o` slot) dout, box
-// (64, 128, 1, 1)
+// (64, 128, 1, 1), or (64, 128 / a.pack, a.pack, 1) for the fused short kernel
 cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs &a, int num_sms,
                           cudaStream_t stream, bool have_lse = false);
 

@@ -518,14 +518,24 @@ int bwd_impl(const void *q, const void *k, const void *v, const void *out, const
   a.lse = reinterpret_cast<float *>(ws);
   a.dsum = reinterpret_cast<float *>(ws + nws / 2);
   a.scale = scale;
+  a.pack = 1;
   if (dtype == MHA_DTYPE_BF16) {
-    // tensor cores (d in {64, 128}, enforced by select_path)
+    // tensor cores (d in {64, 128}, enforced by select_path).  The fused
+    // short kernel packs pack = 128 / R pairs (R: the longer length rounded
+    // up to a power of two) into one 128-row tile when the key/value heads
+    // are not shared
+    if (d_k == 64 && Lq <= 128 && Lk <= 128 && H_kv == H) {
+      const int R = next_pow2(std::max(std::max(Lq, Lk), 8));
+      a.pack = 128 / R;
+      while (a.pack > 1 && a.pack > H) a.pack >>= 1;
+    }
+    const int rows = 128 / a.pack;
     LongMaps m;
     std::memset(&m, 0, sizeof m);
-    const bool ok = make_map(&m.q, q, d_k, Lq, H, B, layout, 128, 1) &&
-                    make_map(&m.k, k, d_k, Lk, H_kv, B, layout, 128, 1) &&
-                    make_map(&m.v, v, d_v, Lk, H_kv, B, layout, 128, 1) &&
-                    make_map(&m.o, dout, d_v, Lq, H, B, layout, 128, 1);
+    const bool ok = make_map(&m.q, q, d_k, Lq, H, B, layout, rows, a.pack) &&
+                    make_map(&m.k, k, d_k, Lk, H_kv, B, layout, rows, a.pack) &&
+                    make_map(&m.v, v, d_v, Lk, H_kv, B, layout, rows, a.pack) &&
+                    make_map(&m.o, dout, d_v, Lq, H, B, layout, rows, a.pack);
     if (!ok) return MHA_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return MHA_ERR_CUDA;
