@@ -971,9 +971,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 // S and dP of head n + 1 go out as soon as the softmax has read those of head
 // n, so the products of one head overlap the softmax of the next; the softmax
 // stores dQ of head n (and dV, dK of a finished unit) after the exponentials
-// of head n + 1.  K and V of the next unit and Q and dout of the next head
-// load while the current one computes.  TMEM: S | dP | dQ | dV | dK (448
-// columns).
+// of head n + 1, staged per warp so that each store instruction writes whole
+// 64-byte row pieces.  D = dout . out comes from shared memory: dout from the
+// head's TMA tile, out from rows each thread copies (cp.async) one head ahead
+// -- a global load at the point of use stalled the softmax for microseconds.
+// K and V of the next unit and Q and dout of the next head load while the
+// current one computes.  TMEM: S | dP | dQ | dV | dK (448 columns).
 struct ShortBwdBars {
   uint64_t kv_full[2], kv_empty[2];  // K, V of a unit (by unit parity)
   uint64_t qd_full[2], qd_empty[2];  // Q, dout of a head (by iteration parity)
@@ -990,14 +993,33 @@ struct ShortBwdBars {
   int abort_flag;
 };
 constexpr int kSbTile = 128 * 128;  // one [128 x 64] bf16 tile
-// K, V (two units), Q, dout (two heads), w and dS (two 64-key slabs each)
-constexpr size_t kSbSmem = 1024 + 12 * static_cast<size_t>(kSbTile) + 512;
+constexpr int kSbStage = 32 * 64;  // one softmax warp's 32 half-rows of output
+// K, V (two units), Q, dout (two heads), w and dS (two 64-key slabs each),
+// the rows of out, the softmax warps' output staging
+constexpr size_t kSbSmem = 1024 + 13 * static_cast<size_t>(kSbTile) + 4 * kSbStage + 512;
 constexpr uint32_t kSbS = 0, kSbDp = 128, kSbDq = 256, kSbDv = 320, kSbDk = 384;
 
 // byte offset of 16-byte piece c (0..15: keys 8c .. 8c + 7) of row r in a
 // [128 x 128] bf16 tile stored as two 128-byte-swizzled 64-key slabs
 __device__ __forceinline__ uint32_t wd_offset(uint32_t r, uint32_t c) {
   return (c >> 3) * kSbTile + r * 128u + (((c & 7u) ^ (r & 7u)) << 4);
+}
+// byte offset of 16-byte piece c (0..3) of 64-byte half-row `row` (0..31) in
+// a warp's staging buffer, swizzled so that the eight lanes of one shared
+// memory wavefront never share a bank group, writing or reading
+__device__ __forceinline__ uint32_t stage64(uint32_t row, uint32_t c) {
+  return row * 64u + ((c ^ ((row >> 1) & 3u)) << 4);
+}
+// sum over 8 bf16 pairs of a[e] * b[e] (fp32)
+__device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    s = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), s);
+    s = fmaf(__uint_as_float(aw[t] & 0xffff0000u), __uint_as_float(bw[t] & 0xffff0000u), s);
+  }
+  return s;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1009,7 +1031,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *qd_smem = kv_smem + 4 * kSbTile;  // 2 x (Q, dout)
   uint8_t *w_smem = qd_smem + 4 * kSbTile;   // w: two slabs
   uint8_t *ds_smem = w_smem + 2 * kSbTile;   // dS: two slabs
-  ShortBwdBars *bars = reinterpret_cast<ShortBwdBars *>(ds_smem + 2 * kSbTile);
+  uint8_t *out_smem = ds_smem + 2 * kSbTile;    // thread r: row r of out
+  uint8_t *stage_smem = out_smem + kSbTile;     // 4 x 2 KiB output staging
+  ShortBwdBars *bars = reinterpret_cast<ShortBwdBars *>(stage_smem + 4 * kSbStage);
   volatile int *abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1162,45 +1186,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pr = r / R, ri = r - pr * R;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t swr = smem_addr(w_smem), sdsr = smem_addr(ds_smem);
-    // query row (b, head h, position ri) of iteration `it` for this thread,
-    // nullptr-free: `valid` says whether it exists
+    // query row (b, head h, position i) of tile row `row` at iteration `it`;
+    // `valid` says whether it exists
     struct RowAt {
-      int b, h;
+      int b, h, i;
       bool valid;
     };
-    auto row_of = [&](int it) -> RowAt {
-      const int ul = it / group, hl = it - ul * group;
+    // (batch, first key/value head, head within the group) of an iteration
+    struct Iter {
+      int b, hk0, hl;
+    };
+    auto iter_of = [&](int it) -> Iter {
+      const int ul = it / group;
       const int u = static_cast<int>(blockIdx.x) + ul * G;
-      const int b = u / upb, hk0 = (u % upb) * P;
+      Iter t;
+      t.b = u / upb;
+      t.hk0 = (u - t.b * upb) * P;
+      t.hl = it - ul * group;
+      return t;
+    };
+    const int r_shift = __ffs(R) - 1;  // R is a power of two
+    auto row_of = [&](const Iter &t, int row) -> RowAt {
+      const int pp = row >> r_shift;
       RowAt x;
-      x.b = b;
-      x.h = (hk0 + pr) * group + hl;  // pr == 0 when group > 1
-      x.valid = hk0 + pr < p.Hkv && ri < p.Lq;
+      x.b = t.b;
+      x.i = row & (R - 1);
+      x.h = (t.hk0 + pp) * group + t.hl;  // pp == 0 when group > 1
+      x.valid = t.hk0 + pp < p.Hkv && x.i < p.Lq;
       return x;
     };
-    auto prefetch_row = [&](int it) {
-      const RowAt x = row_of(it);
+    // this thread's row of out for iteration `it` -> its shared-memory row
+    // (cp.async, in flight for a whole iteration: thread r alone touches
+    // row r, so no other thread waits for it)
+    const uint32_t orow = smem_addr(out_smem) + r * 128;
+    auto fetch_out = [&](int it) {
+      const RowAt x = row_of(iter_of(it), r);
       if (!x.valid) return;
-      const size_t ro = row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64);
-      prefetch_l2(static_cast<const uint16_t *>(a.out) + ro);
-      prefetch_l2(static_cast<const uint16_t *>(a.out) + ro + 63);
-      prefetch_l2(static_cast<const uint16_t *>(a.dout) + ro);
-      prefetch_l2(static_cast<const uint16_t *>(a.dout) + ro + 63);
+      const uint16_t *src = static_cast<const uint16_t *>(a.out) +
+                            row_at(p.layout, x.b, x.h, x.i, p.H, p.Lq, 64);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) cp_async16(orow + ((c ^ (r & 7)) << 4), src + 8 * c);
+      cp_async_commit();
+    };
+    const uint32_t so = smem_addr(stage_smem + warp * kSbStage);
+    // 32 TMEM columns of this thread's row (fp32) * f -> bf16 -> the warp's
+    // staging; then the warp writes its 32 half-rows, eight 64-byte pieces per
+    // store instruction.  dst(rr) is the global address of warp row rr's
+    // half-row (nullptr: not stored).
+    auto store_half = [&](uint32_t taddr, float f, auto dst) {
+      uint32_t v[32];
+      tmem_ld32(taddr, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        st_shared_v4(so + stage64(lane, c4),
+                     pack_bf16x2(__uint_as_float(v[8 * c4 + 0]) * f, __uint_as_float(v[8 * c4 + 1]) * f),
+                     pack_bf16x2(__uint_as_float(v[8 * c4 + 2]) * f, __uint_as_float(v[8 * c4 + 3]) * f),
+                     pack_bf16x2(__uint_as_float(v[8 * c4 + 4]) * f, __uint_as_float(v[8 * c4 + 5]) * f),
+                     pack_bf16x2(__uint_as_float(v[8 * c4 + 6]) * f, __uint_as_float(v[8 * c4 + 7]) * f));
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int rr = 8 * t + (lane >> 2);
+        const uint4 val = ld_shared_v4(so + stage64(rr, lane & 3));
+        uint16_t *g = dst(rr);
+        if (g != nullptr) st_global_v4(g + (lane & 3) * 8, val);
+      }
+      __syncwarp();
     };
     // dQ of iteration `it` (thread r = row r) to global memory
     auto store_dq = [&](int it) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag))) return false;
       tc_fence_after();
-      const RowAt x = row_of(it);
-      uint16_t *dst = static_cast<uint16_t *>(a.dq) +
-                      (x.valid ? row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64) : 0);
+      const Iter itr = iter_of(it);
 #pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kSbDq + ch * 32, v);
-        tmem_wait_ld();
-        if (x.valid) store_row32(dst + ch * 32, v, a.scale);
-      }
+      for (int ch = 0; ch < 2; ++ch)
+        store_half(tmem + lane_base + kSbDq + ch * 32, a.scale, [&](int rr) -> uint16_t * {
+          const RowAt x = row_of(itr, warp * 32 + rr);
+          return x.valid ? static_cast<uint16_t *>(a.dq) +
+                               row_at(p.layout, x.b, x.h, x.i, p.H, p.Lq, 64) + ch * 32
+                         : nullptr;
+        });
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
       return true;
@@ -1211,53 +1277,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!named_barrier_and(1, kWg, okd)) return false;
       tc_fence_after();
       const int u = static_cast<int>(blockIdx.x) + ul * G;
-      const int b = u / upb, hk = (u % upb) * P + pr;
-      const bool key = hk < p.Hkv && ri < p.Lk;
-      const size_t ko = key ? row_at(p.layout, b, hk, ri, p.Hkv, p.Lk, 64) : 0;
-      uint16_t *dvr = static_cast<uint16_t *>(a.dv) + ko;
-      uint16_t *dkr = static_cast<uint16_t *>(a.dk) + ko;
+      const int b = u / upb, hk0 = (u % upb) * P;
+      // element offset of key row rr of this warp (or -1)
+      auto key_at = [&](int rr) -> long long {
+        const int row = warp * 32 + rr, pp = row >> r_shift, j = row & (R - 1);
+        return hk0 + pp < p.Hkv && j < p.Lk
+                   ? static_cast<long long>(row_at(p.layout, b, hk0 + pp, j, p.Hkv, p.Lk, 64))
+                   : -1LL;
+      };
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kSbDv + ch * 32, v);
-        tmem_wait_ld();
-        if (key) store_row32(dvr + ch * 32, v, 1.f);
-        tmem_ld32(tmem + lane_base + kSbDk + ch * 32, v);
-        tmem_wait_ld();
-        if (key) store_row32(dkr + ch * 32, v, a.scale);
+        store_half(tmem + lane_base + kSbDv + ch * 32, 1.f, [&](int rr) -> uint16_t * {
+          const long long o = key_at(rr);
+          return o >= 0 ? static_cast<uint16_t *>(a.dv) + o + ch * 32 : nullptr;
+        });
+        store_half(tmem + lane_base + kSbDk + ch * 32, a.scale, [&](int rr) -> uint16_t * {
+          const long long o = key_at(rr);
+          return o >= 0 ? static_cast<uint16_t *>(a.dk) + o + ch * 32 : nullptr;
+        });
       }
       tc_fence_before();
       mbar_arrive(&bars->dkv_free);
       return true;
     };
+    // D = dout . out of this thread's row: out from its cp.async row, dout
+    // from the TMA tile of the iteration's stage (same 128-byte swizzle)
+    auto row_dsum = [&](int it, bool valid) -> float {
+      cp_async_wait_all();
+      if (!valid) return 0.f;
+      const uint32_t drow = smem_addr(qd_smem + 2 * (it & 1) * kSbTile + kSbTile) + r * 128;
+      float dd = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t off = (c ^ (r & 7)) << 4;
+        dd += dot_bf16x8(ld_shared_v4(orow + off), ld_shared_v4(drow + off));
+      }
+      return dd;
+    };
 
     bool ok = true;
-    if (n_it > 0) prefetch_row(0);
+    if (n_it > 0) fetch_out(0);
     for (int it = 0; ok && it < n_it; ++it) {
       const int ul = it / group, hl = it - ul * group;
-      const RowAt x = row_of(it);
+      const Iter itr = iter_of(it);
+      const RowAt x = row_of(itr, r);
       const int len = clamp_len(p, x.b);
       // allowed tile columns [lo, hi): the row's own pair, keys j < jmax
       const int lo = pr * R;
       const int hi = lo + (x.valid ? row_limit(p, len, ri) : 0);
-      // D of the row (its lines were prefetched one iteration ahead)
-      float dd = 0.f;
-      if (x.valid) {
-        const size_t ro = row_at(p.layout, x.b, x.h, ri, p.H, p.Lq, 64);
-        const uint4 *o4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.out) + ro);
-        const uint4 *g4 = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.dout) + ro);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 ov = o4[c], gv = g4[c];
-          const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            dd = fmaf(__uint_as_float(ow[t] << 16), __uint_as_float(gw[t] << 16), dd);
-            dd = fmaf(__uint_as_float(ow[t] & 0xffff0000u), __uint_as_float(gw[t] & 0xffff0000u), dd);
-          }
-        }
-      }
-      if (it + 1 < n_it) prefetch_row(it + 1);
+      // D of the row: dout's tile has landed (its phase cannot move on before
+      // this head's gradients are issued), out's row came by cp.async
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->qd_full[it & 1], (it >> 1) & 1, abort_flag))))
+        break;
+      const float dd = row_dsum(it, x.valid);
+      if (it + 1 < n_it) fetch_out(it + 1);
       // ---- the row's softmax over its allowed keys, dS over dP
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->sd_full, it & 1, abort_flag));
       if (!ok) break;

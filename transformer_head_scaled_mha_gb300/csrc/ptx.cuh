@@ -740,6 +740,18 @@ __device__ __forceinline__ void st_global_v4(void *ptr, uint4 v) {
                : "memory");
 }
 
+// 16 bytes global -> shared without registers (cp.async, L2 only); complete
+// after cp_async_commit and cp_async_wait_all in the issuing thread
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte
 // swizzled tile (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B)
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
