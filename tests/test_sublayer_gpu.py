@@ -40,7 +40,8 @@ def _linear_case(M, K, N, seed, bias=True):
 
 @pytest.mark.parametrize("M,K,N", [(1000, 512, 512), (128, 64, 64), (300, 256, 72),
                                    (5, 1024, 1536), (129, 200, 136), (1, 8, 8),
-                                   (16384, 512, 512)])
+                                   (16384, 512, 512), (777, 192, 320), (2000, 448, 64),
+                                   (3000, 512, 1536)])
 def test_linear_parity(M, K, N):
     import transformer_head_scaled_mha_gb300 as mha
     x, w, b = _linear_case(M, K, N, seed=M + K + N)

@@ -116,14 +116,24 @@ cudaError_t launch_zero_fill(void *out, size_t bytes, cudaStream_t stream);
 // dst[0, n) = value
 cudaError_t launch_fill_f32(float *dst, size_t n, float value, cudaStream_t stream);
 
-// y = x W + b (bf16), 128-byte swizzle.  Slab tiling (K, N multiples of 64):
+// y_g = x_g W_g + b_g (bf16) for up to kMaxLinear products with the same K in
+// one launch, 128-byte swizzle.  Slab tiling (K and every N multiples of 64):
 // x viewed as (64, M, K/64) box (64, 128, 2), W as (64, K, N/64) box
 // (64, 128, 2); otherwise x as (K, M) box (64, 128), W as (N, K) box (64, 64).
+constexpr int kMaxLinear = 3;
 struct LinearMaps {
-  CUtensorMap x;
-  CUtensorMap w;
+  CUtensorMap x[kMaxLinear];
+  CUtensorMap w[kMaxLinear];
 };
-cudaError_t launch_linear_tc(const LinearMaps &maps, const void *bias, void *y, int M, int N,
+struct LinearProblem {
+  const void *bias;  // [N] or nullptr
+  void *y;           // [M, N]
+  int M, N;
+};
+cudaError_t launch_linear_tc(const LinearMaps &maps, const LinearProblem *probs, int count,
                              int K, bool slabs, int *status, int num_sms, cudaStream_t stream);
+// Slab tiling with every N >= 256: 128 x 256 tiles, stages of 64 of K; x's
+// map then has box (64, 128, 1) and W's box (64, 64, 4)
+bool linear_wide(int K, bool slabs, int min_n);
 
 }  // namespace mha

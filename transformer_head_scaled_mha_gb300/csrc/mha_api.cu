@@ -192,14 +192,16 @@ bool make_map_2d(CUtensorMap *map, const void *base, int cols, int rows, int box
 
 // 3-D view (64, rows, cols / 64) of a row-major bf16 matrix whose column
 // count is a multiple of 64: 64-wide column slabs, 128-byte swizzle; box
-// (64, box_rows, 2) -- two slabs per copy
-bool make_map_slabs(CUtensorMap *map, const void *base, int cols, int rows, int box_rows) {
+// (64, box_rows, box_slabs)
+bool make_map_slabs(CUtensorMap *map, const void *base, int cols, int rows, int box_rows,
+                    int box_slabs = 2) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(cols / 64)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 2u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(box_slabs)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -592,23 +594,47 @@ int check_linear(const void *x, const void *w, const void *b, const void *y, lon
   return MHA_OK;
 }
 
-// Launch of a validated linear layer (M > 0).
-int run_linear(const void *x, const void *w, const void *b, void *y, int M, int K, int N,
-               cudaStream_t stream) {
+// One validated product y = x W + b of a launch (M > 0).
+struct LinearJob {
+  const void *x, *w, *b;
+  void *y;
+  int M, N;
+};
+
+// One launch for up to kMaxLinear validated products with the same K.
+int run_linears(const LinearJob *jobs, int count, int K, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_CUDA;
   const int sms = sm_count(dev);
   int *status = status_ptr();
   if (sms <= 0 || status == nullptr) return MHA_ERR_CUDA;
+  bool slabs = K % 64 == 0;
+  for (int g = 0; g < count; ++g) slabs = slabs && jobs[g].N % 64 == 0;
+  int min_n = jobs[0].N;
+  for (int g = 1; g < count; ++g) min_n = std::min(min_n, jobs[g].N);
+  const bool wide = linear_wide(K, slabs, min_n);
   LinearMaps m;
   std::memset(&m, 0, sizeof m);
-  const bool slabs = K % 64 == 0 && N % 64 == 0;
-  const bool ok = slabs ? make_map_slabs(&m.x, x, K, M, 128) && make_map_slabs(&m.w, w, N, K, 128)
-                        : make_map_2d(&m.x, x, K, M, 64, 128) && make_map_2d(&m.w, w, N, K, 64, 64);
-  if (!ok) return MHA_ERR_CUDA;
-  return launch_linear_tc(m, b, y, M, N, K, slabs, status, sms, stream) == cudaSuccess
+  LinearProblem probs[kMaxLinear];
+  for (int g = 0; g < count; ++g) {
+    const LinearJob &j = jobs[g];
+    const bool ok = slabs ? make_map_slabs(&m.x[g], j.x, K, j.M, 128, wide ? 1 : 2) &&
+                                make_map_slabs(&m.w[g], j.w, j.N, K, wide ? 64 : 128,
+                                               wide ? 4 : 2)
+                          : make_map_2d(&m.x[g], j.x, K, j.M, 64, 128) &&
+                                make_map_2d(&m.w[g], j.w, j.N, K, 64, 64);
+    if (!ok) return MHA_ERR_CUDA;
+    probs[g] = LinearProblem{j.b, j.y, j.M, j.N};
+  }
+  return launch_linear_tc(m, probs, count, K, slabs, status, sms, stream) == cudaSuccess
              ? MHA_OK
              : MHA_ERR_CUDA;
+}
+
+int run_linear(const void *x, const void *w, const void *b, void *y, int M, int K, int N,
+               cudaStream_t stream) {
+  const LinearJob j{x, w, b, y, M, N};
+  return run_linears(&j, 1, K, stream);
 }
 
 constexpr size_t kWsAlign = 256;
@@ -694,16 +720,13 @@ extern "C" int mha_sublayer_fwd(const void *x, const void *mem, void *out, const
                   overlaps(out, n_out, key_lengths, sizeof(int32_t) * B))))
     return MHA_ERR_INVALID_ARGUMENT;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  // 1. projections (head i of each is columns [i d, (i + 1) d): [B, L, heads, d])
-  if ((st = run_linear(x, w_q, b_q, q, static_cast<int>(Mq), d_model, static_cast<int>(nq), stream)) != MHA_OK)
-    return st;
-  if (Mk > 0) {
-    if ((st = run_linear(mem, w_k, b_k, k, static_cast<int>(Mk), d_model, static_cast<int>(nk), stream)) !=
-            MHA_OK ||
-        (st = run_linear(mem, w_v, b_v, v, static_cast<int>(Mk), d_model, static_cast<int>(nv), stream)) !=
-            MHA_OK)
-      return st;
-  }
+  // 1. the three projections in one launch (head i of each is columns
+  //    [i d, (i + 1) d): [B, L, heads, d])
+  const LinearJob proj[3] = {
+      {x, w_q, b_q, q, static_cast<int>(Mq), static_cast<int>(nq)},
+      {mem, w_k, b_k, k, static_cast<int>(Mk), static_cast<int>(nk)},
+      {mem, w_v, b_v, v, static_cast<int>(Mk), static_cast<int>(nv)}};
+  if ((st = run_linears(proj, Mk > 0 ? 3 : 1, d_model, stream)) != MHA_OK) return st;
   // 2. attention per head, in the [B, L, heads, d] layout
   if ((st = mha_fwd_ex(q, k, v, heads, B, H, H_kv, T, S, d_k, d_v, kLayoutBSHD, mask_kind,
                        key_lengths, scale, dtype, stream)) != MHA_OK)
