@@ -157,6 +157,13 @@ def kernel_source_digest(kernel=None):
     return h.hexdigest()[:16]
 
 
+def linear_kernel_name(K, N):
+    """The projection kernel mha_linear_fwd runs for x [M, K] W [K, N]: 128 x 256
+    tiles when K and N are multiples of 64 and N >= 256, else 128 x 128."""
+    return "linear_wide_kernel" if K % 64 == 0 and N % 64 == 0 and N >= 256 else \
+        "linear_tc_kernel"
+
+
 def recorded_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -816,8 +823,8 @@ def run_sublayer(args):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "traffic": recorded_traffic(args.workload + ":linear"),
-                "kernel": "linear_tc_kernel (query projection %dx%dx%d, timed alone)" % (
-                    B * T, d, H * dk),
+                "kernel": "%s (query projection %dx%dx%d, timed alone)" % (
+                    linear_kernel_name(d, H * dk), B * T, d, H * dk),
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback", "algorithmic_flops": lin_flops,
                 "sublayer_share": {"projections_flops": proj_flops, "attention_flops": att_flops}}
