@@ -50,6 +50,22 @@ constexpr int kWg = 128;   // softmax threads
 constexpr int kT = 128;    // rows of every tile (queries or keys)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kMaxSlots = 8;
+constexpr int kBand = 8;  // tiles per band of the CTA order
+
+// CTA order of the per-tile kernels: bands of kBand tiles, heaviest band
+// first; inside a band, a head's tiles side by side.  The CTAs running at one
+// time then cover few heads, and those that read a head's other operand tiles
+// read the same ones at about the same time, mostly from L2.  Tile i of `n`
+// (0 = heaviest) and head index of CTA x over `heads` heads.
+__device__ __forceinline__ void band_order(int x, int heads, int n, int &head, int &i) {
+  const int full = n / kBand;  // full bands; a partial one (the lightest) ends the order
+  const int t = min(x / (heads * kBand), full);
+  const int lo = t * kBand;
+  const int size = min(kBand, n - lo);
+  const int local = x - t * heads * kBand;
+  head = local / size;
+  i = lo + local % size;
+}
 
 template <int D>
 struct Geo {
@@ -164,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqb = (p.Lq + kT - 1) / kT;
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int q0 = (nqb - 1 - static_cast<int>(blockIdx.x / BH)) * kT;  // heaviest (causal) first
+  int bh, qi;
+  band_order(static_cast<int>(blockIdx.x), BH, nqb, bh, qi);
+  const int q0 = (nqb - 1 - qi) * kT;  // heaviest (causal) first
   const int b = bh / p.H, h = bh % p.H, hk = h / (p.H / p.Hkv);
   const int len = clamp_len(p, b);
   const int nt = key_tiles(p, len, q0);
@@ -371,8 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqb = (p.Lq + kT - 1) / kT;
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int qt = nqb - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest (causal) first
+  int bh, qi;
+  band_order(static_cast<int>(blockIdx.x), BH, nqb, bh, qi);
+  const int qt = nqb - 1 - qi;  // heaviest (causal) first
   const int q0 = qt * kT;
   const int b = bh / p.H, h = bh % p.H, hk = h / (p.H / p.Hkv);
   const int len = clamp_len(p, b);
@@ -686,8 +704,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BK = p.B * p.Hkv;
-  const int bk = static_cast<int>(blockIdx.x % BK);
-  const int k0 = static_cast<int>(blockIdx.x / BK) * kT;
+  const int nkb = (p.Lk + kT - 1) / kT;
+  int bk, kt;
+  band_order(static_cast<int>(blockIdx.x), BK, nkb, bk, kt);  // heaviest (causal) first
+  const int k0 = kt * kT;
   const int b = bk / p.Hkv, hk = bk % p.Hkv;
   const int group = p.H / p.Hkv;
   const int len = clamp_len(p, b);
