@@ -372,20 +372,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       float alpha = 1.f;
       if (pos && !need_mask && __all_sync(0xffffffffu, m_use != -INFINITY)) {
         // Unmasked tile, every row of the warp has a running max: 32-column
-        // chunks, exponents against the running max, the next chunk's TMEM
-        // load in flight while this one is computed.  A chunk whose max
+        // chunks, exponents against the running max; all four chunks' TMEM
+        // loads go out at once (one wait instead of one per chunk).  A chunk whose max
         // exceeds the running max by more than 2^8 moves it first (and
         // rescales the P of the chunks already stored).  P of chunk ch goes
         // to columns [16 ch, 16 ch + 16), whose scores are already read.
-        uint32_t va[32], vb[32];
-        tmem_ld32(s_tmem, va);
+        uint32_t vall[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, vall[ch]);
         tmem_wait_ld();
         float tsum = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          uint32_t(&cur)[32] = (ch & 1) ? vb : va;
-          uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
-          if (ch < 3) tmem_ld32(s_tmem + (ch + 1) * 32, nxt);
+          uint32_t(&cur)[32] = vall[ch];
           const float cm = chunk_max32(cur) * p.scale_log2;
           const bool climb = cm > m_use + kRescaleThreshold;
           if (__any_sync(0xffffffffu, climb)) {
@@ -399,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
           tsum += chunk_exp_pack32(cur, p.scale_log2, m_use, pk);
           tmem_st16(s_tmem + ch * 16, pk);
-          if (ch < 3) tmem_wait_ld();
         }
         l_run = l_run * alpha + tsum;
       } else {
