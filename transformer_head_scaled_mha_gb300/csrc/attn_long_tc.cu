@@ -373,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pos && !need_mask && __all_sync(0xffffffffu, m_use != -INFINITY)) {
         // Unmasked tile, every row of the warp has a running max: 32-column
         // chunks, exponents against the running max; all four chunks' TMEM
-        // loads go out at once (one wait instead of one per chunk).  A chunk whose max
-        // exceeds the running max by more than 2^8 moves it first (and
-        // rescales the P of the chunks already stored).  P of chunk ch goes
-        // to columns [16 ch, 16 ch + 16), whose scores are already read.
+        // loads go out at once (one wait instead of one per chunk).  A chunk
+        // whose max exceeds the running max by more than 2^8 moves it first
+        // (and rescales the P of the chunks already stored).  P of chunk ch
+        // goes to columns [16 ch, 16 ch + 16), whose scores are already read.
         uint32_t vall[4][32];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_tmem + ch * 32, vall[ch]);
