@@ -520,24 +520,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t s_t = tmem + lane_base + C::kS + (j & 1) * kT;
       const uint32_t dp_t = tmem + lane_base + C::kDp;
-      // chunk ch + 1 loads from TMEM while chunk ch computes; the packed dS of
-      // chunk ch lands on S columns already in registers that no load in
-      // flight reads
+      // two chunks of S and dP load from TMEM at once (one wait per pair);
+      // the packed dS of chunks 0, 1 lands on S columns [0, 32), which the
+      // loads of chunks 2, 3 do not read
       uint32_t sv[2][32], pv[2][32];
-      tmem_ld32(s_t, sv[0]);
-      tmem_ld32(dp_t, pv[0]);
-      tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if (ch < 3) {
-          tmem_ld32(s_t + (ch + 1) * 32, sv[(ch + 1) & 1]);
-          tmem_ld32(dp_t + (ch + 1) * 32, pv[(ch + 1) & 1]);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        tmem_ld32(s_t + (2 * c2) * 32, sv[0]);
+        tmem_ld32(s_t + (2 * c2 + 1) * 32, sv[1]);
+        tmem_ld32(dp_t + (2 * c2) * 32, pv[0]);
+        tmem_ld32(dp_t + (2 * c2 + 1) * 32, pv[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int ch = 2 * c2 + cc;
+          uint32_t pk[16];
+          const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
+          dq_chunk(sv[cc], pv[cc], lim, p.scale_log2, lse, dd, pk);
+          tmem_st16(s_t + ch * 16, pk);
         }
-        uint32_t pk[16];
-        const int lim = jmax - (j * kT + ch * 32);  // columns c < lim are allowed
-        dq_chunk(sv[ch & 1], pv[ch & 1], lim, p.scale_log2, lse, dd, pk);
-        tmem_st16(s_t + ch * 16, pk);
-        if (ch < 3) tmem_wait_ld();
       }
       tmem_wait_st();
       tc_fence_before();
@@ -889,22 +890,20 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const uint32_t dp_t = tmem + lane_base + C::kDp + 64 * h;
         const float *sth = st + h * 64;
         const int c0 = q0 + h * 64;  // first query of the half
-        // w^T while dP^T_h is still being computed: the second 32 columns
-        // load from TMEM while the first compute, and the packed w of the
-        // first land on columns the load in flight does not read
+        // w^T while dP^T_h is still being computed: both 32-column chunks
+        // load from TMEM at once (one wait)
         float wv[2][32];
         {
           uint32_t sv[2][32];
           tmem_ld32(s_t, sv[0]);
-          tmem_wait_ld();
           tmem_ld32(s_t + 32, sv[1]);
+          tmem_wait_ld();
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t pw[16];
             dkdv_w32(sv[ch], sth + ch * 32, i_min - (c0 + ch * 32), i_max - (c0 + ch * 32),
                      p.scale_log2, wv[ch], pw);
             tmem_st16(s_t + ch * 16, pw);
-            if (ch == 0) tmem_wait_ld();
           }
         }
         tmem_wait_st();
@@ -917,14 +916,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         {
           uint32_t pv[2][32];
           tmem_ld32(dp_t, pv[0]);
-          tmem_wait_ld();
           tmem_ld32(dp_t + 32, pv[1]);
+          tmem_wait_ld();
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t pd[16];
             dkdv_ds32(wv[ch], pv[ch], sth + ch * 32, pd);
             tmem_st16(dp_t + ch * 16, pd);
-            if (ch == 0) tmem_wait_ld();
           }
         }
         tmem_wait_st();
