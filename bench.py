@@ -871,14 +871,16 @@ def run_sublayer(args):
                        "len_range": spec["len_range"], "cross": spec["cross"],
                        "l2": "inputs rotate over %d device copies (%.0f MB > 3x L2 %.0f MB)"
                              % (n_sets, n_sets * set_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graph of %d calls (5 launches each), CUDA events "
-                                 "recorded as the graph's first and last nodes" % args.steps,
+                       "timing": "CUDA graph of %d calls (3 launches each: the three "
+                                 "projections, the attention, the output projection), CUDA "
+                                 "events recorded as the graph's first and last nodes"
+                                 % args.steps,
                        "parallelism": "weak: same workload per rank, no collective"
                        if world > 1 else "1 GPU"},
             "e2e": {"value": round(flops / e2e_t / 1e12 * world, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "note": "weights resident on the device", "pipeline": E2E_PIPELINE},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "clocks": clocks,
