@@ -5,6 +5,7 @@ This file is collected last so that it also runs after every other GPU test;
 it must pass alone as well.  Two calls in a row through each entry point give
 the same bits, whatever the static scratch held before.
 """
+import gc
 import math
 
 import numpy as np
@@ -89,13 +90,20 @@ def test_static_entry_point_allocates_no_device_memory():
     assert call() == mha.MHA_OK
     torch.cuda.synchronize()
     first = from_device(out)
-    before = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
-              torch.cuda.memory_reserved())
-    for _ in range(2):
-        assert call() == mha.MHA_OK
-    torch.cuda.synchronize()
-    after = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
-             torch.cuda.memory_reserved())
+    # tensors left by earlier tests must not be freed in between (that would
+    # move the caching allocator's counters without any call of ours)
+    gc.collect()
+    gc.disable()
+    try:
+        before = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
+                  torch.cuda.memory_reserved())
+        for _ in range(2):
+            assert call() == mha.MHA_OK
+        torch.cuda.synchronize()
+        after = (torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated(),
+                 torch.cuda.memory_reserved())
+    finally:
+        gc.enable()
     assert after == before
     np.testing.assert_array_equal(from_device(out), first)
     assert mha.mha_debug_status() == mha.MHA_OK
