@@ -75,23 +75,23 @@ struct LinearArgs {
   uint16_t *y[kMaxLinear];
   int M[kMaxLinear], N[kMaxLinear];
   int tiles_n[kMaxLinear];    // N tiles of product g
-  int tiles_m[kMaxLinear];    // M tiles of product g
   int tiles_end[kMaxLinear];  // one past product g's last tile
   int count, K;
   int *status;
 };
 
-// product, M offset and N offset of tile t
+// product, M offset and N offset of tile t (tiles bn columns wide)
 struct TileAt {
   int g, m0, n0;
 };
+template <int bn = kBN>
 __device__ __forceinline__ TileAt tile_at(const LinearArgs &a, int t) {
   TileAt x;
   x.g = t < a.tiles_end[0] ? 0 : (t < a.tiles_end[1] ? 1 : 2);
   const int lt = t - (x.g > 0 ? a.tiles_end[x.g - 1] : 0);
   const int tn = a.tiles_n[x.g];
   x.m0 = (lt / tn) * kBM;
-  x.n0 = (lt - (lt / tn) * tn) * kBN;
+  x.n0 = (lt - (lt / tn) * tn) * bn;
   return x;
 }
 
@@ -321,16 +321,6 @@ struct __align__(8) WideBarriers {
 constexpr size_t kWSmem = 1024 + kWStages * (kWA + kWB) + kEpiWarps * kStagingBytes +
                           kEpiWarps * kWN * 4 + sizeof(WideBarriers);
 
-// product, M offset and N offset of wide tile t (n-tile-major within an M block)
-__device__ __forceinline__ TileAt wide_tile_at(const LinearArgs &a, int t) {
-  TileAt x;
-  x.g = t < a.tiles_end[0] ? 0 : (t < a.tiles_end[1] ? 1 : 2);
-  const int lt = t - (x.g > 0 ? a.tiles_end[x.g - 1] : 0);
-  const int tn = a.tiles_n[x.g];
-  x.m0 = (lt / tn) * kBM;
-  x.n0 = (lt - (lt / tn) * tn) * kWN;
-  return x;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     linear_wide_kernel(const __grid_constant__ LinearMaps maps,
@@ -385,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const TileAt at = wide_tile_at(args, t);
+        const TileAt at = tile_at<kWN>(args, t);
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int s = it % kWStages;
           if (!(ok = mbar_wait_spin(&bars->empty[s], ((it / kWStages) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
@@ -434,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tl = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tl) {
       const int a = tl & 1;
-      const TileAt at = wide_tile_at(args, t);
+      const TileAt at = tile_at<kWN>(args, t);
       bool ok = true;
       for (int hh = 0; ok && hh < 2; ++hh) {
         TileAt half = at;
@@ -489,7 +479,6 @@ cudaError_t launch_linear_tc(const LinearMaps &maps, const LinearProblem *probs,
     a.M[g] = probs[g].M;
     a.N[g] = probs[g].N;
     a.tiles_n[g] = (probs[g].N + (wide ? kWN : kBN) - 1) / (wide ? kWN : kBN);
-    a.tiles_m[g] = (probs[g].M + kBM - 1) / kBM;
     tiles += static_cast<long long>((probs[g].M + kBM - 1) / kBM) * a.tiles_n[g];
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     a.tiles_end[g] = static_cast<int>(tiles);
