@@ -80,3 +80,24 @@ def test_closed_forms_of_the_full_workloads():
     assert nbytes == 4 * 2 * 8 * 32 * 64 * 4  # 512 KiB
     assert bench.algorithmic(w["long_causal_bf16_b4_h16_l8192_d128"], None)[1] == \
         pytest.approx(1.0996e12, rel=1e-4)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_backward_flops_are_five_products_per_allowed_pair(case):
+    # scores recomputed (2 d_k), dP (2 d_v), dV (2 d_v), dK (2 d_k), dQ (2 d_k)
+    B, H, Hkv, Lq, Lk, d, dtype, mask, lens = case
+    spec = dict(B=B, H=H, Hkv=Hkv, Lq=Lq, Lk=Lk, dk=d, dv=d, dtype=dtype, mask=mask)
+    lens_a = None if lens is None else np.asarray(lens, dtype=np.int32)
+    _, fwd = brute(spec, lens_a)
+    pairs = fwd // (2 * (d + d))
+    assert bench.backward_flops(spec, lens_a) == pairs * 2 * (3 * d + 2 * d)
+
+
+def test_projection_kernel_name_follows_the_tiling_rule():
+    # 128 x 256 tiles when K and N are multiples of 64 and N >= 256
+    assert bench.linear_kernel_name(512, 512) == "linear_wide_kernel"
+    assert bench.linear_kernel_name(512, 256) == "linear_wide_kernel"
+    assert bench.linear_kernel_name(512, 192) == "linear_tc_kernel"
+    assert bench.linear_kernel_name(200, 512) == "linear_tc_kernel"
+    assert bench.linear_kernel_name(512, 320) == "linear_wide_kernel"
+    assert bench.linear_kernel_name(512, 72) == "linear_tc_kernel"
