@@ -995,6 +995,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 // -- a global load at the point of use stalled the softmax for microseconds.
 // K and V of the next unit and Q and dout of the next head load while the
 // current one computes.  TMEM: S | dP | dQ | dV | dK (448 columns).
+// With the caller's row statistics (the forward's lse; kGiven, taken when the
+// mask is not causal) the weights come straight from them, w = 2^(s scale
+// log2(e) - lse), one 32-key chunk at a time, and a second warpgroup (warps
+// 6-9) stores dQ, dV and dK, so the softmax warpgroup only forms w and dS.
+// Otherwise the softmax warpgroup keeps its row of S in registers for the
+// statistics and also stores.
 struct ShortBwdBars {
   uint64_t kv_full[2], kv_empty[2];  // K, V of a unit (by unit parity)
   uint64_t qd_full[2], qd_empty[2];  // Q, dout of a head (by iteration parity)
@@ -1016,6 +1022,9 @@ constexpr int kSbStage = 32 * 64;  // one softmax warp's 32 half-rows of output
 // the rows of out, the softmax warps' output staging
 constexpr size_t kSbSmem = 1024 + 13 * static_cast<size_t>(kSbTile) + 4 * kSbStage + 512;
 constexpr uint32_t kSbS = 0, kSbDp = 128, kSbDq = 256, kSbDv = 320, kSbDk = 384;
+// with the caller's statistics: softmax warpgroup (warps 0-3), producer (4),
+// MMA issuer (5), stores (6-9)
+constexpr int kSbThreadsGiven = 320;
 
 // byte offset of 16-byte piece c (0..15: keys 8c .. 8c + 7) of row r in a
 // [128 x 128] bf16 tile stored as two 128-byte-swizzled 64-key slabs
@@ -1040,7 +1049,44 @@ __device__ __forceinline__ float dot_bf16x8(const uint4 &a, const uint4 &b) {
   return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// w = 2^(s scale_log2 - lse) and dS = w (dP - D) over 32 key columns of the
+// calling thread's row, packed to bf16 pairs: columns c in [lo, hi) are
+// allowed, the others weigh 0.  A chunk the whole warp may read takes packed
+// fp32 pairs, no mask.
+__device__ __forceinline__ void short_chunk(const uint32_t (&sv)[32], const uint32_t (&pv)[32],
+                                            int lo, int hi, float scale_log2, float lse, float dd,
+                                            uint32_t (&pw)[16], uint32_t (&pd)[16]) {
+  if (__all_sync(0xffffffffu, lo <= 0 && hi >= 32)) {
+    const uint64_t sc = f2_pack(scale_log2, scale_log2), nl = f2_pack(-lse, -lse);
+    const uint64_t d2 = f2_pack(dd, dd);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float x0, x1, g0, g1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc, nl),
+                x0, x1);
+      const float w0 = ex2_approx(x0), w1 = ex2_approx(x1);
+      f2_unpack(f2_mul(f2_pack(w0, w1),
+                       f2_sub(f2_pack(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), d2)),
+                g0, g1);
+      pw[e >> 1] = pack_bf16x2(w0, w1);
+      pd[e >> 1] = pack_bf16x2(g0, g1);
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float w0 =
+        e >= lo && e < hi ? ex2_approx(__uint_as_float(sv[e]) * scale_log2 - lse) : 0.f;
+    const float w1 =
+        e + 1 >= lo && e + 1 < hi ? ex2_approx(__uint_as_float(sv[e + 1]) * scale_log2 - lse) : 0.f;
+    pw[e >> 1] = pack_bf16x2(w0, w1);
+    pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                             w1 * (__uint_as_float(pv[e + 1]) - dd));
+  }
+}
+
+template <bool kGiven>
+__global__ void __launch_bounds__(kGiven ? kSbThreadsGiven : kThreads, 1)
     bwd_short_tc_kernel(const __grid_constant__ LongMaps maps, const Problem p, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1094,6 +1140,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   int kv_issued = 0, qd_issued = 0;
   bool mma_issued = false;
+
+  // ---- stores of dQ, dV, dK by a warp of the storing warpgroup: warp w
+  // reads TMEM lanes [32 (w mod 4), + 32), i.e. those tile rows ------------
+  const int quad = warp & 3;
+  const uint32_t lane_q = static_cast<uint32_t>(quad * 32) << 16;
+  const int rows_shift = __ffs(R) - 1;  // R is a power of two
+  const uint32_t so = smem_addr(stage_smem + quad * kSbStage);
+  // 32 TMEM columns of this thread's row (fp32) * f -> bf16 -> the warp's
+  // staging; then the warp writes its 32 half-rows, eight 64-byte pieces per
+  // store instruction.  dst(rr) is the global address of warp row rr's
+  // half-row (nullptr: not stored).
+  auto stage_store = [&](const uint32_t (&v)[32], float f, auto dst) {
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+      st_shared_v4(so + stage64(lane, c4),
+                   pack_bf16x2(__uint_as_float(v[8 * c4 + 0]) * f, __uint_as_float(v[8 * c4 + 1]) * f),
+                   pack_bf16x2(__uint_as_float(v[8 * c4 + 2]) * f, __uint_as_float(v[8 * c4 + 3]) * f),
+                   pack_bf16x2(__uint_as_float(v[8 * c4 + 4]) * f, __uint_as_float(v[8 * c4 + 5]) * f),
+                   pack_bf16x2(__uint_as_float(v[8 * c4 + 6]) * f, __uint_as_float(v[8 * c4 + 7]) * f));
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int rr = 8 * t + (lane >> 2);
+      const uint4 val = ld_shared_v4(so + stage64(rr, lane & 3));
+      uint16_t *g = dst(rr);
+      if (g != nullptr) st_global_v4(g + (lane & 3) * 8, val);
+    }
+    __syncwarp();
+  };
+  // dQ of iteration `it` (tile row: pair row >> rows_shift, query row & (R - 1))
+  auto store_dq = [&](int it) -> bool {
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag))) return false;
+    tc_fence_after();
+    const int ul = it / group, hl = it - ul * group;
+    const int u = static_cast<int>(blockIdx.x) + ul * G;
+    const int b = u / upb, hk0 = (u - b * upb) * P;
+    auto dst = [&](int ch) {
+      return [&, ch](int rr) -> uint16_t * {
+        const int row = quad * 32 + rr, pp = row >> rows_shift, i = row & (R - 1);
+        return hk0 + pp < p.Hkv && i < p.Lq
+                   ? static_cast<uint16_t *>(a.dq) +
+                         row_at(p.layout, b, (hk0 + pp) * group + hl, i, p.H, p.Lq, 64) + ch * 32
+                   : nullptr;
+      };
+    };
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_q + kSbDq + ch * 32, v);
+      tmem_wait_ld();
+      stage_store(v, a.scale, dst(ch));
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->dq_free);
+    return true;
+  };
+  // dV and dK of unit ul (tile row = key row: pair row >> rows_shift)
+  auto store_dkv = [&](int ul) -> bool {
+    const bool okd = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_full, ul & 1, abort_flag));
+    if (!named_barrier_and(1, kWg, okd)) return false;
+    tc_fence_after();
+    const int u = static_cast<int>(blockIdx.x) + ul * G;
+    const int b = u / upb, hk0 = (u % upb) * P;
+    // element offset of key row rr of this warp (or -1)
+    auto key_at = [&](int rr) -> long long {
+      const int row = quad * 32 + rr, pp = row >> rows_shift, j = row & (R - 1);
+      return hk0 + pp < p.Hkv && j < p.Lk
+                 ? static_cast<long long>(row_at(p.layout, b, hk0 + pp, j, p.Hkv, p.Lk, 64))
+                 : -1LL;
+    };
+    auto dst = [&](void *base, int ch) {
+      return [&, base, ch](int rr) -> uint16_t * {
+        const long long o = key_at(rr);
+        return o >= 0 ? static_cast<uint16_t *>(base) + o + ch * 32 : nullptr;
+      };
+    };
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_q + kSbDv + ch * 32, v);
+      tmem_wait_ld();
+      stage_store(v, 1.f, dst(a.dv, ch));
+      tmem_ld32(tmem + lane_q + kSbDk + ch * 32, v);
+      tmem_wait_ld();
+      stage_store(v, a.scale, dst(a.dk, ch));
+    }
+    tc_fence_before();
+    mbar_arrive(&bars->dkv_free);
+    return true;
+  };
 
   if (warp == 4) {
     // ---- producer: per unit K and V, then Q and dout of each query head ----
@@ -1197,9 +1333,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it + 1 < n_it && !(ok = scores(it + 1))) break;
       ok = grads(it);
     }
+  } else if (kGiven && warp >= 6) {
+    // ---- stores (with the caller's statistics): dQ of every head, then dV
+    // and dK of a finished unit
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      ok = store_dq(it);
+      if (ok && it % group == group - 1) ok = store_dkv(it / group);
+    }
   } else {
-    // ---- softmax: thread r = tile row r (pair r / R, query r % R); for dV and
-    // dK thread r = tile row r of the keys ----------------------------------
+    // ---- softmax: thread r = tile row r (pair r / R, query r % R); without
+    // the caller's statistics also the stores, thread r = tile row r of the
+    // queries (dQ) and of the keys (dV, dK) ----------------------------------
     const int r = threadIdx.x;
     const int pr = r / R, ri = r - pr * R;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -1246,78 +1391,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 8; ++c) cp_async16(orow + ((c ^ (r & 7)) << 4), src + 8 * c);
       cp_async_commit();
     };
-    const uint32_t so = smem_addr(stage_smem + warp * kSbStage);
-    // 32 TMEM columns of this thread's row (fp32) * f -> bf16 -> the warp's
-    // staging; then the warp writes its 32 half-rows, eight 64-byte pieces per
-    // store instruction.  dst(rr) is the global address of warp row rr's
-    // half-row (nullptr: not stored).
-    auto store_half = [&](uint32_t taddr, float f, auto dst) {
-      uint32_t v[32];
-      tmem_ld32(taddr, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-        st_shared_v4(so + stage64(lane, c4),
-                     pack_bf16x2(__uint_as_float(v[8 * c4 + 0]) * f, __uint_as_float(v[8 * c4 + 1]) * f),
-                     pack_bf16x2(__uint_as_float(v[8 * c4 + 2]) * f, __uint_as_float(v[8 * c4 + 3]) * f),
-                     pack_bf16x2(__uint_as_float(v[8 * c4 + 4]) * f, __uint_as_float(v[8 * c4 + 5]) * f),
-                     pack_bf16x2(__uint_as_float(v[8 * c4 + 6]) * f, __uint_as_float(v[8 * c4 + 7]) * f));
-      __syncwarp();
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int rr = 8 * t + (lane >> 2);
-        const uint4 val = ld_shared_v4(so + stage64(rr, lane & 3));
-        uint16_t *g = dst(rr);
-        if (g != nullptr) st_global_v4(g + (lane & 3) * 8, val);
-      }
-      __syncwarp();
-    };
-    // dQ of iteration `it` (thread r = row r) to global memory
-    auto store_dq = [&](int it) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->dq_full, it & 1, abort_flag))) return false;
-      tc_fence_after();
-      const Iter itr = iter_of(it);
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch)
-        store_half(tmem + lane_base + kSbDq + ch * 32, a.scale, [&](int rr) -> uint16_t * {
-          const RowAt x = row_of(itr, warp * 32 + rr);
-          return x.valid ? static_cast<uint16_t *>(a.dq) +
-                               row_at(p.layout, x.b, x.h, x.i, p.H, p.Lq, 64) + ch * 32
-                         : nullptr;
-        });
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      return true;
-    };
-    // dV and dK of unit ul (thread r = key row r: pair r / R, key r % R)
-    auto store_dkv = [&](int ul) -> bool {
-      const bool okd = __all_sync(0xffffffffu, mbar_wait(&bars->dkv_full, ul & 1, abort_flag));
-      if (!named_barrier_and(1, kWg, okd)) return false;
-      tc_fence_after();
-      const int u = static_cast<int>(blockIdx.x) + ul * G;
-      const int b = u / upb, hk0 = (u % upb) * P;
-      // element offset of key row rr of this warp (or -1)
-      auto key_at = [&](int rr) -> long long {
-        const int row = warp * 32 + rr, pp = row >> r_shift, j = row & (R - 1);
-        return hk0 + pp < p.Hkv && j < p.Lk
-                   ? static_cast<long long>(row_at(p.layout, b, hk0 + pp, j, p.Hkv, p.Lk, 64))
-                   : -1LL;
-      };
-#pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        store_half(tmem + lane_base + kSbDv + ch * 32, 1.f, [&](int rr) -> uint16_t * {
-          const long long o = key_at(rr);
-          return o >= 0 ? static_cast<uint16_t *>(a.dv) + o + ch * 32 : nullptr;
-        });
-        store_half(tmem + lane_base + kSbDk + ch * 32, a.scale, [&](int rr) -> uint16_t * {
-          const long long o = key_at(rr);
-          return o >= 0 ? static_cast<uint16_t *>(a.dk) + o + ch * 32 : nullptr;
-        });
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->dkv_free);
-      return true;
-    };
     // D = dout . out of this thread's row: out from its cp.async row, dout
     // from the TMA tile of the iteration's stage (same 128-byte swizzle)
     auto row_dsum = [&](int it, bool valid) -> float {
@@ -1333,76 +1406,146 @@ __global__ void __launch_bounds__(kThreads, 1)
       return dd;
     };
 
-    bool ok = true;
-    if (n_it > 0) fetch_out(0);
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int ul = it / group, hl = it - ul * group;
-      const Iter itr = iter_of(it);
-      const RowAt x = row_of(itr, r);
-      const int len = clamp_len(p, x.b);
-      // allowed tile columns [lo, hi): the row's own pair, keys j < jmax
-      const int lo = pr * R;
-      const int hi = lo + (x.valid ? row_limit(p, len, ri) : 0);
-      // D of the row: dout's tile has landed (its phase cannot move on before
-      // this head's gradients are issued), out's row came by cp.async
-      if (!(ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->qd_full[it & 1], (it >> 1) & 1, abort_flag))))
-        break;
-      const float dd = row_dsum(it, x.valid);
-      if (it + 1 < n_it) fetch_out(it + 1);
-      // ---- the row's softmax over its allowed keys, dS over dP
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sd_full, it & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
-      tmem_wait_ld();
-      const bool need_mask = __any_sync(0xffffffffu, lo > 0 || hi < kT);
-      const bool pos = p.scale_log2 > 0.f;
-      const float m = pos ? mask_max128(sr, need_mask, lo, hi) * p.scale_log2
-                          : scale_mask_max128(sr, p.scale_log2, need_mask, lo, hi);
-      const float l = pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
-                          : exp2_sum128(sr, m, m != -INFINITY);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      // the previous head's dQ, and the previous unit's dV and dK
-      if (it >= 1 && !(ok = store_dq(it - 1))) break;
-      if (it >= 1 && hl == 0 && !(ok = store_dkv(ul - 1))) break;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pv[32], pw[16], pd[16];
-        tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
-        tmem_wait_ld();
-        if (ch == 3) {
-          // every read of S and dP is done: the next head's may go out
-          tc_fence_before();
-          mbar_arrive(&bars->sd_free);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float w0 = __uint_as_float(sr[ch][e]) * inv;
-          const float w1 = __uint_as_float(sr[ch][e + 1]) * inv;
-          pw[e >> 1] = pack_bf16x2(w0, w1);
-          pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
-                                   w1 * (__uint_as_float(pv[e + 1]) - dd));
-        }
-        // the previous head's gradient products have read w and dS
-        if (ch == 0 && it >= 1 &&
-            !(ok = __all_sync(0xffffffffu, mbar_wait(&bars->wd_free, (it - 1) & 1, abort_flag))))
+    if constexpr (kGiven) {
+      // the caller's log2 softmax denominator of the row at iteration `it`
+      // (loaded one iteration ahead)
+      auto lse_of = [&](int it) -> float {
+        const RowAt x = row_of(iter_of(it), r);
+        return x.valid ? a.lse[(static_cast<size_t>(x.b) * p.H + x.h) * p.Lq + x.i] : INFINITY;
+      };
+      float lse_next = n_it > 0 ? lse_of(0) : INFINITY;
+      bool ok = true;
+      if (n_it > 0) fetch_out(0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const Iter itr = iter_of(it);
+        const RowAt x = row_of(itr, r);
+        const int len = clamp_len(p, x.b);
+        // allowed tile columns [lo, hi): the row's own pair, keys j < jmax
+        const int lo = pr * R;
+        const int hi = lo + (x.valid ? row_limit(p, len, ri) : 0);
+        const float lse = lse_next;
+        if (it + 1 < n_it) lse_next = lse_of(it + 1);
+        // D of the row: dout's tile has landed (its phase cannot move on
+        // before this head's gradients are issued), out's row came by cp.async
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->qd_full[it & 1], (it >> 1) & 1, abort_flag))))
           break;
+        const float dd = row_dsum(it, x.valid);
+        if (it + 1 < n_it) fetch_out(it + 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sd_full, it & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t s_t = tmem + lane_base + kSbS, dp_t = tmem + lane_base + kSbDp;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t off = wd_offset(r, ch * 4 + t);
-          st_shared_v4(swr + off, pw[4 * t], pw[4 * t + 1], pw[4 * t + 2], pw[4 * t + 3]);
-          st_shared_v4(sdsr + off, pd[4 * t], pd[4 * t + 1], pd[4 * t + 2], pd[4 * t + 3]);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t sv[2][32], pv[2][32], pw[2][16], pd[2][16];
+          tmem_ld32(s_t + 64 * c2, sv[0]);
+          tmem_ld32(s_t + 64 * c2 + 32, sv[1]);
+          tmem_ld32(dp_t + 64 * c2, pv[0]);
+          tmem_ld32(dp_t + 64 * c2 + 32, pv[1]);
+          tmem_wait_ld();
+          if (c2 == 1) {
+            // every read of S and dP is done: the next head's may go out
+            tc_fence_before();
+            mbar_arrive(&bars->sd_free);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            short_chunk(sv[cc], pv[cc], lo - 32 * (2 * c2 + cc), hi - 32 * (2 * c2 + cc),
+                        p.scale_log2, lse, dd, pw[cc], pd[cc]);
+          // the previous head's gradient products have read w and dS
+          if (c2 == 0 && it >= 1 &&
+              !(ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars->wd_free, (it - 1) & 1, abort_flag))))
+            break;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const uint32_t off = wd_offset(r, (2 * c2 + cc) * 4 + t);
+              st_shared_v4(swr + off, pw[cc][4 * t], pw[cc][4 * t + 1], pw[cc][4 * t + 2],
+                           pw[cc][4 * t + 3]);
+              st_shared_v4(sdsr + off, pd[cc][4 * t], pd[cc][4 * t + 1], pd[cc][4 * t + 2],
+                           pd[cc][4 * t + 3]);
+            }
         }
+        if (!ok) break;
+        // generic-proxy stores, read by the tensor core (async proxy)
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->wd_full);
       }
-      if (!ok) break;
-      // generic-proxy stores, read by the tensor core (async proxy)
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->wd_full);
+    } else {
+      bool ok = true;
+      if (n_it > 0) fetch_out(0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int ul = it / group, hl = it - ul * group;
+        const Iter itr = iter_of(it);
+        const RowAt x = row_of(itr, r);
+        const int len = clamp_len(p, x.b);
+        // allowed tile columns [lo, hi): the row's own pair, keys j < jmax
+        const int lo = pr * R;
+        const int hi = lo + (x.valid ? row_limit(p, len, ri) : 0);
+        // D of the row: dout's tile has landed (its phase cannot move on before
+        // this head's gradients are issued), out's row came by cp.async
+        if (!(ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->qd_full[it & 1], (it >> 1) & 1, abort_flag))))
+          break;
+        const float dd = row_dsum(it, x.valid);
+        if (it + 1 < n_it) fetch_out(it + 1);
+        // ---- the row's softmax over its allowed keys, dS over dP
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sd_full, it & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(tmem + lane_base + kSbS + ch * 32, sr[ch]);
+        tmem_wait_ld();
+        const bool need_mask = __any_sync(0xffffffffu, lo > 0 || hi < kT);
+        const bool pos = p.scale_log2 > 0.f;
+        const float m = pos ? mask_max128(sr, need_mask, lo, hi) * p.scale_log2
+                            : scale_mask_max128(sr, p.scale_log2, need_mask, lo, hi);
+        const float l = pos ? exp2_fma_sum128(sr, p.scale_log2, m, m != -INFINITY)
+                            : exp2_sum128(sr, m, m != -INFINITY);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // the previous head's dQ, and the previous unit's dV and dK
+        if (it >= 1 && !(ok = store_dq(it - 1))) break;
+        if (it >= 1 && hl == 0 && !(ok = store_dkv(ul - 1))) break;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pv[32], pw[16], pd[16];
+          tmem_ld32(tmem + lane_base + kSbDp + ch * 32, pv);
+          tmem_wait_ld();
+          if (ch == 3) {
+            // every read of S and dP is done: the next head's may go out
+            tc_fence_before();
+            mbar_arrive(&bars->sd_free);
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float w0 = __uint_as_float(sr[ch][e]) * inv;
+            const float w1 = __uint_as_float(sr[ch][e + 1]) * inv;
+            pw[e >> 1] = pack_bf16x2(w0, w1);
+            pd[e >> 1] = pack_bf16x2(w0 * (__uint_as_float(pv[e]) - dd),
+                                     w1 * (__uint_as_float(pv[e + 1]) - dd));
+          }
+          // the previous head's gradient products have read w and dS
+          if (ch == 0 && it >= 1 &&
+              !(ok = __all_sync(0xffffffffu, mbar_wait(&bars->wd_free, (it - 1) & 1, abort_flag))))
+            break;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t off = wd_offset(r, ch * 4 + t);
+            st_shared_v4(swr + off, pw[4 * t], pw[4 * t + 1], pw[4 * t + 2], pw[4 * t + 3]);
+            st_shared_v4(sdsr + off, pd[4 * t], pd[4 * t + 1], pd[4 * t + 2], pd[4 * t + 3]);
+          }
+        }
+        if (!ok) break;
+        // generic-proxy stores, read by the tensor core (async proxy)
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->wd_full);
+      }
+      if (ok && n_it > 0) ok = store_dq(n_it - 1) && store_dkv(n_local - 1);
     }
-    if (ok && n_it > 0) ok = store_dq(n_it - 1) && store_dkv(n_local - 1);
   }
 
   if (*abort_flag && warp == 4 && lane == 0) {
@@ -1503,8 +1646,15 @@ cudaError_t launch_bwd_tc(const LongMaps &maps, const Problem &p, const BwdArgs 
   if (p.Lq <= kT && p.Lk <= kT) {
     // one tile each way: the fused persistent kernel (no statistics pass)
     const long long units = static_cast<long long>(p.B) * ((p.Hkv + a.pack - 1) / a.pack);
-    return launch_one(bwd_short_tc_kernel, kSbSmem, units < num_sms ? units : num_sms, maps, p,
-                      a, stream);
+    const long long grid = units < num_sms ? units : num_sms;
+    // the storing warpgroup pays where a row's softmax is heavy; under a
+    // causal mask half of the keys are masked and the softmax warpgroup is
+    // quicker doing its own stores (about 10% faster and 2% slower
+    // respectively, measured on GB300)
+    if (have_lse && !(p.mask & kMaskCausal))
+      return launch_one(bwd_short_tc_kernel<true>, kSbSmem, grid, maps, p, a, stream,
+                        kSbThreadsGiven);
+    return launch_one(bwd_short_tc_kernel<false>, kSbSmem, grid, maps, p, a, stream);
   }
   return launch_bwd_tc_impl<64>(maps, p, a, stream, have_lse);
 }
