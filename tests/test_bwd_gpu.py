@@ -134,6 +134,9 @@ CASES = [
     spec(2, 16, 8, 8, 64, mask=C),
     spec(2, 3, 50, 33, 64, mask=KP, len_range=(1, 33), layout="bshd"),
     spec(4, 8, 64, 64, 64, mask=KP | QP, len_range=(8, 64), layout="bshd"),
+    # single-tile decoding against a short padded cache; no mask (pairs packed)
+    spec(2, 4, 16, 100, 64, mask=TAIL | KP, len_range=(20, 100)),
+    spec(3, 4, 40, 40, 64),
     # several query and key tiles with shared key/value heads
     spec(2, 4, 640, 640, 128, mask=C, amp=0.5, Hkv=2, layout="bshd"),
     spec(2, 6, 333, 555, 64, mask=KP, len_range=(100, 555), Hkv=3),
