@@ -157,6 +157,18 @@ def kernel_source_digest(kernel=None):
     return h.hexdigest()[:16]
 
 
+def bwd_kernel_names(dk, Lq, Lk, mask):
+    """(kernels, traffic kernel) of one backward call given the forward's row
+    statistics: the fused single-tile kernel for d 64 and lengths <= 128 (its
+    storing form <1> unless the mask is causal), else the D pass, dq and
+    dk/dv kernels."""
+    if dk == 64 and Lq <= 128 and Lk <= 128:
+        form = "bwd_short_tc_kernel<%d>" % (0 if mask & gen.MASK_CAUSAL else 1)
+        return form + " (one launch)", form
+    return ("bwd_dsum_kernel + bwd_dq_tc_kernel + bwd_dkdv_tc_kernel (one mha_bwd_lse call, "
+            "3 launches)", "bwd_dkdv_tc_kernel (the largest share of the call)")
+
+
 def linear_kernel_name(K, N):
     """The projection kernel mha_linear_fwd runs for x [M, K] W [K, N]: 128 x 256
     tiles when K and N are multiples of 64 and N >= 256, else 128 x 128."""
@@ -1135,14 +1147,11 @@ def run_backward(args):
     # the bf16 tensor peak; the ncu launch list splits its time by kernel
     peaks, peak_src = read_peaks()
     achieved = flops / per_step / 1e12
+    kernels, traffic_kernel = bwd_kernel_names(dk, Lq, Lk, mask)
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": recorded_traffic(args.workload),
-                "traffic_kernel": "bwd_short_tc_kernel" if spec["dk"] == 64 and Lq <= 128 and
-                                  Lk <= 128 else "bwd_dkdv_tc_kernel (the largest share of the call)",
-                "kernel": "bwd_short_tc_kernel (one launch)" if spec["dk"] == 64 and Lq <= 128
-                          and Lk <= 128 else "bwd_dsum_kernel + bwd_dq_tc_kernel + "
-                          "bwd_dkdv_tc_kernel (one mha_bwd_lse call, 3 launches)",
+                "traffic": recorded_traffic(args.workload), "traffic_kernel": traffic_kernel,
+                "kernel": kernels,
                 "peak_source": peak_src + " (MEASURED_PEAKS.json)" if peak_src == "measured"
                 else "fallback", "algorithmic_flops": flops}
 

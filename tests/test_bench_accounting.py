@@ -101,3 +101,27 @@ def test_projection_kernel_name_follows_the_tiling_rule():
     assert bench.linear_kernel_name(200, 512) == "linear_tc_kernel"
     assert bench.linear_kernel_name(512, 320) == "linear_wide_kernel"
     assert bench.linear_kernel_name(512, 72) == "linear_tc_kernel"
+
+
+def test_backward_kernel_names_follow_the_dispatch_rule():
+    # the fused single-tile kernel (d 64, lengths <= 128): its storing form
+    # <1> with the forward's statistics unless the mask is causal
+    C, KP, TAIL = gen.MASK_CAUSAL, gen.MASK_KEY_PADDING, gen.MASK_CAUSAL_TAIL
+    assert bench.bwd_kernel_names(64, 128, 128, C)[1] == "bwd_short_tc_kernel<0>"
+    assert bench.bwd_kernel_names(64, 96, 128, KP)[1] == "bwd_short_tc_kernel<1>"
+    assert bench.bwd_kernel_names(64, 16, 100, TAIL | KP)[1] == "bwd_short_tc_kernel<1>"
+    assert bench.bwd_kernel_names(64, 64, 64, 0)[0] == "bwd_short_tc_kernel<1> (one launch)"
+    for dk, Lq, Lk in ((128, 128, 128), (64, 129, 128), (64, 128, 8192)):
+        assert bench.bwd_kernel_names(dk, Lq, Lk, C)[1].startswith("bwd_dkdv_tc_kernel")
+    # the committed traffic record of each backward workload was taken on the
+    # kernel that the bench's timed calls run
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    for w, fwd in bench.BWD_WORKLOADS.items():
+        s = gen.WORKLOADS[fwd]
+        want = bench.bwd_kernel_names(s["dk"], s["Lq"], s["Lk"], s["mask"])[1].split(" ")[0]
+        if w in records:
+            got = records[w]["kernel_name"]
+            assert got == want or got.startswith(want + "<"), (w, got, want)
